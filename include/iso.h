@@ -1,0 +1,226 @@
+/*
+ * iso.h -- C ABI of the parallelism-invariant GEMM / RMSNorm / MoE / selected-
+ * token logprob library for NVIDIA GB300 (sm_103a).
+ *
+ * Promise: for a fixed library build and contract digest, every output row's
+ * bits are a function of that row's inputs, the weights and the contract
+ * only -- not of the batch size, the row's position in the batch, how K is
+ * split across (simulated) tensor-parallel ranks, or how experts are split
+ * across (simulated) expert-parallel partitions.
+ *   [IsoExec: Unified Execution to Eliminate Trainer-Inference Mismatch in
+ *    SkyRL, "Unified execution contract", "Parallelism-invariant kernels"]
+ *   [VeXact paper "Diagnosing Training Inference Mismatch in LLM RL", §3.1:
+ *    batch-invariant kernels fix tiling and reduction order]
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as uint16_t bit patterns (iso_bf16).
+ *   - Matrices are row-major with an explicit leading dimension in elements.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains device memory.  Scratch space comes
+ *     from the caller through the *_workspace() size queries.  The library
+ *     owns only the host-side contract object.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on that stream and performs no implicit device sync.
+ *   - Errors: every call returns an iso_status; arguments are validated on the
+ *     host before anything is launched, and an invalid call launches nothing.
+ *     No exception or abort crosses the ABI.  Faults detected on the device
+ *     (a bounded wait that ran out of time, a token id outside [0, V)) set a
+ *     per-device status word that iso_last_device_status() reads and clears.
+ *   - Alignment: device pointers 16-byte aligned; leading dimensions of bf16
+ *     matrices multiples of 8 elements, of fp32 matrices multiples of 4.
+ */
+#ifndef ISO_H_
+#define ISO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ISO_OK = 0,
+  ISO_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+  ISO_ERR_SHAPE = 2,             /* shape outside the contract (e.g. K % (16 L) != 0) */
+  ISO_ERR_ALIGNMENT = 3,         /* pointer / leading dimension alignment */
+  ISO_ERR_UNPROVEN_TOPOLOGY = 4, /* rank count not a power of two dividing L */
+  ISO_ERR_UNSUPPORTED = 5,       /* valid, but not supported by this build */
+  ISO_ERR_CONTRACT_MISMATCH = 6, /* peer digest differs */
+  ISO_ERR_WORKSPACE = 7,         /* workspace / buffer too small */
+  ISO_ERR_CUDA = 8,              /* a CUDA runtime call failed */
+  ISO_ERR_DEVICE_TIMEOUT = 9,    /* a device-side wait ran out of time */
+  ISO_ERR_NOT_IMPLEMENTED = 10,
+  ISO_ERR_BAD_TOKEN_ID = 11      /* a token id outside [0, V) reached the device */
+} iso_status;
+
+typedef enum { ISO_TREE_BALANCED_BINARY = 0 } iso_tree_schedule;
+typedef enum { ISO_F32 = 0, ISO_BF16 = 1 } iso_dtype;
+typedef struct iso_contract iso_contract; /* opaque, immutable after init, thread-safe to share */
+typedef uint16_t iso_bf16;                /* bf16 bit pattern */
+typedef void* iso_stream;                 /* cudaStream_t */
+
+/* ------------------------------------------------------------------ contract
+ * [IsoExec blog, "Unified execution contract": composition constants, claims,
+ *  identities (SHA-256 digests of the serialized contract)]
+ *
+ * iso_contract_init: leaf_count = number of contiguous K-leaves (a power of
+ * two, 1..8 in this build); schedule must be ISO_TREE_BALANCED_BINARY;
+ * acc_dtype must be ISO_F32; out_dtype must be ISO_BF16.  On success *out
+ * receives a new contract (free with iso_contract_destroy) and digest (if not
+ * NULL) the 32-byte SHA-256 of its canonical serialization, which covers every
+ * constant that can change an output bit.  Errors: ISO_ERR_INVALID_ARG (bad
+ * leaf count / NULL out), ISO_ERR_UNSUPPORTED (valid but not built). */
+iso_status iso_contract_init(int leaf_count, iso_tree_schedule schedule, iso_dtype acc_dtype,
+                             iso_dtype out_dtype, iso_contract** out, uint8_t digest[32]);
+void iso_contract_destroy(iso_contract* c);
+/* Canonical serialization (UTF-8 JSON, fixed field order, no whitespace).
+ * *len receives the length without the terminating NUL; buf may be NULL to
+ * query.  ISO_ERR_WORKSPACE if cap < len + 1. */
+iso_status iso_contract_serialize(const iso_contract* c, char* buf, size_t cap, size_t* len);
+iso_status iso_contract_digest(const iso_contract* c, uint8_t digest[32]);
+/* Digest agreement between trainer and rollout engine: ISO_OK if equal, else
+ * ISO_ERR_CONTRACT_MISMATCH (the caller must refuse to run).
+ * [NovaSky IsoExec article, "The execution contract": runtimes exchange
+ *  digests and refuse to run on disagreement] */
+iso_status iso_contract_check_peer(const iso_contract* c, const uint8_t peer_digest[32]);
+/* Topology claim: ISO_OK if num_ranks is a power of two dividing the leaf
+ * count (the sizes for which the tree is proven invariant), else
+ * ISO_ERR_UNPROVEN_TOPOLOGY.  [IsoExec blog, "Unified execution contract":
+ *  the adapter rejects unproven parallel sizes] */
+iso_status iso_contract_check_topology(const iso_contract* c, int num_ranks);
+int iso_contract_leaf_count(const iso_contract* c);
+/* FIPS 180-4 SHA-256 of n host bytes (the digest routine the contract uses). */
+iso_status iso_sha256(const void* data, size_t n, uint8_t digest[32]);
+const char* iso_status_string(iso_status s);
+/* Synchronizes `stream`, then reads and clears the current device's status
+ * word: ISO_OK, ISO_ERR_DEVICE_TIMEOUT or ISO_ERR_BAD_TOKEN_ID. */
+iso_status iso_last_device_status(iso_stream stream);
+
+/* ---------------------------------------------------------------- iso_gemm
+ * C[M x N] = bf16_rn( tree_{l=0..L-1} P_l ),  P_l = sum over leaf l of A*B.
+ * [IsoExec blog, "Parallelism-invariant kernels": K divided into contiguous
+ *  leaves, each a deterministic tensor-core MMA chain with FP32
+ *  accumulation, combined by the contract's binary arithmetic schedule]
+ * [RL-Kernel blog, §2 "Four Common Trigger Points" and §7 "GEMM": FP32
+ *  accumulation, one conversion to BF16 at a fixed point]
+ * A: [M x K] bf16 row-major, lda >= K.  B: [K x N] bf16 row-major, ldb >= N.
+ * C: [M x N] bf16 row-major, ldc >= N.  L = contract leaf count; leaf l covers
+ * k in [l K/L, (l+1) K/L).  Requires K % (16 L) == 0 (ISO_ERR_SHAPE),
+ * N % 8 == 0 (ISO_ERR_SHAPE), lda/ldb/ldc % 8 == 0 and 16-byte aligned
+ * pointers (ISO_ERR_ALIGNMENT).  M == 0 is a no-op. */
+iso_status iso_gemm(const iso_contract* c, const iso_bf16* A, int64_t lda, const iso_bf16* B, int64_t ldb,
+                    iso_bf16* C, int64_t ldc, int M, int N, int K, iso_stream stream);
+
+/* ------------------------------------------------- simulated tensor parallel
+ * iso_gemm_leaf_partial: rank `rank` of `num_ranks` owns the contiguous leaves
+ * [rank L/R, (rank+1) L/R) (rank-to-leaf map fixed by the contract) and
+ * writes the fp32 root of its subtree: S_r[M x N] (lds >= N, lds % 4 == 0).
+ * A_r: [M x K_local] (this rank's K slice), B_r: [K_local x N].  R must be a
+ * power of two dividing L (ISO_ERR_UNPROVEN_TOPOLOGY); K_local % (16 L/R) == 0.
+ * iso_tree_combine: applies the top log2(R) levels of the same tree to
+ * S[r] = S + r * rank_stride (fp32 [M x lds] each) and writes C = bf16_rn(root).
+ * The pair reproduces iso_gemm bit for bit for every R.
+ * [IsoExec blog, "Parallelism-invariant kernels": NCCL only transports the
+ *  partial results]; [RL-Kernel blog, §6 table row 06: the same fixed
+ *  balanced tree for TP1/2/4/8] */
+iso_status iso_gemm_leaf_partial(const iso_contract* c, int rank, int num_ranks, const iso_bf16* A_r, int64_t lda,
+                                 const iso_bf16* B_r, int64_t ldb, float* S_r, int64_t lds, int M, int N,
+                                 int K_local, iso_stream stream);
+iso_status iso_tree_combine(const iso_contract* c, int num_ranks, const float* S, int64_t lds,
+                            int64_t rank_stride, iso_bf16* C, int64_t ldc, int M, int N, iso_stream stream);
+
+/* -------------------------------------------------------------- iso_rmsnorm
+ * y[t, i] = bf16_rn( (x[t,i] * r_t) * gamma[i] ),  r_t = 1 / sqrt(mean_i x^2 + eps)
+ * with the per-row reduction of fixed shape (contract: one warp per row, lane
+ * l sums the 8-element vectors v = l mod 32 in ascending order, then an xor
+ * shuffle tree 16,8,4,2,1).
+ * [RL-Kernel blog, §4 table: RMSNorm reduces over the hidden dimension;
+ *  §6 table row 02]; [VeXact paper, §3.1: batch-invariant RMSNorm]
+ * x, y: [T x H] bf16 row-major (ld = H); gamma: [H] bf16.  H % 8 == 0. */
+iso_status iso_rmsnorm(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps, iso_bf16* y,
+                       int T, int H, iso_stream stream);
+
+/* ---------------------------------------------------- iso_selected_logprob
+ * out[t] = z[t, ids[t]] - LSE_v z[t, v],  z = h W as the fp32 tree root (never
+ * rounded).  LSE: per 128-column vocab tile (m = max, s = sum expf(z - m) over
+ * ascending columns), tiles folded left to right inside chunks of 19 tiles
+ * with the two-block merge m = max(m1,m2), s = s1 e^(m1-m) + s2 e^(m2-m),
+ * chunks combined by a balanced pairwise tree (odd node carried up),
+ * lse = m + logf(s).  Logits are never written to memory.
+ * [RL-Kernel blog, §4 "Focus: The Shared Dependency ... on LogSumExp",
+ *  "Causal Chain: How Block Merge Order Alters LSE"; §6 table row 05; §7
+ *  "LogP": local statistics merged in a fixed vocab-tile order]
+ * [VeXact paper, §2 Eq. (1): delta_t compares exactly these values]
+ * h: [T x H] bf16 row-major; W: [H x V] bf16 row-major (the LM head as K x N);
+ * ids: [T] int32; out: [T] fp32.  H % (16 L) == 0; V % 8 == 0; V <= 622592.
+ * ws: device workspace of at least iso_selected_logprob_workspace(c, T, V)
+ * bytes, 16-byte aligned (ISO_ERR_WORKSPACE otherwise).  A token id outside
+ * [0, V) yields out[t] = NaN and sets ISO_ERR_BAD_TOKEN_ID in the device
+ * status word. */
+size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V);
+iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
+                                float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream);
+
+/* --------------------------------------------------------------------- MoE
+ * [IsoExec blog, "Unified model": deterministic MoE routing and combination;
+ *  "Parallelism-invariant kernels": expert outputs combined in a fixed
+ *  routing order rather than rank order; "Unified execution contract":
+ *  moe.combine = leaf tree, 8 leaves, fp32 leaves]
+ * [RL-Kernel blog, §6 table row 04 and §7 "FFN": packed gate/up, SwiGLU and
+ *  down projection as separate fixed stages]
+ *
+ * iso_moe_route: logits [T x E] fp32 -> topk_ids [T x k] int32 (logit
+ * descending, ties to the lower expert id) and topk_w [T x k] fp32 =
+ * softmax over the k selected logits (denominator summed in slot order).
+ * E <= 256, 1 <= k <= min(E, 32). */
+iso_status iso_moe_route(const iso_contract* c, const float* logits, int T, int E, int k, int32_t* topk_ids,
+                         float* topk_w, iso_stream stream);
+/* Stable counting sort of the (token, slot) pairs p = t k + j by expert, over
+ * the experts e with expert_partition[e] == partition (expert_partition is a
+ * DEVICE array [E] int32; NULL selects every expert): perm lists pair indices
+ * grouped by expert, ascending p inside an expert; offsets[E+1] are the group
+ * boundaries (offsets[E] = number of listed pairs).  perm must hold T k
+ * entries; counts_ws is device scratch of 3 E + 2 int32.  Ids outside [0, E)
+ * set ISO_ERR_BAD_TOKEN_ID on the device.  E <= 256. */
+iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T, int E, int k,
+                           const int32_t* expert_partition, int partition, int32_t* perm, int32_t* offsets,
+                           int32_t* counts_ws, iso_stream stream);
+/* out[t] = bf16_rn( tree_{j=0..k-1} (w[t,j] * y[t,j]) ): products fp32 rn, the
+ * balanced binary tree over routing slots in slot order.  y_slots [T x k x H]
+ * bf16, topk_w [T x k] fp32, out [T x H] bf16.  k a power of two <= 8,
+ * H % 8 == 0. */
+iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const float* topk_w, iso_bf16* out,
+                           int T, int k, int H, iso_stream stream);
+/* The expert layer: for each partition p (experts with expert_partition[e] ==
+ * p; NULL = one partition): permute, gather, grouped gate/up leaf-tree GEMM
+ * (K = H) with G rounded to bf16, h = bf16_rn(silu(g) u), grouped down
+ * leaf-tree GEMM (K = F) rounded to bf16 into y_slots; then iso_moe_combine.
+ * The result does not depend on the partition map.
+ * x [T x H] bf16; topk_ids / topk_w as produced by iso_moe_route;
+ * W1 [E x H x 2F] bf16 (gate columns [0,F), up columns [F,2F));
+ * W2 [E x F x H] bf16; expert_partition: HOST array [E] int32 with values in
+ * [0, num_partitions) (NULL = a single partition); out [T x H] bf16.
+ * H % (16 L) == 0, F % (16 L) == 0, H % 128 == 0, F % 64 == 0, k a power of
+ * two <= 8, E <= 256.  ws: iso_grouped_gemm_moe_workspace(c, T, E, k, H, F)
+ * bytes. */
+size_t iso_grouped_gemm_moe_workspace(const iso_contract* c, int T, int E, int k, int H, int F);
+iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
+                                const float* topk_w, const iso_bf16* W1, const iso_bf16* W2,
+                                const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
+                                int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream);
+
+/* --------------------------------------------------------- failure checks
+ * Launches one kernel whose only job is a bounded wait on an mbarrier that
+ * nothing ever completes; after timeout_ns it gives up, sets
+ * ISO_ERR_DEVICE_TIMEOUT in the status word and returns, leaving the context
+ * usable.  Exercises the same bounded-wait path every kernel uses.  No
+ * counterpart on the pages: the pages' runtimes refuse to run on a contract
+ * violation; this is the device-side half of that behaviour. */
+iso_status iso_selftest_bounded_wait(uint64_t timeout_ns, iso_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ISO_H_ */

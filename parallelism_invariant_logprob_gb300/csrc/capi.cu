@@ -1,0 +1,438 @@
+// capi.cu -- the C ABI: argument validation, TMA descriptors, launch order.
+// All compute runs in the kernels of gemm_tcgen05.cu and elementwise.cu.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "iso_elementwise.h"
+#include "iso_internal.h"
+
+// Per-device status word written by kernels (timeouts, bad token ids).
+static __device__ unsigned int g_iso_status_word;
+
+namespace iso {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+bool ensure_device_state() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return false;
+  if (g_status_ptr[d] && g_sm_count[d]) return true;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_iso_status_word) != cudaSuccess) return false;
+    g_status_ptr[d] = static_cast<unsigned int*>(p);
+  }
+  if (!g_sm_count[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return false;
+    g_sm_count[d] = n;
+  }
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+cudaStream_t S(iso_stream s) { return static_cast<cudaStream_t>(s); }
+
+int div_up(int a, int b) { return (a + b - 1) / b; }
+
+void trace(const char* what, int a, int b, int c, int d) {
+  if (trace_enabled()) fprintf(stderr, "[iso] %s %d %d %d %d\n", what, a, b, c, d);
+}
+
+}  // namespace
+
+unsigned int* device_status_ptr() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  return g_status_ptr[d];
+}
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices || !g_sm_count[d]) return 148;
+  return g_sm_count[d];
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* e = getenv("ISO_WAIT_TIMEOUT_NS");
+    uint64_t t = e ? strtoull(e, nullptr, 10) : 0;
+    return t ? t : 2000000000ull;
+  }();
+  return v;
+}
+
+bool trace_enabled() {
+  static bool v = [] {
+    const char* e = getenv("ISO_TRACE");
+    return e && e[0] == '1';
+  }();
+  return v;
+}
+
+iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                          uint32_t box_cols, uint32_t box_rows) {
+  if (!g_encode) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return ISO_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ISO_OK : ISO_ERR_CUDA;
+}
+
+namespace {
+
+GemmParams base_params(int M, int N, int K, int L) {
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = L;
+  p.leaf_len = K / L;
+  p.num_kb = div_up(K, BK);
+  p.m_blocks = div_up(M, BM);
+  p.n_blocks = div_up(N, BN);
+  p.group_m = 8;
+  p.status = device_status_ptr();
+  p.timeout_ns = wait_timeout_ns();
+  return p;
+}
+
+// Shared checks of a leaf-tree GEMM launch.
+iso_status check_gemm_args(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                           int ldc_mult, int M, int N, int K, int L) {
+  if (M < 0 || N <= 0 || K <= 0) return ISO_ERR_INVALID_ARG;
+  if (M > 0 && (!A || !B || !C)) return ISO_ERR_INVALID_ARG;
+  if (L > MAX_LEAVES) return ISO_ERR_UNSUPPORTED;
+  if (K % (UMMA_K * L) != 0) return ISO_ERR_SHAPE;
+  if (N % 8 != 0) return ISO_ERR_SHAPE;
+  if (lda < K || ldb < N || ldc < N) return ISO_ERR_INVALID_ARG;
+  if (lda % 8 || ldb % 8 || ldc % ldc_mult) return ISO_ERR_ALIGNMENT;
+  if (M > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(C))) return ISO_ERR_ALIGNMENT;
+  return ISO_OK;
+}
+
+iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M,
+                    int N, int K, int L, cudaStream_t s) {
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  CUtensorMap tA, tB;
+  iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, BM);
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
+  if (st != ISO_OK) return st;
+  GemmParams p = base_params(M, N, K, L);
+  p.unit_mode = UNIT_GEMM;
+  p.num_units = p.m_blocks * p.n_blocks;
+  p.out = C;
+  p.ldo = ldc;
+  const int grid = p.num_units < sm_count() ? p.num_units : sm_count();
+  trace(epi == EPI_BF16 ? "gemm" : "gemm_partial", M, N, K, L);
+  return launch_gemm(epi, tA, tB, p, grid, s);
+}
+
+}  // namespace
+
+}  // namespace iso
+
+using namespace iso;
+
+extern "C" {
+
+iso_status iso_last_device_status(iso_stream stream) {
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return ISO_ERR_CUDA;
+  unsigned int w = 0;
+  if (cudaMemcpy(&w, device_status_ptr(), sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return ISO_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(device_status_ptr(), &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ISO_ERR_CUDA;
+  if (w & kDevTimeout) return ISO_ERR_DEVICE_TIMEOUT;
+  if (w & kDevBadToken) return ISO_ERR_BAD_TOKEN_ID;
+  if (w) return ISO_ERR_SHAPE;
+  return ISO_OK;
+}
+
+iso_status iso_gemm(const iso_contract* c, const iso_bf16* A, int64_t lda, const iso_bf16* B, int64_t ldb,
+                    iso_bf16* C, int64_t ldc, int M, int N, int K, iso_stream stream) {
+  if (!c) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  iso_status st = check_gemm_args(A, lda, B, ldb, C, ldc, 8, M, N, K, L);
+  if (st != ISO_OK || M == 0) return st;
+  return run_gemm(EPI_BF16, A, lda, B, ldb, C, ldc, M, N, K, L, S(stream));
+}
+
+iso_status iso_gemm_leaf_partial(const iso_contract* c, int rank, int num_ranks, const iso_bf16* A_r, int64_t lda,
+                                 const iso_bf16* B_r, int64_t ldb, float* S_r, int64_t lds, int M, int N,
+                                 int K_local, iso_stream stream) {
+  if (!c) return ISO_ERR_INVALID_ARG;
+  iso_status st = iso_contract_check_topology(c, num_ranks);
+  if (st != ISO_OK) return st;
+  if (rank < 0 || rank >= num_ranks) return ISO_ERR_INVALID_ARG;
+  const int Lr = iso_contract_leaf_count(c) / num_ranks;
+  st = check_gemm_args(A_r, lda, B_r, ldb, S_r, lds, 4, M, N, K_local, Lr);
+  if (st != ISO_OK || M == 0) return st;
+  return run_gemm(EPI_F32, A_r, lda, B_r, ldb, S_r, lds, M, N, K_local, Lr, S(stream));
+}
+
+iso_status iso_tree_combine(const iso_contract* c, int num_ranks, const float* Sp, int64_t lds, int64_t rank_stride,
+                            iso_bf16* C, int64_t ldc, int M, int N, iso_stream stream) {
+  if (!c) return ISO_ERR_INVALID_ARG;
+  iso_status st = iso_contract_check_topology(c, num_ranks);
+  if (st != ISO_OK) return st;
+  if (M < 0 || N <= 0) return ISO_ERR_INVALID_ARG;
+  if (M == 0) return ISO_OK;
+  if (!Sp || !C) return ISO_ERR_INVALID_ARG;
+  if (N % 8 != 0) return ISO_ERR_SHAPE;
+  if (lds < N || ldc < N || (num_ranks > 1 && rank_stride < static_cast<int64_t>(M) * lds)) return ISO_ERR_INVALID_ARG;
+  if (lds % 4 || rank_stride % 4 || ldc % 8 || !aligned16(Sp) || !aligned16(C)) return ISO_ERR_ALIGNMENT;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  return launch_tree_combine(Sp, lds, rank_stride, num_ranks, C, ldc, M, N, S(stream)) == cudaSuccess ? ISO_OK
+                                                                                                     : ISO_ERR_CUDA;
+}
+
+iso_status iso_rmsnorm(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps, iso_bf16* y,
+                       int T, int H, iso_stream stream) {
+  if (!c || T < 0 || H <= 0) return ISO_ERR_INVALID_ARG;
+  if (T == 0) return ISO_OK;
+  if (!x || !gamma || !y) return ISO_ERR_INVALID_ARG;
+  if (H % 8 != 0) return ISO_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(y)) return ISO_ERR_ALIGNMENT;
+  if (!(eps >= 0.0f)) return ISO_ERR_INVALID_ARG;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  trace("rmsnorm", T, H, 0, 0);
+  return launch_rmsnorm(x, gamma, eps, y, T, H, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+static int lp_num_chunks(int V) { return div_up(div_up(V, LP_TILE_COLS), LP_CHUNK_TILES); }
+
+static size_t lp_stats_bytes(int T, int V) {
+  return ((static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)) + 255) & ~size_t(255);
+}
+
+size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V) {
+  if (!c || T < 0 || V <= 0) return 0;
+  return lp_stats_bytes(T, V) + ((static_cast<size_t>(T) * sizeof(float) + 255) & ~size_t(255));
+}
+
+iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
+                                float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream) {
+  if (!c || T < 0 || H <= 0 || V <= 0) return ISO_ERR_INVALID_ARG;
+  if (T == 0) return ISO_OK;
+  if (!h || !W || !ids || !out || !ws) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  if (H % (UMMA_K * L) != 0) return ISO_ERR_SHAPE;
+  if (V % 8 != 0 || lp_num_chunks(V) > 256) return ISO_ERR_SHAPE;
+  if (H % 8 != 0) return ISO_ERR_ALIGNMENT;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
+  if (ws_bytes < iso_selected_logprob_workspace(c, T, V)) return ISO_ERR_WORKSPACE;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  CUtensorMap tA, tB;
+  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, BM);
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, W, H, V, V, 64, BK);
+  if (st != ISO_OK) return st;
+  float2* stats = static_cast<float2*>(ws);
+  float* zsel = reinterpret_cast<float*>(static_cast<char*>(ws) + lp_stats_bytes(T, V));
+  GemmParams p = base_params(T, V, H, L);
+  p.unit_mode = UNIT_LOGPROB;
+  p.chunk_tiles = LP_CHUNK_TILES;
+  p.num_chunks = lp_num_chunks(V);
+  p.num_units = p.m_blocks * p.num_chunks;
+  p.ids = ids;
+  p.ws_stats = stats;
+  p.ws_zsel = zsel;
+  p.V = V;
+  const int grid = p.num_units < sm_count() ? p.num_units : sm_count();
+  trace("selected_logprob", T, H, V, p.num_chunks);
+  st = launch_gemm(EPI_LOGPROB, tA, tB, p, grid, S(stream));
+  if (st != ISO_OK) return st;
+  return launch_lse_finalize(stats, zsel, ids, out, T, p.num_chunks, V, S(stream)) == cudaSuccess ? ISO_OK
+                                                                                                   : ISO_ERR_CUDA;
+}
+
+iso_status iso_moe_route(const iso_contract* c, const float* logits, int T, int E, int k, int32_t* topk_ids,
+                         float* topk_w, iso_stream stream) {
+  if (!c || T < 0 || E <= 0 || k <= 0) return ISO_ERR_INVALID_ARG;
+  if (E > 256 || k > E || k > 32) return ISO_ERR_UNSUPPORTED;
+  if (T == 0) return ISO_OK;
+  if (!logits || !topk_ids || !topk_w) return ISO_ERR_INVALID_ARG;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  return launch_moe_route(logits, T, E, k, topk_ids, topk_w, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T, int E, int k,
+                           const int32_t* expert_partition, int partition, int32_t* perm, int32_t* offsets,
+                           int32_t* counts_ws, iso_stream stream) {
+  if (!c || T < 0 || E <= 0 || k <= 0 || E > 256) return ISO_ERR_INVALID_ARG;
+  if (!topk_ids || !perm || !offsets || !counts_ws) return ISO_ERR_INVALID_ARG;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  // unit prefixes are not needed by a caller of the plain permutation: write them over counts_ws + E.
+  int32_t* up = counts_ws + E;
+  int32_t* dn = up + (E + 1);
+  return launch_moe_permute(topk_ids, static_cast<int64_t>(T) * k, E, expert_partition, partition, counts_ws, perm,
+                            offsets, up, 1, dn, 1, S(stream)) == cudaSuccess
+             ? ISO_OK
+             : ISO_ERR_CUDA;
+}
+
+iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const float* topk_w, iso_bf16* out, int T,
+                           int k, int H, iso_stream stream) {
+  if (!c || T < 0 || H <= 0 || k <= 0) return ISO_ERR_INVALID_ARG;
+  if (!is_pow2(k) || k > 8) return ISO_ERR_UNSUPPORTED;
+  if (T == 0) return ISO_OK;
+  if (!y_slots || !topk_w || !out) return ISO_ERR_INVALID_ARG;
+  if (H % 8 != 0) return ISO_ERR_SHAPE;
+  if (!aligned16(y_slots) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  return launch_moe_combine(y_slots, topk_w, T, k, H, out, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+// Workspace layout of the expert layer (each region 256-byte aligned):
+//   y_slots [P x H] bf16 | x_perm [P x H] bf16 | G [P x 2F] bf16 | h [P x F] bf16 |
+//   perm [P] | offsets [E+1] | counts [E] | up_prefix [E+1] | down_prefix [E+1] | part_map [E]
+namespace {
+struct MoeWs {
+  size_t y, xp, G, h, perm, offs, counts, up, dn, part, total;
+};
+size_t al(size_t x) { return (x + 255) & ~size_t(255); }
+MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
+  const size_t P = static_cast<size_t>(T) * k;
+  MoeWs w;
+  size_t o = 0;
+  w.y = o; o += al(P * H * 2);
+  w.xp = o; o += al(P * H * 2);
+  w.G = o; o += al(P * 2 * F * 2);
+  w.h = o; o += al(P * F * 2);
+  w.perm = o; o += al(P * 4);
+  w.offs = o; o += al((E + 1) * 4);
+  w.counts = o; o += al(E * 4);
+  w.up = o; o += al((E + 1) * 4);
+  w.dn = o; o += al((E + 1) * 4);
+  w.part = o; o += al(E * 4);
+  w.total = o;
+  return w;
+}
+}  // namespace
+
+size_t iso_grouped_gemm_moe_workspace(const iso_contract* c, int T, int E, int k, int H, int F) {
+  if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return 0;
+  return moe_ws_layout(T, E, k, H, F).total;
+}
+
+iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
+                                const float* topk_w, const iso_bf16* W1, const iso_bf16* W2,
+                                const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
+                                int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream) {
+  if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return ISO_ERR_INVALID_ARG;
+  if (E > 256 || !is_pow2(k) || k > 8) return ISO_ERR_UNSUPPORTED;
+  if (T == 0) return ISO_OK;
+  if (!x || !topk_ids || !topk_w || !W1 || !W2 || !out || !ws) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  if (H % (UMMA_K * L) || F % (UMMA_K * L) || H % BN || F % 64) return ISO_ERR_SHAPE;
+  if (expert_partition) {
+    if (num_partitions <= 0) return ISO_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e)
+      if (expert_partition[e] < 0 || expert_partition[e] >= num_partitions) return ISO_ERR_INVALID_ARG;
+  } else {
+    num_partitions = 1;
+  }
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) || !aligned16(ws)) return ISO_ERR_ALIGNMENT;
+  const MoeWs lay = moe_ws_layout(T, E, k, H, F);
+  if (ws_bytes < lay.total) return ISO_ERR_WORKSPACE;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  char* base = static_cast<char*>(ws);
+  uint16_t* y = reinterpret_cast<uint16_t*>(base + lay.y);
+  uint16_t* xp = reinterpret_cast<uint16_t*>(base + lay.xp);
+  uint16_t* G = reinterpret_cast<uint16_t*>(base + lay.G);
+  uint16_t* hb = reinterpret_cast<uint16_t*>(base + lay.h);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
+  int32_t* offs = reinterpret_cast<int32_t*>(base + lay.offs);
+  int32_t* counts = reinterpret_cast<int32_t*>(base + lay.counts);
+  int32_t* up = reinterpret_cast<int32_t*>(base + lay.up);
+  int32_t* dn = reinterpret_cast<int32_t*>(base + lay.dn);
+  int32_t* part = reinterpret_cast<int32_t*>(base + lay.part);
+  const int64_t P = static_cast<int64_t>(T) * k;
+  if (expert_partition &&
+      cudaMemcpyAsync(part, expert_partition, sizeof(int32_t) * E, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return ISO_ERR_CUDA;
+
+  CUtensorMap tX, tW1, tH, tW2;
+  iso_status st = make_tmap_bf16(&tX, xp, P, H, H, BK, BM);
+  if (st == ISO_OK) st = make_tmap_bf16(&tW1, W1, static_cast<uint64_t>(E) * H, 2 * F, 2 * F, 64, BK);
+  if (st == ISO_OK) st = make_tmap_bf16(&tH, hb, P, F, F, BK, BM);
+  if (st == ISO_OK) st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, BK);
+  if (st != ISO_OK) return st;
+  const int up_nb = div_up(2 * F, BN), dn_nb = H / BN;
+  trace("grouped_gemm_moe", T, E, k, num_partitions);
+  for (int pi = 0; pi < num_partitions; ++pi) {
+    if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, perm, offs, up, up_nb, dn,
+                           dn_nb, s) != cudaSuccess)
+      return ISO_ERR_CUDA;
+    if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
+    GemmParams p = base_params(0, 2 * F, H, L);
+    p.unit_mode = UNIT_GROUPED;
+    p.g_offsets = offs;
+    p.g_unit_prefix = up;
+    p.E = E;
+    p.out = G;
+    p.ldo = 2 * F;
+    st = launch_gemm(EPI_BF16, tX, tW1, p, sm_count(), s);
+    if (st != ISO_OK) return st;
+    if (launch_moe_swiglu(G, offs + E, P, F, hb, s) != cudaSuccess) return ISO_ERR_CUDA;
+    GemmParams q = base_params(0, H, F, L);
+    q.unit_mode = UNIT_GROUPED;
+    q.g_offsets = offs;
+    q.g_unit_prefix = dn;
+    q.E = E;
+    q.out = y;
+    q.ldo = H;
+    q.row_scatter = perm;
+    st = launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s);
+    if (st != ISO_OK) return st;
+  }
+  return launch_moe_combine(y, topk_w, T, k, H, out, s) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+iso_status iso_selftest_bounded_wait(uint64_t timeout_ns, iso_stream stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return ISO_ERR_INVALID_ARG;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  return launch_bounded_wait_selftest(timeout_ns, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+}  // extern "C"

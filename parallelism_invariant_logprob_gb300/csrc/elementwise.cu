@@ -1,0 +1,522 @@
+// elementwise.cu -- the memory-bound steps of the path: tree combine of rank
+// partials, RMSNorm, the logprob chunk tree + gather, MoE routing, permutation,
+// gather, SwiGLU and the routing-slot combine, plus the bounded-wait self test.
+// Every reduction has a fixed shape that depends only on the problem's row
+// length (H, k, C), never on the number of rows or on the launch geometry.
+#include <cuda_bf16.h>
+
+#include "iso_elementwise.h"
+#include "iso_ptx.cuh"
+
+namespace iso {
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f2bf(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
+}
+
+// Balanced binary tree over v[0..n) (n a power of two <= 8), left = lower index.
+template <int NMAX>
+__device__ __forceinline__ float tree_sum(float (&v)[NMAX], int n) {
+#pragma unroll
+  for (int w = 1; w < NMAX; w *= 2) {
+#pragma unroll
+    for (int p = 0; p + w < NMAX; p += 2 * w)
+      if (p + w < n) v[p] = __fadd_rn(v[p], v[p + w]);
+  }
+  return v[0];
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- tree combine
+// C[i, j] = bf16_rn(tree_r S[r][i, j]); each thread owns 4 consecutive columns.
+__global__ void tree_combine_kernel(const float* __restrict__ S, int64_t lds, int64_t rank_stride, int R,
+                                    __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N) {
+  const int64_t nvec_row = N / 4;
+  const int64_t total = static_cast<int64_t>(M) * nvec_row;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = idx / nvec_row;
+    const int64_t j = (idx - i * nvec_row) * 4;
+    float a[8], b[8], c[8], d[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < R) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(S + r * rank_stride + i * lds + j));
+        a[r] = v.x;
+        b[r] = v.y;
+        c[r] = v.z;
+        d[r] = v.w;
+      } else {
+        a[r] = b[r] = c[r] = d[r] = 0.f;
+      }
+    }
+    const float ra = tree_sum<8>(a, R), rb = tree_sum<8>(b, R), rc = tree_sum<8>(c, R), rd = tree_sum<8>(d, R);
+    uint2 o = make_uint2(pack2(ra, rb), pack2(rc, rd));
+    *reinterpret_cast<uint2*>(C + i * ldc + j) = o;
+  }
+}
+
+// ---------------------------------------------------------------------- RMSNorm
+// One warp per row.  Lane l owns the 8-element vectors v = l, l+32, l+64, ...
+// and sums x^2 over them in ascending order (rn multiply, rn add); an xor
+// shuffle tree 16,8,4,2,1 completes the row sum, identical in every lane.
+template <int VPL>  // vectors per lane when H == 256*VPL (kept in registers); 0 = generic
+__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+                               float eps, __nv_bfloat16* __restrict__ y, int T, int H) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = blockDim.x >> 5;
+  const int nvec = H / 8;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5); row < T;
+       row += static_cast<int64_t>(gridDim.x) * warps_per_block) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
+    uint4* yr = reinterpret_cast<uint4*>(y + row * H);
+    const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+    float acc = 0.f;
+    if constexpr (VPL > 0) {
+      uint4 v[VPL];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) v[i] = __ldcs(xr + lane + 32 * i);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+          acc = __fadd_rn(acc, __fmul_rn(a, a));
+          acc = __fadd_rn(acc, __fmul_rn(b, b));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+      const float ms = __fdiv_rn(acc, static_cast<float>(H));
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const uint4 g = __ldg(gr + lane + 32 * i);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __fmul_rn(__fmul_rn(bf16_lo(w[q]), r), bf16_lo(gw[q]));
+          const float hi = __fmul_rn(__fmul_rn(bf16_hi(w[q]), r), bf16_hi(gw[q]));
+          o[q] = pack2(lo, hi);
+        }
+        __stcs(yr + lane + 32 * i, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    } else {
+      for (int vi = lane; vi < nvec; vi += 32) {
+        const uint4 v = xr[vi];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+          acc = __fadd_rn(acc, __fmul_rn(a, a));
+          acc = __fadd_rn(acc, __fmul_rn(b, b));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+      const float ms = __fdiv_rn(acc, static_cast<float>(H));
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+      for (int vi = lane; vi < nvec; vi += 32) {
+        const uint4 v = xr[vi];
+        const uint4 g = __ldg(gr + vi);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __fmul_rn(__fmul_rn(bf16_lo(w[q]), r), bf16_lo(gw[q]));
+          const float hi = __fmul_rn(__fmul_rn(bf16_hi(w[q]), r), bf16_hi(gw[q]));
+          o[q] = pack2(lo, hi);
+        }
+        yr[vi] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------- logprob: chunk tree
+// Per row: the C chunk statistics are merged by the balanced pairwise tree
+// with the odd node carried up, evaluated as a binary counter (merge two
+// equal-size subtrees as soon as both exist, then collapse right to left),
+// which builds exactly that tree.  lse = m + logf(s); out = z_sel - lse.
+__global__ void lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
+                                    const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
+                                    unsigned int* status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  float sm[10], ss[10];
+  int sz[10];
+  int depth = 0;
+  const float2* st = stats + static_cast<int64_t>(t) * C;
+  for (int c = 0; c < C; ++c) {
+    const float2 v = st[c];
+    sm[depth] = v.x;
+    ss[depth] = v.y;
+    sz[depth] = 1;
+    ++depth;
+    while (depth >= 2 && sz[depth - 1] == sz[depth - 2]) {
+      float m1 = sm[depth - 2], s1 = ss[depth - 2];
+      const float m2 = sm[depth - 1], s2 = ss[depth - 1];
+      if (m2 != -INFINITY) {
+        if (m1 == -INFINITY) {
+          m1 = m2;
+          s1 = s2;
+        } else {
+          const float mm = fmaxf(m1, m2);
+          s1 = __fadd_rn(__fmul_rn(s1, expf(__fsub_rn(m1, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
+          m1 = mm;
+        }
+      }
+      sm[depth - 2] = m1;
+      ss[depth - 2] = s1;
+      sz[depth - 2] *= 2;
+      --depth;
+    }
+  }
+  while (depth >= 2) {
+    float m1 = sm[depth - 2], s1 = ss[depth - 2];
+    const float m2 = sm[depth - 1], s2 = ss[depth - 1];
+    if (m2 != -INFINITY) {
+      if (m1 == -INFINITY) {
+        m1 = m2;
+        s1 = s2;
+      } else {
+        const float mm = fmaxf(m1, m2);
+        s1 = __fadd_rn(__fmul_rn(s1, expf(__fsub_rn(m1, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
+        m1 = mm;
+      }
+    }
+    sm[depth - 2] = m1;
+    ss[depth - 2] = s1;
+    sz[depth - 2] += sz[depth - 1];
+    --depth;
+  }
+  const int id = ids[t];
+  if (id < 0 || id >= V) {
+    out[t] = __int_as_float(0x7fc00000);
+    atomicOr(status, kDevBadToken);
+    return;
+  }
+  const float lse = __fadd_rn(sm[0], logf(ss[0]));
+  out[t] = __fsub_rn(zsel[t], lse);
+}
+
+// ------------------------------------------------------------------ MoE route
+// One warp per token; each lane holds E/32 logits (expert e = lane + 32 i).
+// k rounds of a warp argmax with ties to the lower expert id; gates are
+// expf(l_j - l_0) / sum_j, the sum taken in slot order.
+template <int EPL>
+__global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                                 float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); t < T;
+       t += static_cast<int64_t>(gridDim.x) * warps) {
+    float v[EPL];
+    bool taken[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? logits[t * E + e] : -INFINITY;
+      taken[i] = e >= E;
+    }
+    float sel_l[32];
+    int sel_e[32];
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be) || be == 0x7fffffff)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i == be) taken[i] = true;
+      if (j < 32) {
+        sel_l[j] = bv;
+        sel_e[j] = be;
+      }
+    }
+    if (lane == 0) {
+      const float m = sel_l[0];
+      float s = 0.f;
+      for (int j = 0; j < k; ++j) s = __fadd_rn(s, expf(__fsub_rn(sel_l[j], m)));
+      for (int j = 0; j < k; ++j) {
+        ids[t * k + j] = sel_e[j];
+        w[t * k + j] = __fdiv_rn(expf(__fsub_rn(sel_l[j], m)), s);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MoE permute
+// Block e counts the pairs routed to expert e (exact integer sums).
+__global__ void moe_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
+                                 const int32_t* __restrict__ part_map, int part, int32_t* __restrict__ counts,
+                                 unsigned int* status) {
+  const int e = blockIdx.x;
+  __shared__ int warp_cnt[32];
+  int c = 0;
+  for (int64_t p = threadIdx.x; p < P; p += blockDim.x) {
+    const int id = ids[p];
+    c += (id == e);
+    if (e == 0 && (id < 0 || id >= E)) atomicOr(status, kDevBadToken);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+  if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += warp_cnt[i];
+    counts[e] = (part_map == nullptr || part_map[e] == part) ? tot : 0;
+  }
+}
+
+// Block e writes its offset, its pairs in ascending pair order (stable
+// compaction with warp ballots), and the unit prefix entries of the two
+// grouped GEMMs.  Block E writes the totals.
+__global__ void moe_fill_kernel(const int32_t* __restrict__ ids, int64_t P, int E, const int32_t* __restrict__ counts,
+                                int32_t* __restrict__ perm, int32_t* __restrict__ offsets,
+                                int32_t* __restrict__ up_prefix, int up_nblocks, int32_t* __restrict__ down_prefix,
+                                int down_nblocks) {
+  const int e = blockIdx.x;
+  __shared__ int base_sh;
+  __shared__ int warp_tot[32];
+  if (threadIdx.x == 0) {
+    int off = 0, up = 0, dn = 0;
+    for (int i = 0; i < e; ++i) {
+      off += counts[i];
+      const int mb = (counts[i] + 127) / 128;
+      up += mb * up_nblocks;
+      dn += mb * down_nblocks;
+    }
+    offsets[e] = off;
+    up_prefix[e] = up;
+    down_prefix[e] = dn;
+    base_sh = off;
+  }
+  __syncthreads();
+  if (e == E) return;
+  if (counts[e] == 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int running = base_sh;
+  for (int64_t p0 = 0; p0 < P; p0 += blockDim.x) {
+    const int64_t p = p0 + threadIdx.x;
+    const bool hit = p < P && ids[p] == e;
+    const unsigned int bal = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int i = 0; i < nw; ++i) {
+      if (i < warp) before += warp_tot[i];
+      all += warp_tot[i];
+    }
+    if (hit) perm[running + before + __popc(bal & ((1u << lane) - 1u))] = static_cast<int32_t>(p);
+    running += all;
+    __syncthreads();
+  }
+}
+
+// x_perm[i] = x[perm[i] / k]: one warp per row, 16-byte vectors.
+__global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm,
+                                  const int32_t* __restrict__ total, int k, int H, __nv_bfloat16* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int n = *total;
+  const int nvec = H / 8;
+  for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < n; i += gridDim.x * warps) {
+    const int t = perm[i] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(i) * H);
+    for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+  }
+}
+
+// h = bf16_rn(silu(g) * u), silu(g) = g / (1 + expf(-g)), from G = [g | u] in bf16.
+__global__ void moe_swiglu_kernel(const __nv_bfloat16* __restrict__ G, const int32_t* __restrict__ total, int F,
+                                  __nv_bfloat16* __restrict__ h) {
+  const int64_t n = static_cast<int64_t>(*total) * (F / 8);
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = idx / (F / 8);
+    const int64_t c = (idx - row * (F / 8)) * 8;
+    const uint4 gv = *reinterpret_cast<const uint4*>(G + row * 2 * F + c);
+    const uint4 uv = *reinterpret_cast<const uint4*>(G + row * 2 * F + F + c);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float g0 = bf16_lo(gw[q]), g1 = bf16_hi(gw[q]);
+      const float s0 = __fdiv_rn(g0, __fadd_rn(1.0f, expf(-g0)));
+      const float s1 = __fdiv_rn(g1, __fadd_rn(1.0f, expf(-g1)));
+      o[q] = pack2(__fmul_rn(s0, bf16_lo(uw[q])), __fmul_rn(s1, bf16_hi(uw[q])));
+    }
+    *reinterpret_cast<uint4*>(h + row * F + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// out[t, c] = bf16_rn(tree_j rn(w[t,j] * y[t,j,c])): 8 columns per thread.
+__global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w, int T, int k,
+                                   int H, __nv_bfloat16* __restrict__ out) {
+  const int64_t nv = H / 8;
+  const int64_t n = static_cast<int64_t>(T) * nv;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / nv;
+    const int64_t c = (idx - t * nv) * 8;
+    float acc[8][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const float wj = w[t * k + j];
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(y + (t * k + j) * H + c));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q][j] = __fmul_rn(wj, bf16_lo(vw[q]));
+          acc[2 * q + 1][j] = __fmul_rn(wj, bf16_hi(vw[q]));
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q][j] = 0.f;
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = pack2(tree_sum<8>(acc[2 * q], k), tree_sum<8>(acc[2 * q + 1], k));
+    *reinterpret_cast<uint4*>(out + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ----------------------------------------------------------- bounded wait test
+__global__ void bounded_wait_selftest_kernel(uint64_t timeout_ns, unsigned int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the wait must give up after timeout_ns
+    (void)mbar_wait(&bar, 0, timeout_ns, &abort_flag, status);
+  }
+  __syncthreads();
+}
+
+// ================================================================== launchers
+static int grid_for(int64_t work_items, int threads, int max_blocks) {
+  int64_t b = (work_items + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > max_blocks) b = max_blocks;
+  return static_cast<int>(b);
+}
+
+cudaError_t launch_tree_combine(const float* S, int64_t lds, int64_t rank_stride, int R, uint16_t* C, int64_t ldc,
+                                int M, int N, cudaStream_t s) {
+  const int64_t work = static_cast<int64_t>(M) * (N / 4);
+  tree_combine_kernel<<<grid_for(work, 256, sm_count() * 8), 256, 0, s>>>(
+      S, lds, rank_stride, R, reinterpret_cast<__nv_bfloat16*>(C), ldc, M, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* y, int T, int H,
+                           cudaStream_t s) {
+  const int threads = 256;  // 8 rows per block
+  const int blocks = grid_for(static_cast<int64_t>(T) * 32, threads, sm_count() * 16);
+  auto X = reinterpret_cast<const __nv_bfloat16*>(x);
+  auto G = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  auto Y = reinterpret_cast<__nv_bfloat16*>(y);
+  switch (H) {
+    case 1024: rmsnorm_kernel<4><<<blocks, threads, 0, s>>>(X, G, eps, Y, T, H); break;
+    case 2048: rmsnorm_kernel<8><<<blocks, threads, 0, s>>>(X, G, eps, Y, T, H); break;
+    case 4096: rmsnorm_kernel<16><<<blocks, threads, 0, s>>>(X, G, eps, Y, T, H); break;
+    case 8192: rmsnorm_kernel<32><<<blocks, threads, 0, s>>>(X, G, eps, Y, T, H); break;
+    default: rmsnorm_kernel<0><<<blocks, threads, 0, s>>>(X, G, eps, Y, T, H); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_finalize(const float2* stats, const float* zsel, const int32_t* ids, float* out, int T, int C,
+                                int V, cudaStream_t s) {
+  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(stats, zsel, ids, out, T, C, V, device_status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = grid_for(static_cast<int64_t>(T) * 32, threads, sm_count() * 16);
+  if (E <= 32) moe_route_kernel<1><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);
+  else if (E <= 64) moe_route_kernel<2><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);
+  else if (E <= 128) moe_route_kernel<4><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);
+  else moe_route_kernel<8><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
+                               int32_t* counts,
+                               int32_t* perm, int32_t* offsets, int32_t* up_prefix, int up_nblocks,
+                               int32_t* down_prefix, int down_nblocks, cudaStream_t s) {
+  moe_count_kernel<<<E, 1024, 0, s>>>(ids, P, E, part_map, part, counts, device_status_ptr());
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  moe_fill_kernel<<<E + 1, 1024, 0, s>>>(ids, P, E, counts, perm, offsets, up_prefix, up_nblocks, down_prefix,
+                                         down_nblocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int32_t* total, int64_t max_rows, int k,
+                              int H, uint16_t* xp, cudaStream_t s) {
+  const int threads = 256;
+  moe_gather_kernel<<<grid_for(max_rows * 32, threads, sm_count() * 16), threads, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), perm, total, k, H, reinterpret_cast<__nv_bfloat16*>(xp));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_swiglu(const uint16_t* G, const int32_t* total, int64_t max_rows, int F, uint16_t* h,
+                              cudaStream_t s) {
+  const int threads = 256;
+  moe_swiglu_kernel<<<grid_for(max_rows * (F / 8), threads, sm_count() * 16), threads, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(G), total, F, reinterpret_cast<__nv_bfloat16*>(h));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,
+                               cudaStream_t s) {
+  const int threads = 256;
+  moe_combine_kernel<<<grid_for(static_cast<int64_t>(T) * (H / 8), threads, sm_count() * 16), threads, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(y), w, T, k, H, reinterpret_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(uint64_t timeout_ns, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(timeout_ns, device_status_ptr());
+  return cudaGetLastError();
+}
+
+}  // namespace iso

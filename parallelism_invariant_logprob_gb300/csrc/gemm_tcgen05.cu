@@ -1,0 +1,517 @@
+// gemm_tcgen05.cu -- the leaf-tree GEMM engine on 5th-generation tensor cores.
+//
+// What it computes [IsoExec blog, "Parallelism-invariant kernels"]: K is cut
+// into L contiguous leaves; each leaf is one deterministic chain of
+// tcgen05.mma (M=128, N=128, K=16, bf16 x bf16 -> fp32 in TMEM), ascending k,
+// the first MMA of a leaf overwriting its accumulator; the L leaf partials are
+// combined by the fixed balanced binary tree (level by level, left operand =
+// lower leaf index, IEEE fp32 round-to-nearest adds) and the root is either
+//   EPI_BF16    converted to bf16 once and stored [RL-Kernel blog, §2 trigger
+//               table "accumulate-then-convert"; §7 "GEMM"],
+//   EPI_F32     stored as fp32 (a simulated rank's subtree root), or
+//   EPI_LOGPROB reduced to per-row (max, sum exp) statistics per 128-column
+//               vocab tile, folded left to right over the tiles of a vocab
+//               chunk with the two-block LSE merge [RL-Kernel blog, §4
+//               "Causal Chain: How Block Merge Order Alters LSE"; §7 "LogP"],
+//               plus the logit of the selected token.
+//
+// A row's bits depend only on that row, the B columns and the contract: the
+// MMA instruction shape, the per-leaf chain and the tree are the same for
+// every M, every tile position and every schedule; nothing is split along K
+// beyond the contract's leaves and nothing uses atomics.
+//
+// Structure (one CTA per SM, persistent over work units):
+//   warp 0    TMA producer: A tile 128x64 (K-major) and B tile 64x128
+//             (MN-major, two 64-column boxes), 128-byte swizzle, 6-stage ring.
+//   warp 1    TMEM allocator and MMA issuer (one thread).
+//   warps 2-5 epilogue: one thread per accumulator row (TMEM lane); they run
+//             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMA
+//             fills the next leaf, and write the output.
+// The tree's working set lives in four 128-column TMEM buffers.  Buffer
+// assignment is a FIFO free list replayed identically by the MMA thread and
+// the epilogue, so both sides agree without exchanging buffer ids.
+#include <cuda_bf16.h>
+
+#include "iso_internal.h"
+#include "iso_ptx.cuh"
+
+namespace iso {
+
+namespace {
+
+struct Unit {
+  int a_row0;      // first A row of this unit
+  int b_row0;      // first B row (K offset of the expert in grouped mode)
+  int n_tile0;     // first 128-column tile
+  int n_tiles;     // tiles in this unit
+  int rows_valid;  // rows of the 128 that are real
+  int chunk;       // vocab chunk (logprob)
+};
+
+__device__ __forceinline__ int unit_count(const GemmParams& p) {
+  if (p.unit_mode == UNIT_GROUPED) return p.g_unit_prefix[p.E];
+  return p.num_units;
+}
+
+__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U) {
+  if (p.unit_mode == UNIT_GEMM) {
+    const int per_group = p.group_m * p.n_blocks;
+    const int g = u / per_group;
+    const int r = u - g * per_group;
+    const int gm0 = g * p.group_m;
+    const int gsz = min(p.group_m, p.m_blocks - gm0);
+    const int mb = gm0 + r % gsz;
+    const int nb = r / gsz;
+    U.a_row0 = mb * BM;
+    U.b_row0 = 0;
+    U.n_tile0 = nb;
+    U.n_tiles = 1;
+    U.rows_valid = min(BM, p.M - U.a_row0);
+    U.chunk = 0;
+  } else if (p.unit_mode == UNIT_LOGPROB) {
+    // chunk-major: the row blocks working on one vocab chunk run together and
+    // share its W columns in L2.
+    const int chunk = u / p.m_blocks;
+    const int rb = u - chunk * p.m_blocks;
+    U.a_row0 = rb * BM;
+    U.b_row0 = 0;
+    U.n_tile0 = chunk * p.chunk_tiles;
+    U.n_tiles = min(p.chunk_tiles, p.n_blocks - U.n_tile0);
+    U.rows_valid = min(BM, p.M - U.a_row0);
+    U.chunk = chunk;
+  } else {
+    int lo = 0, hi = p.E;  // largest e with prefix[e] <= u
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.g_unit_prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int local = u - p.g_unit_prefix[e];
+    const int mb = local / p.n_blocks;
+    const int nb = local - mb * p.n_blocks;
+    const int off = p.g_offsets[e];
+    const int ne = p.g_offsets[e + 1] - off;
+    U.a_row0 = off + mb * BM;
+    U.b_row0 = e * p.K;
+    U.n_tile0 = nb;
+    U.n_tiles = 1;
+    U.rows_valid = min(BM, ne - mb * BM);
+    U.chunk = 0;
+  }
+}
+
+// FIFO of free TMEM buffers plus the tree stack; replayed identically by the
+// MMA thread and every epilogue thread.
+struct TreeBufs {
+  int fifo[NUM_TMEM_BUFS];
+  int head, count;
+  int stack[NUM_TMEM_BUFS];
+  int depth;
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < NUM_TMEM_BUFS; ++i) fifo[i] = i;
+    head = 0;
+    count = NUM_TMEM_BUFS;
+    depth = 0;
+  }
+  __device__ __forceinline__ int pop_free() {
+    const int b = fifo[head];
+    head = (head + 1) & (NUM_TMEM_BUFS - 1);
+    --count;
+    return b;
+  }
+  __device__ __forceinline__ void push_free(int b) {
+    fifo[(head + count) & (NUM_TMEM_BUFS - 1)] = b;
+    ++count;
+  }
+};
+
+__device__ __forceinline__ int merges_after_leaf(int l) { return __ffs(l + 1) - 1; }  // trailing zeros of l+1
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(lo);
+  const __nv_bfloat16 b = __float2bfloat16_rn(hi);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Two-block LSE merge with (-inf, 0) as the empty block.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mm = fmaxf(m, m2);
+  s = __fadd_rn(__fmul_rn(s, expf(__fsub_rn(m, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
+  m = mm;
+}
+
+}  // namespace
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    iso_leaf_tree_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                              const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* leaf_full = empty_bar + STAGES;
+  uint64_t* buf_free = leaf_full + NUM_TMEM_BUFS;
+  uint64_t* drain_bar = buf_free + NUM_TMEM_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < NUM_TMEM_BUFS; ++b) {
+      mbar_init(&leaf_full[b], 1);
+      mbar_init(&buf_free[b], 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nunits = unit_count(p);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t round = 0;
+      int last_round[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        Unit U;
+        decode_unit(p, u, U);
+        for (int t = 0; t < U.n_tiles && ok; ++t) {
+          const int n0 = (U.n_tile0 + t) * BN;
+          for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sA = smem + stage * STAGE_BYTES;
+            uint8_t* sB = sA + A_STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+            tma_load_2d(sA, &tmA, &full_bar[stage], kb * BK, U.a_row0);
+            tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kb * BK);
+            tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kb * BK);
+            last_round[stage] = static_cast<int>(round);
+            if (++stage == STAGES) {
+              stage = 0;
+              ++round;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for every load this thread issued to land
+        for (int s = 0; s < STAGES; ++s)
+          if (last_round[s] >= 0) {
+            const uint32_t a = smem_u32(&full_bar[s]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(a, static_cast<uint32_t>(last_round[s]) & 1)) {
+              if (globaltimer_ns() - t0 > p.timeout_ns) break;
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+      TreeBufs tb;
+      tb.init();
+      int use_cnt[NUM_TMEM_BUFS] = {0, 0, 0, 0};
+      int stage = 0;
+      uint32_t round = 0;
+      bool ok = true;
+      const uint32_t smem_base = smem_u32(smem);
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        Unit U;
+        decode_unit(p, u, U);
+        for (int t = 0; t < U.n_tiles && ok; ++t) {
+          int cur = 0;
+          for (int kb = 0; kb < p.num_kb && ok; ++kb) {
+            if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
+            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / UMMA_K; ++j) {
+              const int k = kb * BK + j * UMMA_K;
+              if (k >= p.K) break;
+              const int kin = k % p.leaf_len;
+              if (kin == 0) {
+                // first MMA of a leaf: take the next free TMEM buffer
+                cur = tb.pop_free();
+                tb.stack[tb.depth++] = cur;
+                if (use_cnt[cur] > 0) {
+                  if (!mbar_wait(&buf_free[cur], (use_cnt[cur] - 1) & 1, p.timeout_ns, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                }
+                ++use_cnt[cur];
+              }
+              // A: K-major, 128 rows x 128 B per row, 8-row atoms 1024 B apart; +32 B per K=16 step.
+              const uint64_t adesc = sdesc_sw128(a_addr + j * 32, 16, 1024);
+              // B: MN-major, two 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
+              // +2 KB per K=16 step.
+              const uint64_t bdesc = sdesc_sw128(b_addr + j * 2048, 8192, 1024);
+              umma_bf16(tmem_base + static_cast<uint32_t>(cur * BN), adesc, bdesc, idesc, kin != 0 ? 1u : 0u);
+              if (kin + UMMA_K == p.leaf_len) {
+                umma_commit(&leaf_full[cur]);
+                // replay the epilogue's tree bookkeeping for this leaf
+                const int l = k / p.leaf_len;
+                const int nm = merges_after_leaf(l);
+                for (int m = 0; m < nm; ++m) tb.push_free(tb.stack[--tb.depth]);
+                if (l == p.L - 1) tb.push_free(tb.stack[--tb.depth]);  // root, freed after output
+              }
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              ++round;
+            }
+          }
+        }
+      }
+      // drain: every MMA issued by this thread completes before TMEM is released
+      umma_commit(drain_bar);
+      const uint32_t a = smem_u32(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(a, 0)) {
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+          *abort_flag = 1;
+          atomicOr(p.status, kDevTimeout);
+          break;
+        }
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    TreeBufs tb;
+    tb.init();
+    int fill_cnt[NUM_TMEM_BUFS] = {0, 0, 0, 0};
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      Unit U;
+      decode_unit(p, u, U);
+      const bool row_ok = row_in_tile < U.rows_valid;
+      const int row = U.a_row0 + row_in_tile;
+      float run_m = -INFINITY, run_s = 0.f;  // logprob: running chunk statistics
+      int sel = -1;
+      if (EPI == EPI_LOGPROB && row_ok) sel = p.ids[row];
+      float zsel = 0.f;
+      bool have_sel = false;
+      for (int t = 0; t < U.n_tiles && ok; ++t) {
+        const int n0 = (U.n_tile0 + t) * BN;
+        for (int l = 0; l < p.L; ++l) {
+          const int b = tb.pop_free();
+          tb.stack[tb.depth++] = b;
+          if (!mbar_wait(&leaf_full[b], fill_cnt[b] & 1, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          ++fill_cnt[b];
+          tc_fence_after();
+          const int nm = merges_after_leaf(l);
+          for (int m = 0; m < nm; ++m) {
+            const int rb = tb.stack[--tb.depth];
+            const int lb = tb.stack[tb.depth - 1];
+            // left (lower leaves) += right, in place in TMEM
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              uint32_t x[32], y[32];
+              tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 32), x);
+              tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(rb * BN + c * 32), y);
+              tmem_ld_wait2(x, y);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) x[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
+              tmem_st32(tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 32), x);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&buf_free[rb]);
+            tb.push_free(rb);
+          }
+        }
+        if (!ok) break;
+        // ---- the root of this tile
+        const int root = tb.stack[--tb.depth];
+        const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
+        if (EPI == EPI_BF16) {
+          int orow = row;
+          if (p.row_scatter != nullptr && row_ok) orow = p.row_scatter[row];
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(root_addr + c * 32, v);
+            tmem_ld_wait(v);
+            if (row_ok) {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int col = n0 + c * 32 + q * 8;
+                if (col < p.N) {
+                  uint4 w;
+                  w.x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
+                  w.y = pack_bf16x2(u2f(v[q * 8 + 2]), u2f(v[q * 8 + 3]));
+                  w.z = pack_bf16x2(u2f(v[q * 8 + 4]), u2f(v[q * 8 + 5]));
+                  w.w = pack_bf16x2(u2f(v[q * 8 + 6]), u2f(v[q * 8 + 7]));
+                  *reinterpret_cast<uint4*>(dst + col) = w;
+                }
+              }
+            }
+          }
+        } else if (EPI == EPI_F32) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(root_addr + c * 32, v);
+            tmem_ld_wait(v);
+            if (row_ok) {
+              float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ldo;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const int col = n0 + c * 32 + q * 4;
+                if (col < p.N) {
+                  uint4 w = make_uint4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+                  *reinterpret_cast<uint4*>(dst + col) = w;
+                }
+              }
+            }
+          }
+        } else {
+          // tile statistics: m = max over the tile's valid columns (order-free),
+          // s = sum over ascending columns of expf(z - m); then the left fold.
+          float m = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(root_addr + c * 32, v);
+            tmem_ld_wait(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = n0 + c * 32 + i;
+              if (col < p.V) m = fmaxf(m, u2f(v[i]));
+              if (col == sel) {
+                zsel = u2f(v[i]);
+                have_sel = true;
+              }
+            }
+          }
+          float s = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(root_addr + c * 32, v);
+            tmem_ld_wait(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = n0 + c * 32 + i;
+              if (col < p.V) s = __fadd_rn(s, expf(__fsub_rn(u2f(v[i]), m)));
+            }
+          }
+          if (n0 >= p.V) {
+            m = -INFINITY;
+            s = 0.f;
+          }
+          if (t == 0) {
+            run_m = m;
+            run_s = s;
+          } else {
+            lse_merge(run_m, run_s, m, s);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&buf_free[root]);
+        tb.push_free(root);
+      }
+      if (EPI == EPI_LOGPROB && ok && row_ok) {
+        p.ws_stats[static_cast<int64_t>(row) * p.num_chunks + U.chunk] = make_float2(run_m, run_s);
+        if (have_sel) p.ws_zsel[row] = zsel;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                       cudaStream_t s) {
+  static bool attr_set[3] = {false, false, false};
+  cudaError_t e = cudaSuccess;
+  switch (epi) {
+    case EPI_BF16:
+      if (!attr_set[0]) {
+        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES);
+        attr_set[0] = (e == cudaSuccess);
+      }
+      if (e == cudaSuccess)
+        iso_leaf_tree_gemm_kernel<EPI_BF16><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+      break;
+    case EPI_F32:
+      if (!attr_set[1]) {
+        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES);
+        attr_set[1] = (e == cudaSuccess);
+      }
+      if (e == cudaSuccess)
+        iso_leaf_tree_gemm_kernel<EPI_F32><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+      break;
+    case EPI_LOGPROB:
+      if (!attr_set[2]) {
+        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_LOGPROB>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+        attr_set[2] = (e == cudaSuccess);
+      }
+      if (e == cudaSuccess)
+        iso_leaf_tree_gemm_kernel<EPI_LOGPROB><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+      break;
+    default:
+      return ISO_ERR_INVALID_ARG;
+  }
+  if (e != cudaSuccess) return ISO_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+}  // namespace iso

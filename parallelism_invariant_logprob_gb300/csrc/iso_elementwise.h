@@ -1,0 +1,26 @@
+// iso_elementwise.h -- launchers of the memory-bound kernels (elementwise.cu).
+#pragma once
+#include "iso_internal.h"
+
+namespace iso {
+
+cudaError_t launch_tree_combine(const float* S, int64_t lds, int64_t rank_stride, int R, uint16_t* C, int64_t ldc,
+                                int M, int N, cudaStream_t s);
+cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* y, int T, int H,
+                           cudaStream_t s);
+cudaError_t launch_lse_finalize(const float2* stats, const float* zsel, const int32_t* ids, float* out, int T, int C,
+                                int V, cudaStream_t s);
+cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+// part_map (device, [E]) selects experts with part_map[e] == part; NULL = all.
+cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
+                               int32_t* counts, int32_t* perm, int32_t* offsets, int32_t* up_prefix, int up_nblocks,
+                               int32_t* down_prefix, int down_nblocks, cudaStream_t s);
+cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int32_t* total, int64_t max_rows, int k,
+                              int H, uint16_t* xp, cudaStream_t s);
+cudaError_t launch_moe_swiglu(const uint16_t* G, const int32_t* total, int64_t max_rows, int F, uint16_t* h,
+                              cudaStream_t s);
+cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,
+                               cudaStream_t s);
+cudaError_t launch_bounded_wait_selftest(uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace iso

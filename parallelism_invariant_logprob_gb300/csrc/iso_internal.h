@@ -1,0 +1,85 @@
+// iso_internal.h -- declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/iso.h"
+
+namespace iso {
+
+// Device status bits, OR-ed into the library's device status word.
+enum : unsigned int {
+  kDevTimeout = 1u << 0,   // an mbarrier wait ran out of time
+  kDevBadToken = 1u << 1,  // a token id outside [0, V)
+  kDevBadShape = 1u << 2,  // a device-side shape check failed
+};
+
+// Output tile of one CTA: 128 rows (TMEM lanes) x 128 columns; K staged in
+// blocks of 64 (one 128-byte swizzle row of bf16).
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 6;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BK * BN * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
+constexpr int TMEM_COLS = 512;
+constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+// Logprob vocab tiling: statistics per 128-column tile, 19 tiles per chunk.
+constexpr int LP_TILE_COLS = BN;
+constexpr int LP_CHUNK_TILES = 19;
+
+enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2 };
+enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2 };
+
+struct GemmParams {
+  int M, N, K;     // K = contraction length handled by this launch
+  int L;           // leaves in this launch
+  int leaf_len;    // K / L, a multiple of 16
+  int num_kb;      // ceil(K / BK)
+  int m_blocks, n_blocks;
+  int unit_mode;
+  int num_units;   // GEMM / LOGPROB: host-known unit count
+  int group_m;     // GEMM raster: m-blocks per group
+  void* out;
+  int64_t ldo;
+  const int32_t* row_scatter;  // grouped down projection: destination row of each permuted row
+  // logprob
+  const int32_t* ids;
+  float2* ws_stats;  // [T][C] (m, s)
+  float* ws_zsel;    // [T]
+  int V;
+  int chunk_tiles;
+  int num_chunks;
+  // grouped
+  const int32_t* g_offsets;      // [E+1]
+  const int32_t* g_unit_prefix;  // [E+1]
+  int E;
+  // error reporting
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+// Library-wide state, per device.
+unsigned int* device_status_ptr();  // device address of the status word (current device)
+uint64_t wait_timeout_ns();
+int sm_count();
+bool trace_enabled();
+
+// Tensor map over a row-major bf16 matrix [rows x cols] with leading
+// dimension ld (elements), box {box_cols, box_rows}, 128-byte swizzle.
+iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                          uint32_t box_cols, uint32_t box_rows);
+
+// Launchers (gemm_tcgen05.cu).
+iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                       cudaStream_t s);
+
+}  // namespace iso

@@ -1,0 +1,185 @@
+"""GPU parity and invariance of iso_gemm / iso_gemm_leaf_partial /
+iso_tree_combine, through the C ABI, against the float64 oracle.
+
+Tolerance (floating point): per row, max |C_gpu - C_oracle| <= 2e-2 * ||C_oracle row||_2.
+Exact-integer inputs and single-term (identity / permutation) products are
+exact in every summation order, so there the bits must be equal."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parallelism_invariant_logprob_gb300 import binding as B
+from parallelism_invariant_logprob_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def same_bits(a, b):
+    return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+def first_diff(a, b):
+    x, y = bits(a), bits(b)
+    idx = np.argwhere(x != y)
+    if len(idx) == 0:
+        return None
+    i = tuple(idx[0])
+    return f"first differing element {i}: {x[i]:#06x} vs {y[i]:#06x} ({len(idx)} differ)"
+
+
+def check_row_tolerance(C, root):
+    got = oracle.bf16_to_f64(bits(C))
+    err = np.abs(got - root).max(axis=1)
+    bound = 2e-2 * np.linalg.norm(root, axis=1)
+    bad = np.nonzero(err > bound)[0]
+    assert len(bad) == 0, f"rows {bad[:8]} exceed 2e-2 * row norm: err {err[bad[:4]]} bound {bound[bad[:4]]}"
+    # tighter: one bf16 ulp of the defined value, plus fp32-accumulation slack
+    ulp = np.spacing(np.abs(oracle.bf16_to_f64(oracle.round_bf16(root))).astype(np.float32)) * 65536
+    slack = 1e-5 * np.linalg.norm(root, axis=1, keepdims=True)
+    assert np.all(np.abs(got - root) <= ulp + slack)
+
+
+@pytest.fixture(scope="module")
+def c4():
+    return B.Contract(4)
+
+
+@pytest.fixture(scope="module")
+def c8():
+    return B.Contract(8)
+
+
+@pytest.mark.parametrize("M", [1, 7, 32])
+def test_config1_exact_integer_bits_equal_oracle(c4, M):
+    A = inputs.small_int_bf16((M, 2048), -4, 4, seed=10 + M)
+    Bm = inputs.small_int_bf16((2048, 512), -4, 4, seed=20 + M)
+    C = B.gemm(c4, A.to(DEV), Bm.to(DEV))
+    ref = oracle.gemm(bits(A), bits(Bm), 4)
+    assert np.array_equal(bits(C), ref), first_diff(C, torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16))
+
+
+@pytest.mark.parametrize("M,N,K,L", [(300, 392, 1024, 8), (129, 136, 256, 1), (5, 1024, 4096, 8), (64, 256, 768, 8)])
+def test_exact_integer_multi_tile_ragged(M, N, K, L):
+    c = B.Contract(L)
+    A = inputs.small_int_bf16((M, K), -3, 3, seed=M)
+    Bm = inputs.small_int_bf16((K, N), -3, 3, seed=N)
+    C = B.gemm(c, A.to(DEV), Bm.to(DEV))
+    assert np.array_equal(bits(C), oracle.gemm(bits(A), bits(Bm), L))
+
+
+def test_identity_and_permutation_are_exact(c8):
+    A, _ = inputs.gemm_inputs(200, 256, 1, seed=3)
+    I = torch.eye(256, dtype=torch.bfloat16)
+    assert same_bits(B.gemm(c8, A.to(DEV), I.to(DEV)).cpu(), A)
+    perm = torch.randperm(256, generator=torch.Generator().manual_seed(1))
+    assert same_bits(B.gemm(c8, A.to(DEV), I[:, perm].contiguous().to(DEV)).cpu(), A[:, perm])
+
+
+def test_tree_shape_on_gpu(c4):
+    # leaves (2^24, 1, 1, -2^24): the balanced tree gives 1, a left fold 0.
+    K = 4 * 16
+    A = torch.zeros(1, K, dtype=torch.bfloat16)
+    Bm = torch.zeros(K, 8, dtype=torch.bfloat16)
+    for l, v in enumerate([2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)]):
+        A[0, l * 16] = 1.0
+        Bm[l * 16, :] = v
+    C = B.gemm(c4, A.to(DEV), Bm.to(DEV))
+    assert torch.all(C.float().cpu() == 1.0)
+    S = B.gemm_leaf_partial(B.Contract(4), 0, 1, A.to(DEV), Bm.to(DEV))
+    assert torch.all(S.cpu() == 1.0)
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 512, 2048), (300, 392, 1024), (1000, 1024, 1536)])
+def test_normal_inputs_within_tolerance(c8, M, N, K):
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=M + N)
+    C = B.gemm(c8, A.to(DEV), Bm.to(DEV))
+    check_row_tolerance(C, oracle.gemm_root(bits(A), bits(Bm), 8))
+
+
+def test_config1_bitwise_invariance(c4):
+    A, Bm = inputs.gemm_inputs(32, 2048, 512, seed=0)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c4, Ad, Bd)
+    check_row_tolerance(full, oracle.gemm_root(bits(A), bits(Bm), 4))
+    for M in (1, 7):
+        for start in (0, 3, 32 - M):
+            part = B.gemm(c4, Ad[start:start + M].contiguous(), Bd)
+            assert same_bits(part, full[start:start + M]), (M, start)
+    perm = torch.randperm(32, generator=torch.Generator().manual_seed(5)).to(DEV)
+    shuf = B.gemm(c4, Ad[perm].contiguous(), Bd)
+    assert same_bits(shuf, full[perm])
+    # rows embedded in a much larger batch, at other tile positions
+    big = torch.cat([inputs.gemm_inputs(700, 2048, 1, seed=9)[0].to(DEV), Ad, Ad[:5]], dim=0)
+    Cb = B.gemm(c4, big.contiguous(), Bd)
+    assert same_bits(Cb[700:732], full) and same_bits(Cb[732:], full[:5])
+
+
+@pytest.mark.parametrize("R", [1, 2, 4])
+def test_config1_partial_combine_equals_single_pass(c4, R):
+    A, Bm = inputs.gemm_inputs(32, 2048, 512, seed=0)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c4, Ad, Bd)
+    Kl = 2048 // R
+    S = torch.stack([B.gemm_leaf_partial(c4, r, R, Ad[:, r * Kl:(r + 1) * Kl].contiguous(), Bd[r * Kl:(r + 1) * Kl])
+                     for r in range(R)])
+    C = B.tree_combine(c4, S)
+    assert same_bits(C, full), first_diff(C, full)
+    # the rank subtree roots match the oracle's subtree roots within fp32 rounding of the tree
+    for r in range(R):
+        sub = oracle.gemm_root(bits(A), bits(Bm), 4, leaf_lo=r * (4 // R), leaf_hi=(r + 1) * (4 // R))
+        assert np.allclose(S[r].cpu().double().numpy(), sub, rtol=0, atol=1e-4 * np.abs(sub).max() + 1e-6)
+
+
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 12288), (12288, 4096)])
+def test_config2_shapes_sampled_rows_and_ranks(c8, K, N):
+    M = 512
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=1)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c8, Ad, Bd)
+    rows = torch.tensor([0, 1, 127, 128, 300, 511])
+    ref = oracle.gemm_root(bits(A[rows]), bits(Bm), 8)
+    check_row_tolerance(full[rows.to(DEV)], ref)
+    for M1 in (1, 8, 64):
+        assert same_bits(B.gemm(c8, Ad[:M1].contiguous(), Bd), full[:M1])
+    for R in (2, 4, 8):
+        Kl = K // R
+        S = torch.stack([B.gemm_leaf_partial(c8, r, R, Ad[:, r * Kl:(r + 1) * Kl].contiguous(),
+                                             Bd[r * Kl:(r + 1) * Kl]) for r in range(R)])
+        assert same_bits(B.tree_combine(c8, S), full), R
+
+
+@pytest.mark.slow
+def test_config2_full_size_m4096_sampled(c8):
+    K, N, M = 4096, 4096, 4096
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=1, device=DEV)
+    full = B.gemm(c8, A, Bm)
+    rows = torch.tensor([0, 1000, 2047, 4095])
+    ref = oracle.gemm_root(bits(A[rows.to(DEV)]), bits(Bm), 8)
+    check_row_tolerance(full[rows.to(DEV)], ref)
+    assert same_bits(B.gemm(c8, A[4000:4001].contiguous(), Bm), full[4000:4001])
+    assert same_bits(B.gemm(c8, A[1:65].contiguous(), Bm), full[1:65])
+
+
+def test_canary_guard_bands(c8):
+    """Output written exactly inside its [M x N] window of a wider ldc buffer."""
+    M, N, K, ldc = 70, 136, 512, 264
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=4)
+    buf = torch.full((M + 2, ldc), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[1:M + 1]
+    st = c8.lib.iso_gemm(c8.handle, B._ptr(A.to(DEV)), K, B._ptr(Bm.to(DEV)), N, B._vp(out.data_ptr()), ldc, M, N, K,
+                         B._stream())
+    assert st == B.ISO_OK
+    torch.cuda.synchronize()
+    assert torch.all(buf[0] == 7.0) and torch.all(buf[M + 1] == 7.0) and torch.all(buf[1:M + 1, N:] == 7.0)
+    ref = B.gemm(c8, A.to(DEV), Bm.to(DEV))
+    assert same_bits(out[:, :N], ref)
+
+
+def test_device_status_clean(c8):
+    assert B.last_device_status(c8) == B.ISO_OK

@@ -1,0 +1,132 @@
+"""GPU parity and invariance of iso_selected_logprob and iso_rmsnorm through the
+C ABI.  Logprob tolerance: <= 1e-3 absolute against the float64 oracle.
+RMSNorm: bf16 outputs within one bf16 ulp of the oracle's exactly rounded
+value (the GPU reduces in fp32)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parallelism_invariant_logprob_gb300 import binding as B
+from parallelism_invariant_logprob_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32_same(a, b):
+    return torch.equal(a.contiguous().view(torch.int32), b.contiguous().view(torch.int32))
+
+
+@pytest.fixture(scope="module")
+def c8():
+    return B.Contract(8)
+
+
+# ------------------------------------------------------------------ logprob
+@pytest.mark.parametrize("T,H,V", [(300, 512, 2440), (7, 1024, 128 * 19 * 3), (130, 256, 40000), (1, 128, 8)])
+def test_logprob_vs_oracle(c8, T, H, V):
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=T)
+    out = B.selected_logprob(c8, h.to(DEV), W.to(DEV), ids.to(DEV))
+    ref = oracle.selected_logprob(bits(h), bits(W), ids.numpy(), 8)
+    got = out.cpu().double().numpy()
+    assert np.max(np.abs(got - ref["out"])) <= 1e-3
+    assert np.all(got <= 0)
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
+def test_logprob_batch_invariance_bitwise(c8):
+    T, H, V = 300, 512, 2440
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=1)
+    hd, Wd, idd = h.to(DEV), W.to(DEV), ids.to(DEV)
+    full = B.selected_logprob(c8, hd, Wd, idd)
+    for t in (0, 1, 127, 128, 299):
+        one = B.selected_logprob(c8, hd[t:t + 1].contiguous(), Wd, idd[t:t + 1].contiguous())
+        assert f32_same(one, full[t:t + 1]), t
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(3)).to(DEV)
+    sh = B.selected_logprob(c8, hd[perm].contiguous(), Wd, idd[perm].contiguous())
+    assert f32_same(sh, full[perm])
+
+
+def test_logprob_zero_weights_uniform(c8):
+    T, H, V = 64, 256, 151936
+    h, _, ids = inputs.logprob_inputs(T, H, 8, seed=2)
+    ids = inputs.uniform_ids(T, V, seed=5)
+    W = torch.zeros(H, V, dtype=torch.bfloat16, device=DEV)
+    out = B.selected_logprob(c8, h.to(DEV), W, ids.to(DEV))
+    assert torch.all(torch.abs(out.double() + math.log(V)) <= 2e-6)
+    # every row has the identical computation: identical bits
+    assert torch.all(out.view(torch.int32) == out[0].view(torch.int32))
+
+
+def test_logprob_dominant_logit(c8):
+    H, V = 128, 1024
+    h = torch.ones(2, H, dtype=torch.bfloat16)
+    W = torch.zeros(H, V, dtype=torch.bfloat16)
+    W[:, 777] = 0.5  # z[777] = 64
+    out = B.selected_logprob(c8, h.to(DEV), W.to(DEV), torch.tensor([777, 3], dtype=torch.int32, device=DEV)).cpu()
+    assert abs(float(out[0])) < 1e-6
+    assert abs(float(out[1]) + 64.0) < 1e-4
+
+
+def test_logprob_bad_token_id_reports(c8):
+    h, W, _ = inputs.logprob_inputs(4, 128, 256, seed=3)
+    ids = torch.tensor([0, 256, -1, 5], dtype=torch.int32, device=DEV)
+    out = B.selected_logprob(c8, h.to(DEV), W.to(DEV), ids).cpu()
+    assert torch.isnan(out[1]) and torch.isnan(out[2]) and not torch.isnan(out[0]) and not torch.isnan(out[3])
+    assert B.last_device_status(c8) == 11  # ISO_ERR_BAD_TOKEN_ID
+    assert B.last_device_status(c8) == B.ISO_OK  # read clears
+
+
+@pytest.mark.slow
+def test_logprob_config3_full_size_sampled_rows(c8):
+    T, H, V = 4096, 4096, 151936
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=2, device=DEV)
+    out = B.selected_logprob(c8, h, W, ids)
+    rows = torch.tensor([0, 1, 777, 2048, 4095], device=DEV)
+    ref = oracle.selected_logprob(bits(h[rows]), bits(W), ids[rows].cpu().numpy(), 8)
+    assert np.max(np.abs(out[rows].cpu().double().numpy() - ref["out"])) <= 1e-3
+    assert torch.all(out <= 0) and not torch.any(torch.isnan(out))
+    # decode-style M = 1 calls give the packed-prefill bits
+    for t in (0, 777, 4095):
+        one = B.selected_logprob(c8, h[t:t + 1].contiguous(), W, ids[t:t + 1].contiguous())
+        assert f32_same(one, out[t:t + 1])
+
+
+# ------------------------------------------------------------------ RMSNorm
+@pytest.mark.parametrize("T,H", [(33, 4096), (5, 2048), (17, 1000 * 8 // 8), (3, 8192), (64, 776)])
+def test_rmsnorm_vs_oracle(c8, T, H):
+    x, gamma = inputs.rmsnorm_inputs(T, H, seed=H)
+    y = B.rmsnorm(c8, x.to(DEV), gamma.to(DEV), 1e-6)
+    ref, ye = oracle.rmsnorm(bits(x), bits(gamma), 1e-6, exact=True)
+    got = oracle.bf16_to_f64(bits(y))
+    ulp = np.spacing(np.abs(oracle.bf16_to_f64(ref)).astype(np.float32)) * 65536
+    assert np.all(np.abs(got - ye) <= ulp * 1.01)
+    assert np.mean(bits(y) == ref) > 0.99
+
+
+def test_rmsnorm_batch_invariance_bitwise(c8):
+    x, gamma = inputs.rmsnorm_inputs(1000, 4096, seed=4)
+    xd, gd = x.to(DEV), gamma.to(DEV)
+    full = B.rmsnorm(c8, xd, gd, 1e-6)
+    for t in (0, 5, 999):
+        assert torch.equal(B.rmsnorm(c8, xd[t:t + 1].contiguous(), gd, 1e-6).view(torch.int16),
+                           full[t:t + 1].view(torch.int16))
+    perm = torch.randperm(1000, generator=torch.Generator().manual_seed(0)).to(DEV)
+    assert torch.equal(B.rmsnorm(c8, xd[perm].contiguous(), gd, 1e-6).view(torch.int16), full[perm].view(torch.int16))
+
+
+def test_rmsnorm_constant_row(c8):
+    H = 4096
+    x = torch.full((2, H), 2.0, dtype=torch.bfloat16, device=DEV)
+    g = torch.ones(H, dtype=torch.bfloat16, device=DEV)
+    y = B.rmsnorm(c8, x, g, 0.0)
+    assert torch.all(y.float() == 1.0)
+    y0 = B.rmsnorm(c8, torch.zeros_like(x), g, 1e-6)
+    assert torch.all(y0.float() == 0.0)

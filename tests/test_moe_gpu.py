@@ -1,0 +1,123 @@
+"""GPU parity and invariance of the MoE expert layer through the C ABI:
+routing ids and the permutation bit-exact against the oracle, gates within
+1e-6, the layer output within 2e-2 of the row norm, and the output bitwise
+independent of the expert-to-partition assignment."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parallelism_invariant_logprob_gb300 import binding as B
+from parallelism_invariant_logprob_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def same_bits(a, b):
+    return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+@pytest.fixture(scope="module")
+def c8():
+    return B.Contract(8)
+
+
+@pytest.mark.parametrize("T,E,k", [(100, 128, 8), (33, 16, 4), (7, 256, 8), (64, 32, 1)])
+def test_route_exact(c8, T, E, k):
+    g = torch.Generator().manual_seed(T + E)
+    logits = torch.randn(T, E, generator=g)
+    logits[0, :] = 0.5  # all ties: must pick experts 0..k-1
+    ids, w = B.moe_route(c8, logits.to(DEV), k)
+    ids_ref, w_ref = oracle.moe_route(logits.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert list(ids[0].cpu().numpy()) == list(range(k))
+    assert np.max(np.abs(w.cpu().double().numpy() - w_ref)) <= 1e-6
+
+
+def test_permute_exact(c8):
+    T, E, k = 257, 16, 4
+    _, _, _, logits = inputs.moe_inputs(T, 8, E, 8, seed=1)
+    ids, _ = B.moe_route(c8, logits.to(DEV), k)
+    perm, offs = B.moe_permute(c8, ids, E)
+    p_ref, o_ref = oracle.moe_permute(ids.cpu().numpy(), E)
+    assert np.array_equal(offs.cpu().numpy(), o_ref)
+    assert np.array_equal(perm.cpu().numpy()[:o_ref[-1]], p_ref)
+    part = inputs.random_partition(E, 3, seed=2).to(DEV)
+    for p in range(3):
+        perm, offs = B.moe_permute(c8, ids, E, expert_partition=part, partition=p)
+        mask = (part.cpu().numpy() == p).astype(np.uint8)
+        p_ref, o_ref = oracle.moe_permute(ids.cpu().numpy(), E, mask)
+        assert np.array_equal(offs.cpu().numpy(), o_ref)
+        assert np.array_equal(perm.cpu().numpy()[:o_ref[-1]], p_ref)
+
+
+def test_combine_vs_oracle(c8):
+    T, k, H = 50, 8, 256
+    y = inputs.normal_bf16((T, k, H), 1.0, seed=5)
+    g = torch.Generator().manual_seed(6)
+    w = torch.softmax(torch.randn(T, k, generator=g), dim=1)
+    out = B.moe_combine(c8, y.to(DEV), w.to(DEV))
+    ref, oe = oracle.moe_combine(bits(y), w.double().numpy(), exact=True)
+    got = oracle.bf16_to_f64(bits(out))
+    ulp = np.spacing(np.abs(oracle.bf16_to_f64(ref)).astype(np.float32)) * 65536
+    assert np.all(np.abs(got - oe) <= ulp + 1e-6)
+    onehot = torch.zeros(T, k)
+    onehot[:, 3] = 1.0
+    assert same_bits(B.moe_combine(c8, y.to(DEV), onehot.to(DEV)), y[:, 3].to(DEV))
+
+
+def _layer(c, x, ids, w, W1, W2, part=None):
+    return B.grouped_gemm_moe(c, x, ids, w, W1, W2, expert_partition=part)
+
+
+@pytest.mark.parametrize("T,H,E,F,k", [(64, 256, 8, 128, 4), (200, 512, 16, 256, 8)])
+def test_layer_vs_oracle(c8, T, H, E, F, k):
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=T)
+    ids, w = B.moe_route(c8, logits.to(DEV), k)
+    out = _layer(c8, x.to(DEV), ids, w, W1.to(DEV), W2.to(DEV))
+    ref = oracle.moe_layer(bits(x), ids.cpu().numpy(), w.cpu().double().numpy(), bits(W1), bits(W2), 8, exact=True)
+    oe = ref["out_exact"]
+    got = oracle.bf16_to_f64(bits(out))
+    err = np.abs(got - oe).max(axis=1)
+    assert np.all(err <= 2e-2 * np.linalg.norm(oe, axis=1))
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
+def test_layer_partition_invariance_bitwise(c8):
+    T, H, E, F, k = 300, 256, 16, 128, 8
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=11)
+    xd, W1d, W2d = x.to(DEV), W1.to(DEV), W2.to(DEV)
+    ids, w = B.moe_route(c8, logits.to(DEV), k)
+    base = _layer(c8, xd, ids, w, W1d, W2d)
+    for P in (2, 4, 8):
+        contiguous = [e * P // E for e in range(E)]
+        assert same_bits(_layer(c8, xd, ids, w, W1d, W2d, contiguous), base), P
+    rnd = inputs.random_partition(E, 4, seed=7).tolist()
+    assert same_bits(_layer(c8, xd, ids, w, W1d, W2d, rnd), base)
+    # token subsets: a token's output does not depend on the other tokens routed with it
+    sub = torch.arange(0, T, 7, device=DEV)
+    out_sub = _layer(c8, xd[sub].contiguous(), ids[sub].contiguous(), w[sub].contiguous(), W1d, W2d)
+    assert same_bits(out_sub, base[sub])
+
+
+@pytest.mark.slow
+def test_config4_full_size_sampled(c8):
+    T, H, E, F, k = 8192, 2048, 128, 768, 8
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=3, device=DEV)
+    ids, w = B.moe_route(c8, logits, k)
+    ids_ref, _ = oracle.moe_route(logits.cpu().numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    base = _layer(c8, x, ids, w, W1, W2)
+    rows = torch.tensor([0, 4095, 8191], device=DEV)
+    ref = oracle.moe_layer(bits(x[rows]), ids[rows].cpu().numpy(), w[rows].cpu().double().numpy(), bits(W1), bits(W2),
+                           8, exact=True)
+    oe = ref["out_exact"]
+    got = oracle.bf16_to_f64(bits(base[rows]))
+    assert np.all(np.abs(got - oe).max(axis=1) <= 2e-2 * np.linalg.norm(oe, axis=1))
+    for P in (2, 8):
+        assert same_bits(_layer(c8, x, ids, w, W1, W2, [e * P // E for e in range(E)]), base)
