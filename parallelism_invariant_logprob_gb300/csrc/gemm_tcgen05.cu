@@ -100,31 +100,43 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U)
   }
 }
 
-// FIFO of free TMEM buffers plus the tree stack; replayed identically by the
-// MMA thread and every epilogue thread.
+// FIFO of free TMEM buffers plus the tree stack, replayed identically by the
+// MMA thread and every epilogue thread.  Both live in registers as packed
+// 2-bit buffer ids (no local-memory arrays on the MMA issue path).
 struct TreeBufs {
-  int fifo[NUM_TMEM_BUFS];
-  int head, count;
-  int stack[NUM_TMEM_BUFS];
-  int depth;
+  uint32_t fifo;   // free buffers, front in bits [0,2)
+  uint32_t nfree;
+  uint32_t stack;  // tree stack, bottom in bits [0,2)
+  uint32_t depth;
   __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int i = 0; i < NUM_TMEM_BUFS; ++i) fifo[i] = i;
-    head = 0;
-    count = NUM_TMEM_BUFS;
-    depth = 0;
+    fifo = 0u | (1u << 2) | (2u << 4) | (3u << 6);
+    nfree = NUM_TMEM_BUFS;
+    stack = 0u;
+    depth = 0u;
   }
   __device__ __forceinline__ int pop_free() {
-    const int b = fifo[head];
-    head = (head + 1) & (NUM_TMEM_BUFS - 1);
-    --count;
+    const int b = static_cast<int>(fifo & 3u);
+    fifo >>= 2;
+    --nfree;
     return b;
   }
   __device__ __forceinline__ void push_free(int b) {
-    fifo[(head + count) & (NUM_TMEM_BUFS - 1)] = b;
-    ++count;
+    fifo |= static_cast<uint32_t>(b) << (2u * nfree);
+    ++nfree;
   }
+  __device__ __forceinline__ void push(int b) {
+    stack = (stack & ~(3u << (2u * depth))) | (static_cast<uint32_t>(b) << (2u * depth));
+    ++depth;
+  }
+  __device__ __forceinline__ int pop() {
+    --depth;
+    return static_cast<int>((stack >> (2u * depth)) & 3u);
+  }
+  __device__ __forceinline__ int top() const { return static_cast<int>((stack >> (2u * (depth - 1u))) & 3u); }
 };
+
+// Per-buffer phase bits (one bit per TMEM buffer) kept in a register.
+__device__ __forceinline__ uint32_t bit_of(uint32_t bits, int b) { return (bits >> b) & 1u; }
 
 __device__ __forceinline__ int merges_after_leaf(int l) { return __ffs(l + 1) - 1; }  // trailing zeros of l+1
 
@@ -151,6 +163,9 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 }
 
 }  // namespace
+
+// M = 128, N = 128, A K-major, B MN-major, bf16 x bf16 -> fp32.
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
 
 template <int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
@@ -200,8 +215,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // ------------------------------------------------------------ producer
       int stage = 0;
       uint32_t round = 0;
-      int last_round[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+      uint32_t issued = 0;  // stages issued in total
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         Unit U;
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tma_load_2d(sA, &tmA, &full_bar[stage], kb * BK, U.a_row0);
             tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kb * BK);
             tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kb * BK);
-            last_round[stage] = static_cast<int>(round);
+            ++issued;
             if (++stage == STAGES) {
               stage = 0;
               ++round;
@@ -228,72 +242,116 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       if (!ok) {
-        // drain: wait (bounded) for every load this thread issued to land
-        for (int s = 0; s < STAGES; ++s)
-          if (last_round[s] >= 0) {
-            const uint32_t a = smem_u32(&full_bar[s]);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(a, static_cast<uint32_t>(last_round[s]) & 1)) {
-              if (globaltimer_ns() - t0 > p.timeout_ns) break;
-            }
+        // drain: wait (bounded) for every load this thread issued to land.  Stage s was
+        // last filled in round `round` if s < stage, else in round - 1.
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued <= static_cast<uint32_t>(s)) continue;
+          const uint32_t r = (s < stage) ? round : round - 1u;
+          const uint32_t a = smem_u32(&full_bar[s]);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(a, r & 1u)) {
+            if (globaltimer_ns() - t0 > p.timeout_ns) break;
           }
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------------- MMA
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
       TreeBufs tb;
       tb.init();
-      int use_cnt[NUM_TMEM_BUFS] = {0, 0, 0, 0};
+      uint32_t used = 0u;        // bit b: buffer b has been used before
+      uint32_t free_par = 0u;    // bit b: parity of the next buf_free phase to wait for
       int stage = 0;
       uint32_t round = 0;
       bool ok = true;
       const uint32_t smem_base = smem_u32(smem);
+      // descriptor templates; the start-address field (bits 0..13, 16-byte units) is added per use
+      const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(0, 8192, 1024);
+      const bool leaf_aligned = (p.leaf_len % BK) == 0;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         Unit U;
         decode_unit(p, u, U);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           int cur = 0;
+          int pos = 0;   // k offset inside the current leaf
+          int leaf = 0;  // current leaf index
+          int k = 0;
           for (int kb = 0; kb < p.num_kb && ok; ++kb) {
             if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
-            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
-#pragma unroll
-            for (int j = 0; j < BK / UMMA_K; ++j) {
-              const int k = kb * BK + j * UMMA_K;
-              if (k >= p.K) break;
-              const int kin = k % p.leaf_len;
-              if (kin == 0) {
-                // first MMA of a leaf: take the next free TMEM buffer
+            const uint32_t a_lo = (smem_base + stage * STAGE_BYTES) >> 4;
+            const uint32_t b_lo = a_lo + (A_STAGE_BYTES >> 4);
+            // A: K-major, 128 rows x 128 B, 8-row atoms 1024 B apart; +32 B (2 units) per K=16 step.
+            // B: MN-major, two 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
+            //    +2 KB (128 units) per K=16 step.
+            const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
+            if (leaf_aligned && k + BK <= p.K) {
+              // leaves are whole blocks: four straight-line MMAs, the first overwriting at a leaf start
+              if (pos == 0) {
                 cur = tb.pop_free();
-                tb.stack[tb.depth++] = cur;
-                if (use_cnt[cur] > 0) {
-                  if (!mbar_wait(&buf_free[cur], (use_cnt[cur] - 1) & 1, p.timeout_ns, abort_flag, p.status)) {
+                tb.push(cur);
+                if (bit_of(used, cur)) {
+                  if (!mbar_wait(&buf_free[cur], bit_of(free_par, cur), p.timeout_ns, abort_flag, p.status)) {
                     ok = false;
+                    umma_commit(&empty_bar[stage]);
                     break;
                   }
+                  free_par ^= 1u << cur;
                   tc_fence_after();
                 }
-                ++use_cnt[cur];
+                used |= 1u << cur;
               }
-              // A: K-major, 128 rows x 128 B per row, 8-row atoms 1024 B apart; +32 B per K=16 step.
-              const uint64_t adesc = sdesc_sw128(a_addr + j * 32, 16, 1024);
-              // B: MN-major, two 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
-              // +2 KB per K=16 step.
-              const uint64_t bdesc = sdesc_sw128(b_addr + j * 2048, 8192, 1024);
-              umma_bf16(tmem_base + static_cast<uint32_t>(cur * BN), adesc, bdesc, idesc, kin != 0 ? 1u : 0u);
-              if (kin + UMMA_K == p.leaf_len) {
+              const uint32_t d = tmem_base + static_cast<uint32_t>(cur * BN);
+              umma_bf16(d, adesc, bdesc, kIdesc, pos != 0 ? 1u : 0u);
+              umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
+              umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
+              umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+              pos += BK;
+              k += BK;
+              if (pos == p.leaf_len) {
                 umma_commit(&leaf_full[cur]);
-                // replay the epilogue's tree bookkeeping for this leaf
-                const int l = k / p.leaf_len;
-                const int nm = merges_after_leaf(l);
-                for (int m = 0; m < nm; ++m) tb.push_free(tb.stack[--tb.depth]);
-                if (l == p.L - 1) tb.push_free(tb.stack[--tb.depth]);  // root, freed after output
+                const int nm = merges_after_leaf(leaf);
+                for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
+                if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
+                pos = 0;
+                ++leaf;
+              }
+            } else {
+#pragma unroll 1
+              for (int j = 0; j < BK / UMMA_K; ++j, k += UMMA_K) {
+                if (k >= p.K) break;
+                if (pos == 0) {
+                  // first MMA of a leaf: take the next free TMEM buffer
+                  cur = tb.pop_free();
+                  tb.push(cur);
+                  if (bit_of(used, cur)) {
+                    if (!mbar_wait(&buf_free[cur], bit_of(free_par, cur), p.timeout_ns, abort_flag, p.status)) {
+                      ok = false;
+                      break;
+                    }
+                    free_par ^= 1u << cur;
+                    tc_fence_after();
+                  }
+                  used |= 1u << cur;
+                }
+                umma_bf16(tmem_base + static_cast<uint32_t>(cur * BN), adesc + 2 * j, bdesc + 128 * j, kIdesc,
+                          pos != 0 ? 1u : 0u);
+                pos += UMMA_K;
+                if (pos == p.leaf_len) {
+                  umma_commit(&leaf_full[cur]);
+                  // replay the epilogue's tree bookkeeping for this leaf
+                  const int nm = merges_after_leaf(leaf);
+                  for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
+                  if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
+                  pos = 0;
+                  ++leaf;
+                }
               }
             }
             umma_commit(&empty_bar[stage]);
@@ -323,7 +381,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     TreeBufs tb;
     tb.init();
-    int fill_cnt[NUM_TMEM_BUFS] = {0, 0, 0, 0};
+    uint32_t fill_par = 0u;  // bit b: parity of the next leaf_full phase of buffer b
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       Unit U;
@@ -339,17 +397,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int n0 = (U.n_tile0 + t) * BN;
         for (int l = 0; l < p.L; ++l) {
           const int b = tb.pop_free();
-          tb.stack[tb.depth++] = b;
-          if (!mbar_wait(&leaf_full[b], fill_cnt[b] & 1, p.timeout_ns, abort_flag, p.status)) {
+          tb.push(b);
+          if (!mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          ++fill_cnt[b];
+          fill_par ^= 1u << b;
           tc_fence_after();
           const int nm = merges_after_leaf(l);
           for (int m = 0; m < nm; ++m) {
-            const int rb = tb.stack[--tb.depth];
-            const int lb = tb.stack[tb.depth - 1];
+            const int rb = tb.pop();
+            const int lb = tb.top();
             // left (lower leaves) += right, in place in TMEM
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -369,7 +427,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         if (!ok) break;
         // ---- the root of this tile
-        const int root = tb.stack[--tb.depth];
+        const int root = tb.pop();
         const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
         if (EPI == EPI_BF16) {
           int orow = row;
