@@ -126,6 +126,7 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.L = L;
   p.leaf_len = K / L;
   p.num_kb = div_up(K, BK);
+  p.kb_per_leaf = div_up(K / L, BK);
   p.m_blocks = div_up(M, BM);
   p.n_blocks = div_up(N, BN);
   p.group_m = 8;

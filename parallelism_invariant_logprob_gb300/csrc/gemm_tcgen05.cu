@@ -23,10 +23,13 @@
 // Structure (one CTA per SM, persistent over work units):
 //   warp 0    TMA producer: A tile 128x64 (K-major) and B tile 64x128
 //             (MN-major, two 64-column boxes), 128-byte swizzle, 6-stage ring.
-//   warp 1    TMEM allocator and MMA issuer (one thread).
-//   warps 2-5 epilogue: one thread per accumulator row (TMEM lane); they run
-//             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMA
-//             fills the next leaf, and write the output.
+//   warps 1-2 MMA issuers, one thread each: warp 1 issues the even leaves and
+//             warp 2 the odd leaves of every leaf pair (one thread cannot issue
+//             128x128x16 MMAs as fast as the tensor core retires them); warp 1
+//             also owns the TMEM allocation.
+//   warps 3-6 epilogue: one thread per accumulator row (TMEM lane); they run
+//             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMAs
+//             fill the next leaves, and write the output.
 // The tree's working set lives in four 128-column TMEM buffers.  Buffer
 // assignment is a FIFO free list replayed identically by the MMA thread and
 // the epilogue, so both sides agree without exchanging buffer ids.
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* leaf_full = empty_bar + STAGES;
   uint64_t* buf_free = leaf_full + NUM_TMEM_BUFS;
   uint64_t* drain_bar = buf_free + NUM_TMEM_BUFS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -195,7 +198,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&leaf_full[b], 1);
       mbar_init(&buf_free[b], 128);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -210,6 +214,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int nunits = unit_count(p);
 
+  // Leaves are issued in pairs (2g, 2g+1) by two MMA threads (warps 1 and 2), one leaf each;
+  // the producer interleaves their K-blocks, so issuer q owns the stages of parity q.  With one
+  // leaf (L = 1) issuer 0 does everything.  K-blocks are leaf-relative: leaf l's block j covers
+  // k in [l*leaf_len + 64 j, min(+64, (l+1)*leaf_len)).
+  const int per = (p.L >= 2) ? 2 : 1;
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -222,21 +232,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         decode_unit(p, u, U);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           const int n0 = (U.n_tile0 + t) * BN;
-          for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* sA = smem + stage * STAGE_BYTES;
-            uint8_t* sB = sA + A_STAGE_BYTES;
-            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
-            tma_load_2d(sA, &tmA, &full_bar[stage], kb * BK, U.a_row0);
-            tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kb * BK);
-            tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kb * BK);
-            ++issued;
-            if (++stage == STAGES) {
-              stage = 0;
-              ++round;
+          for (int g = 0; g < p.L / per && ok; ++g) {
+            for (int j = 0; j < p.kb_per_leaf && ok; ++j) {
+              for (int q = 0; q < per; ++q) {
+                const int kx = (g * per + q) * p.leaf_len + j * BK;
+                if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+                uint8_t* sA = smem + stage * STAGE_BYTES;
+                uint8_t* sB = sA + A_STAGE_BYTES;
+                mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+                tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
+                tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
+                ++issued;
+                if (++stage == STAGES) {
+                  stage = 0;
+                  ++round;
+                }
+              }
             }
           }
         }
@@ -255,116 +270,82 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 2) {
+    const int me = warp - 1;  // leaf parity issued by this thread
+    if (lane == 0 && me < per) {
       // ----------------------------------------------------------------- MMA
       TreeBufs tb;
       tb.init();
-      uint32_t used = 0u;        // bit b: buffer b has been used before
-      uint32_t free_par = 0u;    // bit b: parity of the next buf_free phase to wait for
-      int stage = 0;
+      uint32_t used = 0u;      // bit b: buffer b has been used before (both issuers' leaves)
+      uint32_t free_par = 0u;  // bit b: parity of the next buf_free phase of buffer b
+      int stage = me;          // this thread's blocks sit at global stage indices me, me+per, ...
       uint32_t round = 0;
       bool ok = true;
       const uint32_t smem_base = smem_u32(smem);
       // descriptor templates; the start-address field (bits 0..13, 16-byte units) is added per use
       const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(0, 8192, 1024);
-      const bool leaf_aligned = (p.leaf_len % BK) == 0;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         Unit U;
         decode_unit(p, u, U);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
-          int cur = 0;
-          int pos = 0;   // k offset inside the current leaf
-          int leaf = 0;  // current leaf index
-          int k = 0;
-          for (int kb = 0; kb < p.num_kb && ok; ++kb) {
-            if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_lo = (smem_base + stage * STAGE_BYTES) >> 4;
-            const uint32_t b_lo = a_lo + (A_STAGE_BYTES >> 4);
-            // A: K-major, 128 rows x 128 B, 8-row atoms 1024 B apart; +32 B (2 units) per K=16 step.
-            // B: MN-major, two 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
-            //    +2 KB (128 units) per K=16 step.
-            const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
-            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
-            if (leaf_aligned && k + BK <= p.K) {
-              // leaves are whole blocks: four straight-line MMAs, the first overwriting at a leaf start
-              if (pos == 0) {
-                cur = tb.pop_free();
-                tb.push(cur);
-                if (bit_of(used, cur)) {
-                  if (!mbar_wait(&buf_free[cur], bit_of(free_par, cur), p.timeout_ns, abort_flag, p.status)) {
-                    ok = false;
-                    umma_commit(&empty_bar[stage]);
-                    break;
-                  }
-                  free_par ^= 1u << cur;
-                  tc_fence_after();
+          for (int leaf = 0; leaf < p.L && ok; ++leaf) {
+            // replay of the tree bookkeeping (identical in both issuers and the epilogue)
+            const int b = tb.pop_free();
+            tb.push(b);
+            const bool reuse = bit_of(used, b) != 0u;
+            const uint32_t wpar = bit_of(free_par, b);
+            if (reuse) free_par ^= 1u << b;
+            used |= 1u << b;
+            if (per == 1 || (leaf & 1) == me) {
+              if (reuse) {
+                if (!mbar_wait(&buf_free[b], wpar, p.timeout_ns, abort_flag, p.status)) {
+                  ok = false;
+                  break;
                 }
-                used |= 1u << cur;
+                tc_fence_after();
               }
-              const uint32_t d = tmem_base + static_cast<uint32_t>(cur * BN);
-              umma_bf16(d, adesc, bdesc, kIdesc, pos != 0 ? 1u : 0u);
-              umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
-              umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
-              umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
-              pos += BK;
-              k += BK;
-              if (pos == p.leaf_len) {
-                umma_commit(&leaf_full[cur]);
-                const int nm = merges_after_leaf(leaf);
-                for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
-                if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
-                pos = 0;
-                ++leaf;
-              }
-            } else {
-#pragma unroll 1
-              for (int j = 0; j < BK / UMMA_K; ++j, k += UMMA_K) {
-                if (k >= p.K) break;
-                if (pos == 0) {
-                  // first MMA of a leaf: take the next free TMEM buffer
-                  cur = tb.pop_free();
-                  tb.push(cur);
-                  if (bit_of(used, cur)) {
-                    if (!mbar_wait(&buf_free[cur], bit_of(free_par, cur), p.timeout_ns, abort_flag, p.status)) {
-                      ok = false;
-                      break;
-                    }
-                    free_par ^= 1u << cur;
-                    tc_fence_after();
-                  }
-                  used |= 1u << cur;
+              const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
+              for (int j = 0; j < p.kb_per_leaf; ++j) {
+                if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
+                  ok = false;
+                  break;
                 }
-                umma_bf16(tmem_base + static_cast<uint32_t>(cur * BN), adesc + 2 * j, bdesc + 128 * j, kIdesc,
-                          pos != 0 ? 1u : 0u);
-                pos += UMMA_K;
-                if (pos == p.leaf_len) {
-                  umma_commit(&leaf_full[cur]);
-                  // replay the epilogue's tree bookkeeping for this leaf
-                  const int nm = merges_after_leaf(leaf);
-                  for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
-                  if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
-                  pos = 0;
-                  ++leaf;
+                tc_fence_after();
+                // A: K-major, 128 rows x 128 B, 8-row atoms 1024 B apart; +32 B (2 units) per K=16.
+                // B: MN-major, 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
+                //    +2 KB (128 units) per K=16.
+                const uint32_t a_lo = (smem_base + stage * STAGE_BYTES) >> 4;
+                const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
+                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(a_lo + (A_STAGE_BYTES >> 4));
+                const int rem = p.leaf_len - j * BK;
+                if (rem >= BK) {
+                  umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
+                  umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
+                  umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
+                  umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+                } else {
+                  for (int i = 0; i < rem / UMMA_K; ++i)
+                    umma_bf16(d, adesc + 2 * i, bdesc + 128 * i, kIdesc, (j != 0 || i != 0) ? 1u : 0u);
+                }
+                if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
+                umma_commit(&empty_bar[stage]);
+                stage += per;
+                if (stage >= STAGES) {
+                  stage -= STAGES;
+                  ++round;
                 }
               }
             }
-            umma_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              ++round;
-            }
+            const int nm = merges_after_leaf(leaf);
+            for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
+            if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
           }
         }
       }
       // drain: every MMA issued by this thread completes before TMEM is released
-      umma_commit(drain_bar);
-      const uint32_t a = smem_u32(drain_bar);
+      umma_commit(&drain_bar[me]);
+      const uint32_t a = smem_u32(&drain_bar[me]);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(a, 0)) {
         if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -398,7 +379,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int l = 0; l < p.L; ++l) {
           const int b = tb.pop_free();
           tb.push(b);
-          if (!mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status)) {
+          // One thread (warp 3, a sub-partition shared with neither the TMA nor an MMA warp)
+          // polls the barrier; the other epilogue warps sleep in a hardware named barrier so
+          // they take no issue slots from the MMA threads.
+          if (threadIdx.x == 96)
+            (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+          named_bar_sync(1, 128);
+          if (*abort_flag) {
             ok = false;
             break;
           }

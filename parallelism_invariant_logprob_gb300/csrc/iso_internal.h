@@ -28,7 +28,7 @@ constexpr int B_STAGE_BYTES = BK * BN * 2;
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
-constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int GEMM_THREADS = 224;  // warp 0 TMA, warps 1-2 MMA (even/odd leaves), warps 3..6 epilogue
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
 constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
@@ -44,6 +44,7 @@ struct GemmParams {
   int L;           // leaves in this launch
   int leaf_len;    // K / L, a multiple of 16
   int num_kb;      // ceil(K / BK)
+  int kb_per_leaf; // ceil(leaf_len / BK)
   int m_blocks, n_blocks;
   int unit_mode;
   int num_units;   // GEMM / LOGPROB: host-known unit count
