@@ -21,13 +21,15 @@
 // beyond the contract's leaves and nothing uses atomics.
 //
 // Structure (one CTA per SM, persistent over work units):
-//   warp 0    TMA producer: A tile 128x64 (K-major) and B tile 64x128
-//             (MN-major, two 64-column boxes), 128-byte swizzle, 6-stage ring.
+//   warps 0,3 TMA producers, one thread each (warp 0 the stages of the even
+//             leaves, warp 3 those of the odd leaves): A tile 128x64 (K-major)
+//             and B tile 64x128 (MN-major, two 64-column boxes), 128-byte
+//             swizzle, 6-stage ring.
 //   warps 1-2 MMA issuers, one thread each: warp 1 issues the even leaves and
 //             warp 2 the odd leaves of every leaf pair (one thread cannot issue
 //             128x128x16 MMAs as fast as the tensor core retires them); warp 1
 //             also owns the TMEM allocation.
-//   warps 3-6 epilogue: one thread per accumulator row (TMEM lane); they run
+//   warps 4-7 epilogue: one thread per accumulator row (TMEM lane); they run
 //             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMAs
 //             fill the next leaves, and write the output.
 // The tree's working set lives in four 128-column TMEM buffers.  Buffer
@@ -138,6 +140,24 @@ struct TreeBufs {
   __device__ __forceinline__ int top() const { return static_cast<int>((stack >> (2u * (depth - 1u))) & 3u); }
 };
 
+// Bounded wait until the shared leaf ticket reaches `want`.
+__device__ __forceinline__ bool wait_ticket(volatile uint32_t* ticket, uint32_t want, uint64_t timeout_ns,
+                                            volatile int* abort_flag, unsigned int* status) {
+  if (*ticket == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (*ticket == want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
 // Per-buffer phase bits (one bit per TMEM buffer) kept in a register.
 __device__ __forceinline__ uint32_t bit_of(uint32_t bits, int b) { return (bits >> b) & 1u; }
 
@@ -183,6 +203,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* drain_bar = buf_free + NUM_TMEM_BUFS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Sequence number of the next leaf allowed to start.  The two MMA threads start their leaves
+  // strictly in leaf order; without that, a thread could wait on a TMEM buffer's buf_free
+  // barrier two phases ahead of its current phase, which the parity wait cannot tell apart
+  // from the phase before.
+  volatile uint32_t* next_leaf = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -201,6 +226,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(&drain_bar[0], 1);
     mbar_init(&drain_bar[1], 1);
     *abort_flag = 0;
+    *next_leaf = 0u;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -220,12 +246,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   // k in [l*leaf_len + 64 j, min(+64, (l+1)*leaf_len)).
   const int per = (p.L >= 2) ? 2 : 1;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp == 0 || warp == 3) {
+    const int me = warp == 0 ? 0 : 1;  // stage parity loaded by this thread
+    if (lane == 0 && me < per) {
       // ------------------------------------------------------------ producer
-      int stage = 0;
+      int stage = me;
       uint32_t round = 0;
-      uint32_t issued = 0;  // stages issued in total
+      uint32_t issued = 0;  // stages issued by this thread
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         Unit U;
@@ -233,38 +260,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           const int n0 = (U.n_tile0 + t) * BN;
           for (int g = 0; g < p.L / per && ok; ++g) {
-            for (int j = 0; j < p.kb_per_leaf && ok; ++j) {
-              for (int q = 0; q < per; ++q) {
-                const int kx = (g * per + q) * p.leaf_len + j * BK;
-                if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
-                  ok = false;
-                  break;
-                }
-                uint8_t* sA = smem + stage * STAGE_BYTES;
-                uint8_t* sB = sA + A_STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
-                tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
-                tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
-                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
-                ++issued;
-                if (++stage == STAGES) {
-                  stage = 0;
-                  ++round;
-                }
+            for (int j = 0; j < p.kb_per_leaf; ++j) {
+              const int kx = (g * per + me) * p.leaf_len + j * BK;
+              if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              uint8_t* sA = smem + stage * STAGE_BYTES;
+              uint8_t* sB = sA + A_STAGE_BYTES;
+              mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+              tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
+              tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+              tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
+              ++issued;
+              stage += per;
+              if (stage >= STAGES) {
+                stage -= STAGES;
+                ++round;
               }
             }
           }
         }
       }
       if (!ok) {
-        // drain: wait (bounded) for every load this thread issued to land.  Stage s was
-        // last filled in round `round` if s < stage, else in round - 1.
-        for (int s = 0; s < STAGES; ++s) {
-          if (issued <= static_cast<uint32_t>(s)) continue;
-          const uint32_t r = (s < stage) ? round : round - 1u;
-          const uint32_t a = smem_u32(&full_bar[s]);
+        // drain: wait (bounded) for every load this thread issued to land.  This thread's k-th
+        // stage index is me + per*k; stage s was last filled in the round of its latest use.
+        const uint32_t total = issued;
+        for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(STAGES / per); ++back) {
+          const uint32_t gidx = static_cast<uint32_t>(me) + static_cast<uint32_t>(per) * (total - back);
+          const uint32_t a = smem_u32(&full_bar[gidx % STAGES]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, r & 1u)) {
+          while (!mbar_try_wait(a, (gidx / STAGES) & 1u)) {
             if (globaltimer_ns() - t0 > p.timeout_ns) break;
           }
         }
@@ -285,11 +311,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // descriptor templates; the start-address field (bits 0..13, 16-byte units) is added per use
       const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(0, 8192, 1024);
+      uint32_t seq = 0;  // sequence number of the current leaf (all tiles, both threads' leaves)
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         Unit U;
         decode_unit(p, u, U);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
-          for (int leaf = 0; leaf < p.L && ok; ++leaf) {
+          for (int leaf = 0; leaf < p.L && ok; ++leaf, ++seq) {
             // replay of the tree bookkeeping (identical in both issuers and the epilogue)
             const int b = tb.pop_free();
             tb.push(b);
@@ -298,6 +325,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (reuse) free_par ^= 1u << b;
             used |= 1u << b;
             if (per == 1 || (leaf & 1) == me) {
+              if (per == 2 && !wait_ticket(next_leaf, seq, p.timeout_ns, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
               if (reuse) {
                 if (!mbar_wait(&buf_free[b], wpar, p.timeout_ns, abort_flag, p.status)) {
                   ok = false;
@@ -305,6 +336,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 tc_fence_after();
               }
+              if (per == 2) *next_leaf = seq + 1u;
               const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
               for (int j = 0; j < p.kb_per_leaf; ++j) {
                 if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
@@ -379,10 +411,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int l = 0; l < p.L; ++l) {
           const int b = tb.pop_free();
           tb.push(b);
-          // One thread (warp 3, a sub-partition shared with neither the TMA nor an MMA warp)
-          // polls the barrier; the other epilogue warps sleep in a hardware named barrier so
-          // they take no issue slots from the MMA threads.
-          if (threadIdx.x == 96)
+          // One thread polls the barrier; the other epilogue warps sleep in a hardware named
+          // barrier so they take no issue slots from the TMA and MMA threads.
+          if (threadIdx.x == 128)
             (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
           named_bar_sync(1, 128);
           if (*abort_flag) {
