@@ -1,0 +1,424 @@
+"""Benchmark: invariant GEMM TFLOP/s (headline) and selected-token logprob
+tokens/s on one GB300, with roofline fractions, the float64 oracle timed on
+the host cores, and an end-to-end number through the C ABI with host buffers.
+
+Step (the timed unit): the three dense projection GEMMs of an 8B-class
+decoder at M = 4096 tokens -- (K, N) in {(4096, 4096), (4096, 12288),
+(12288, 4096)} -- through iso_gemm with an 8-leaf contract.  Inputs are
+resident in HBM; L2 is flushed (256 MiB write) before every step, outside
+the per-step CUDA-event window.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same step on its own batch (data
+parallel replicas, no collective on the data path; weak scaling); timing is
+the max over ranks.  ``--impl reference`` times the float64 CPU oracle (the
+only reference implementation this project has) on a bounded sample of the
+same workload on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SHAPES = [(4096, 4096), (4096, 12288), (12288, 4096)]  # (K, N)
+M_TOKENS = 4096
+LEAVES = 8
+METRIC = "invariant GEMM TFLOP/s & logprob tokens/s on 1 GB300; % of roofline; bitwise checks"
+WORKLOAD = ("dense projection GEMMs of an 8B-class decoder: M=4096 tokens, (K,N) in "
+            "{(4096,4096),(4096,12288),(12288,4096)}, bf16 in / fp32 accumulate / bf16 out, 8 contiguous K-leaves, "
+            "balanced-tree combine")
+LP_T, LP_H, LP_V = 4096, 4096, 151936
+
+
+def step_flops(M=M_TOKENS):
+    return sum(2.0 * M * K * N for K, N in SHAPES)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), tc=float(d["bf16_tflops"]), tc_sus=float(d["bf16_tflops_sustained"]),
+                    src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, src="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tcgen05.cu", "iso_ptx.cuh", "iso_internal.h"):
+        h.update(open(os.path.join(ROOT, "parallelism_invariant_logprob_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel
+    source has not changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return dict(sm_mhz=statistics.median(loaded) if loaded else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=reasons, samples=len(self.rows))
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_gemm_sample(rows, seed=1):
+    """Time the oracle on `rows` rows of each projection; returns (flops, seconds, cores)."""
+    import numpy as np
+    import torch
+    import oracle
+    from parallelism_invariant_logprob_gb300 import inputs
+    oracle._load()
+    flops, secs = 0.0, 0.0
+    for K, N in SHAPES:
+        A, Bm = inputs.gemm_inputs(rows, K, N, seed=seed)
+        Ab = A.view(torch.int16).numpy().view(np.uint16)
+        Bb = Bm.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.gemm_root(Ab, Bb, LEAVES)
+        secs += time.perf_counter() - t0
+        flops += 2.0 * rows * K * N
+    return flops, secs, os.cpu_count() or 1
+
+
+def cpu_baseline(target_s=10.0):
+    f, s, cores = oracle_gemm_sample(4)
+    rows = max(4, min(512, int(4 * target_s / max(s, 1e-3))))
+    f, s, cores = oracle_gemm_sample(rows)
+    return dict(value=f / s / 1e12, unit="TFLOP/s", cores=cores, kind="oracle",
+                sample=f"float64 oracle (leaf tree, 8 leaves) on {rows} rows of each of the 3 projection shapes "
+                       f"(full K and N), {s:.1f} s; value = flops / time")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    times, vals = [], []
+    rows = None
+    for i in range(args.warmup + args.steps):
+        if rows is None:
+            f, s, cores = oracle_gemm_sample(4)
+            rows = max(4, min(256, int(4 * 6.0 / max(s, 1e-3))))
+        f, s, cores = oracle_gemm_sample(rows)
+        if i >= args.warmup:
+            times.append(s)
+            vals.append(f / s / 1e12)
+    v = statistics.mean(vals)
+    sample = (f"float64 oracle on {rows} of the {M_TOKENS} rows of each projection per step (full K, N); "
+              f"value = flops of that sample / its time")
+    line = dict(impl="reference", metric=METRIC, value=v, unit="TFLOP/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * statistics.mean(times), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=WORKLOAD, parallelism="replicas", l2="n/a (CPU)"),
+                cpu_baseline=dict(value=v, unit="TFLOP/s", cores=os.cpu_count() or 1, kind="oracle", sample=sample),
+                e2e=dict(value=v, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    c = B.Contract(LEAVES)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    # resident inputs (one batch per rank)
+    Xs, Ws, Cs = [], [], []
+    for i, (K, N) in enumerate(SHAPES):
+        X, W = inputs.gemm_inputs(M_TOKENS, K, N, seed=100 + 10 * rank + i, device=dev)
+        Xs.append(X)
+        Ws.append(W)
+        Cs.append(torch.empty(M_TOKENS, N, dtype=torch.bfloat16, device=dev))
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        for i in range(len(SHAPES)):
+            if ev is not None:
+                ev[i][0].record(stream)
+            B.gemm(c, Xs[i], Ws[i], out=Cs[i], stream=stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert B.last_device_status(c) == B.ISO_OK
+
+    per_step_ms, launch_ms = [], [[] for _ in SHAPES]
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in SHAPES]
+        step(ev)
+        torch.cuda.synchronize()
+        per_step_ms.append(ev[0][0].elapsed_time(ev[-1][1]))
+        for i in range(len(SHAPES)):
+            launch_ms[i].append(ev[i][0].elapsed_time(ev[i][1]))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    assert B.last_device_status(c) == B.ISO_OK
+
+    ms = statistics.mean(per_step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * step_flops() / (ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the leaf-tree GEMM): algorithmic flops / its launch time
+    kern_s = sum(sum(l) for l in launch_ms) * 1e-3
+    achieved = args.steps * step_flops() / kern_s / 1e12
+    traffic = committed_traffic("iso_leaf_tree_gemm_kernel<EPI_BF16>/M4096")
+    roofline = dict(bound="tensor", achieved=achieved, peak=peaks["tc"], unit="TFLOP/s", frac=achieved / peaks["tc"],
+                    traffic=traffic, peak_kind=f"bf16 dense burst, {peaks['src']}",
+                    per_shape_tflops={f"{K}x{N}": 2.0 * M_TOKENS * K * N / (statistics.mean(launch_ms[i]) * 1e-3) / 1e12
+                                      for i, (K, N) in enumerate(SHAPES)})
+
+    # end to end through the C ABI with host buffers: H2D of the step's activations, D2H of its outputs
+    pinned_x = [X.cpu().pin_memory() for X in Xs]
+    pinned_c = [torch.empty(Cc.shape, dtype=Cc.dtype, pin_memory=True) for Cc in Cs]
+    h2d = sum(x.numel() * 2 for x in pinned_x)
+    d2h = sum(x.numel() * 2 for x in pinned_c)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(len(SHAPES)):
+            Xs[i].copy_(pinned_x[i], non_blocking=True)
+            B.gemm(c, Xs[i], Ws[i], out=Cs[i], stream=stream)
+            pinned_c[i].copy_(Cs[i], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+    e2e = dict(value=world * step_flops() / (e2e_t * 1e-3) / 1e12, unit="TFLOP/s", h2d_bytes_per_step=h2d,
+               d2h_bytes_per_step=d2h)
+
+    extra = {}
+    if not args.skip_secondary:
+        extra = secondary(c, dev, stream, peaks, rank)
+
+    if rank == 0:
+        line = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                    ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+                    data="synthetic",
+                    config=dict(workload=WORKLOAD, global_batch=M_TOKENS * world, parallelism=f"replicas{world}",
+                                l2="flushed before every step (256 MiB write, outside the event window)",
+                                leaves=LEAVES, contract_digest=c.digest.hex()),
+                    roofline=roofline, e2e=e2e, gpu_launches=args.steps * len(SHAPES), clocks=clocks,
+                    wall_s_timed_region=wall)
+        line.update(extra)
+        if world == 1 and not args.skip_cpu:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+
+
+def time_call(fn, iters, warm, stream, flush=None):
+    import torch
+    for _ in range(warm):
+        if flush is not None:
+            flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.mean(ts)
+
+
+def secondary(c, dev, stream, peaks, rank):
+    """Logprob (config 3), small-M GEMMs, simulated-TP partial+combine, RMSNorm,
+    MoE layer and a non-invariant cuBLAS reference for the invariance overhead."""
+    import torch
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import inputs
+    out = {}
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    # selected-token logprob, T = 4096, H = 4096, V = 151936
+    h, W, ids = inputs.logprob_inputs(LP_T, LP_H, LP_V, seed=2, device=dev)
+    lp_out = torch.empty(LP_T, dtype=torch.float32, device=dev)
+    ws = torch.empty(B.selected_logprob_workspace(c, LP_T, LP_V), dtype=torch.uint8, device=dev)
+    t = time_call(lambda: B.selected_logprob(c, h, W, ids, out=lp_out, ws=ws, stream=stream), 5, 2, stream)
+    fl = 2.0 * LP_T * LP_H * LP_V
+    byt = 2.0 * LP_H * LP_V + 2.0 * LP_T * LP_H + 8.0 * LP_T
+    ideal = max(fl / (peaks["tc"] * 1e12), byt / (peaks["hbm"] * 1e9))
+    out["logprob"] = dict(workload="T=4096, H=4096, V=151936, 8 leaves, 128-col tiles, 63 chunks",
+                          tokens_per_s=LP_T / (t * 1e-3), ms=t, tflops=fl / (t * 1e-3) / 1e12,
+                          roofline_frac=ideal / (t * 1e-3), bound="tensor")
+    for T in (1, 64):
+        hT, idT = h[:T].contiguous(), ids[:T].contiguous()
+        wsT = torch.empty(B.selected_logprob_workspace(c, T, LP_V), dtype=torch.uint8, device=dev)
+        oT = torch.empty(T, dtype=torch.float32, device=dev)
+        tt = time_call(lambda: B.selected_logprob(c, hT, W, idT, out=oT, ws=wsT, stream=stream), 5, 2, stream, flush)
+        byt = 2.0 * LP_H * LP_V + 2.0 * T * LP_H + 8.0 * T
+        out["logprob"][f"T{T}"] = dict(ms=tt, tokens_per_s=T / (tt * 1e-3), hbm_gbs=byt / (tt * 1e-3) / 1e9,
+                                       roofline_frac=byt / (peaks["hbm"] * 1e9) / (tt * 1e-3), bound="hbm")
+    del h, W, ids, ws
+
+    # GEMM at small M (weight-streaming, HBM-bound) and the cuBLAS non-invariant reference
+    gm = {}
+    for K, N in SHAPES:
+        X, Wt = inputs.gemm_inputs(M_TOKENS, K, N, seed=5, device=dev)
+        for M in (1, 8, 64, 512, 4096):
+            Xm = X[:M].contiguous()
+            Cm = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            tt = time_call(lambda: B.gemm(c, Xm, Wt, out=Cm, stream=stream), 5, 2, stream, flush)
+            tb = time_call(lambda: torch.matmul(Xm, Wt, out=Cm), 5, 2, stream, flush)
+            byt = 2.0 * (M * K + K * N + M * N)
+            gm[f"M{M}_K{K}_N{N}"] = dict(ms=tt, tflops=2.0 * M * K * N / (tt * 1e-3) / 1e12,
+                                         hbm_gbs=byt / (tt * 1e-3) / 1e9, cublas_ms=tb,
+                                         overhead_vs_cublas=tt / tb)
+        # simulated TP: R ranks' partials + combine at M = 4096
+        for R in (2, 8):
+            Kl = K // R
+            Xr = [X[:, r * Kl:(r + 1) * Kl].contiguous() for r in range(R)]
+            Wr = [Wt[r * Kl:(r + 1) * Kl] for r in range(R)]
+            S = torch.empty(R, M_TOKENS, N, dtype=torch.float32, device=dev)
+            Cc = torch.empty(M_TOKENS, N, dtype=torch.bfloat16, device=dev)
+
+            def tp():
+                for r in range(R):
+                    B.gemm_leaf_partial(c, r, R, Xr[r], Wr[r], out=S[r], stream=stream)
+                B.tree_combine(c, S, out=Cc, stream=stream)
+            tt = time_call(tp, 3, 1, stream, flush)
+            gm[f"TP{R}_M4096_K{K}_N{N}"] = dict(ms=tt, tflops=2.0 * M_TOKENS * K * N / (tt * 1e-3) / 1e12)
+        del X, Wt
+    out["gemm_sweep"] = gm
+
+    # RMSNorm, T = 262144 x 4096 (the packed-prefill size)
+    x, g = inputs.rmsnorm_inputs(262144, 4096, seed=4, device=dev)
+    y = torch.empty_like(x)
+    tt = time_call(lambda: B.rmsnorm(c, x, g, 1e-6, out=y, stream=stream), 5, 2, stream)
+    byt = 4.0 * 262144 * 4096 + 2 * 4096
+    out["rmsnorm"] = dict(workload="T=262144, H=4096", ms=tt, hbm_gbs=byt / (tt * 1e-3) / 1e9,
+                          roofline_frac=byt / (peaks["hbm"] * 1e9) / (tt * 1e-3), bound="hbm")
+    del x, y
+
+    # MoE expert layer: T=8192, H=2048, E=128, F=768, k=8
+    T, H, E, F, k = 8192, 2048, 128, 768, 8
+    xm, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=3, device=dev)
+    ids_m, w_m = B.moe_route(c, logits, k)
+    om = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    wsm = torch.empty(B.grouped_gemm_moe_workspace(c, T, E, k, H, F), dtype=torch.uint8, device=dev)
+    tt = time_call(lambda: B.grouped_gemm_moe(c, xm, ids_m, w_m, W1, W2, out=om, ws=wsm, stream=stream), 3, 1, stream)
+    fl = 2.0 * T * k * (H * 2 * F + F * H)
+    out["moe"] = dict(workload="T=8192, H=2048, E=128, F=768, k=8", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
+                      roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3))
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-secondary", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

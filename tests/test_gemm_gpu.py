@@ -172,12 +172,12 @@ def test_canary_guard_bands(c8):
     A, Bm = inputs.gemm_inputs(M, K, N, seed=4)
     buf = torch.full((M + 2, ldc), 7.0, dtype=torch.bfloat16, device=DEV)
     out = buf[1:M + 1]
-    st = c8.lib.iso_gemm(c8.handle, B._ptr(A.to(DEV)), K, B._ptr(Bm.to(DEV)), N, B._vp(out.data_ptr()), ldc, M, N, K,
-                         B._stream())
+    Ad, Bd = A.to(DEV), Bm.to(DEV)  # keep the device copies alive until the kernel has run
+    st = c8.lib.iso_gemm(c8.handle, B._ptr(Ad), K, B._ptr(Bd), N, B._vp(out.data_ptr()), ldc, M, N, K, B._stream())
     assert st == B.ISO_OK
     torch.cuda.synchronize()
     assert torch.all(buf[0] == 7.0) and torch.all(buf[M + 1] == 7.0) and torch.all(buf[1:M + 1, N:] == 7.0)
-    ref = B.gemm(c8, A.to(DEV), Bm.to(DEV))
+    ref = B.gemm(c8, Ad, Bd)
     assert same_bits(out[:, :N], ref)
 
 
