@@ -162,6 +162,28 @@ size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V);
 iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
                                 float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream);
 
+/* ------------------------------------------ logprob without allocation
+ * No counterpart on the pages: this entry point exists for callers of this
+ * library that cannot allocate device memory -- code behind a plugin or
+ * callback interface that receives only input/output pointers (no allocator,
+ * no workspace argument), or code inside a framework that owns all device
+ * memory or must not call cudaMalloc (it synchronizes the device) in its hot
+ * loop.  Same arguments and bit-identical results as iso_selected_logprob,
+ * minus the workspace: the scratch is one fixed device array of
+ * ISO_LOGPROB_STATIC_SCRATCH_BYTES compiled into the library, present on
+ * every GPU that loads it until the process exits.  Nothing is allocated.
+ * Limit: calls with iso_selected_logprob_workspace(c, T, V) larger than
+ * ISO_LOGPROB_STATIC_SCRATCH_BYTES return ISO_ERR_WORKSPACE and launch
+ * nothing (8 MiB: up to 16,512 tokens at V = 151936).
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array: calls whose kernels may overlap on the GPU (unordered streams) race
+ * and must be serialized by the caller. */
+#define ISO_LOGPROB_STATIC_SCRATCH_BYTES (8u << 20)
+iso_status iso_selected_logprob_static_scratch(const iso_contract* c, const iso_bf16* h, const iso_bf16* W,
+                                               const int32_t* ids, float* out, int T, int H, int V,
+                                               iso_stream stream);
+
 /* --------------------------------------------------------------------- MoE
  * [IsoExec blog, "Unified model": deterministic MoE routing and combination;
  *  "Parallelism-invariant kernels": expert outputs combined in a fixed

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "iso_grouped_gemm_moe": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _int, _int, _int, _int,
                                     _vp, _sz, _vp]),
     "iso_selftest_bounded_wait": (_int, [_u64, _vp]),
+    "iso_selected_logprob_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
 }
 
 
