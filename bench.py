@@ -45,6 +45,22 @@ def step_flops(M=M_TOKENS):
     return sum(2.0 * M * K * N for K, N in SHAPES)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the job's time is its slowest rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -231,12 +247,8 @@ def run_ours(args, rank, world):
     clocks = sampler.stop()
     assert B.last_device_status(c) == B.ISO_OK
 
-    ms = statistics.mean(per_step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * step_flops() / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(statistics.mean(per_step_ms), world, dev)
+    value = job_throughput(world, step_flops(), ms) / 1e12
 
     # roofline of the dominant kernel (the leaf-tree GEMM): algorithmic flops / its launch time
     kern_s = sum(sum(l) for l in launch_ms) * 1e-3
@@ -265,12 +277,8 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_t = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_t], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
-    e2e = dict(value=world * step_flops() / (e2e_t * 1e-3) / 1e12, unit="TFLOP/s", h2d_bytes_per_step=h2d,
+    e2e_t = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+    e2e = dict(value=job_throughput(world, step_flops(), e2e_t) / 1e12, unit="TFLOP/s", h2d_bytes_per_step=h2d,
                d2h_bytes_per_step=d2h)
 
     extra = {}
