@@ -117,6 +117,23 @@ iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uin
 
 namespace {
 
+// A box rows and the stage count that fits the shared-memory budget (even, for the two producers).
+void set_a_rows(GemmParams& p, int a_rows) {
+  p.a_rows = a_rows;
+  p.a_bytes = a_rows * BK * 2;
+  int st = (GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES) / (p.a_bytes + B_STAGE_BYTES);
+  if (st > MAX_STAGES) st = MAX_STAGES;
+  p.stages = st & ~1;
+}
+
+// Smallest A box that covers a single row block of `rows` rows.
+int a_rows_for(int rows) {
+  if (rows <= 16) return 16;
+  if (rows <= 32) return 32;
+  if (rows <= 64) return 64;
+  return 128;
+}
+
 GemmParams base_params(int M, int N, int K, int L) {
   GemmParams p;
   memset(&p, 0, sizeof p);
@@ -130,6 +147,7 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.m_blocks = div_up(M, BM);
   p.n_blocks = div_up(N, BN);
   p.group_m = 8;
+  set_a_rows(p, 128);
   p.status = device_status_ptr();
   p.timeout_ns = wait_timeout_ns();
   return p;
@@ -152,12 +170,13 @@ iso_status check_gemm_args(const void* A, int64_t lda, const void* B, int64_t ld
 iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M,
                     int N, int K, int L, cudaStream_t s) {
   if (!ensure_device_state()) return ISO_ERR_CUDA;
+  GemmParams p = base_params(M, N, K, L);
+  if (p.m_blocks == 1) set_a_rows(p, a_rows_for(M));
   CUtensorMap tA, tB;
-  iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, BM);
+  iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, static_cast<uint32_t>(p.a_rows));
   if (st != ISO_OK) return st;
   st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
   if (st != ISO_OK) return st;
-  GemmParams p = base_params(M, N, K, L);
   p.unit_mode = UNIT_GEMM;
   p.num_units = p.m_blocks * p.n_blocks;
   p.out = C;
@@ -239,10 +258,18 @@ iso_status iso_rmsnorm(const iso_contract* c, const iso_bf16* x, const iso_bf16*
   return launch_rmsnorm(x, gamma, eps, y, T, H, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
 
-static int lp_num_chunks(int V) { return div_up(div_up(V, LP_TILE_COLS), LP_CHUNK_TILES); }
+static int lp_num_tiles(int V) { return div_up(V, LP_TILE_COLS); }
+static int lp_num_chunks(int V) { return div_up(lp_num_tiles(V), LP_CHUNK_TILES); }
+
+// Few row blocks leave most SMs idle when one CTA owns a whole chunk (T = 1: 63 units).
+// Then every 128-column tile is its own work unit and the finalize kernel folds the
+// tile statistics of each chunk left to right -- the same fold, so the same bits.
+static const int kLpTileModeMaxT = 512;
+static bool lp_tile_mode(int T) { return T <= kLpTileModeMaxT; }
 
 static size_t lp_stats_bytes(int T, int V) {
-  return ((static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)) + 255) & ~size_t(255);
+  const size_t per_row = lp_tile_mode(T) ? static_cast<size_t>(lp_num_tiles(V)) : static_cast<size_t>(lp_num_chunks(V));
+  return ((static_cast<size_t>(T) * per_row * sizeof(float2)) + 255) & ~size_t(255);
 }
 
 size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V) {
@@ -262,28 +289,32 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
   if (ws_bytes < iso_selected_logprob_workspace(c, T, V)) return ISO_ERR_WORKSPACE;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
+  GemmParams p = base_params(T, V, H, L);
+  if (p.m_blocks == 1) set_a_rows(p, a_rows_for(T));
   CUtensorMap tA, tB;
-  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, BM);
+  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
   if (st != ISO_OK) return st;
   st = make_tmap_bf16(&tB, W, H, V, V, 64, BK);
   if (st != ISO_OK) return st;
+  const bool tiles = lp_tile_mode(T);
   float2* stats = static_cast<float2*>(ws);
   float* zsel = reinterpret_cast<float*>(static_cast<char*>(ws) + lp_stats_bytes(T, V));
-  GemmParams p = base_params(T, V, H, L);
   p.unit_mode = UNIT_LOGPROB;
-  p.chunk_tiles = LP_CHUNK_TILES;
-  p.num_chunks = lp_num_chunks(V);
+  p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;           // tiles per work unit
+  p.num_chunks = tiles ? lp_num_tiles(V) : lp_num_chunks(V);  // statistics entries per row
   p.num_units = p.m_blocks * p.num_chunks;
   p.ids = ids;
   p.ws_stats = stats;
   p.ws_zsel = zsel;
   p.V = V;
   const int grid = p.num_units < sm_count() ? p.num_units : sm_count();
-  trace("selected_logprob", T, H, V, p.num_chunks);
+  trace(tiles ? "selected_logprob[tile units]" : "selected_logprob[chunk units]", T, H, V, p.num_chunks);
   st = launch_gemm(EPI_LOGPROB, tA, tB, p, grid, S(stream));
   if (st != ISO_OK) return st;
-  return launch_lse_finalize(stats, zsel, ids, out, T, p.num_chunks, V, S(stream)) == cudaSuccess ? ISO_OK
-                                                                                                   : ISO_ERR_CUDA;
+  return launch_lse_finalize(stats, zsel, ids, out, T, lp_num_chunks(V), V, tiles ? 1 : 0, lp_num_tiles(V),
+                             LP_CHUNK_TILES, S(stream)) == cudaSuccess
+             ? ISO_OK
+             : ISO_ERR_CUDA;
 }
 
 iso_status iso_moe_route(const iso_contract* c, const float* logits, int T, int E, int k, int32_t* topk_ids,

@@ -144,59 +144,61 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_b
 }
 
 // ----------------------------------------------------- logprob: chunk tree
+// Two-block LSE merge with (-inf, 0) as the empty block (same operations as the
+// GEMM epilogue's fold).
+__device__ __forceinline__ void lse_merge_into(float& m1, float& s1, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m1 == -INFINITY) {
+    m1 = m2;
+    s1 = s2;
+    return;
+  }
+  const float mm = fmaxf(m1, m2);
+  s1 = __fadd_rn(__fmul_rn(s1, expf(__fsub_rn(m1, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
+  m1 = mm;
+}
+
 // Per row: the C chunk statistics are merged by the balanced pairwise tree
 // with the odd node carried up, evaluated as a binary counter (merge two
 // equal-size subtrees as soon as both exist, then collapse right to left),
 // which builds exactly that tree.  lse = m + logf(s); out = z_sel - lse.
+// When `tile_stats` is set, `stats` holds one entry per 128-column tile and
+// each chunk's entry is first formed by folding its tiles left to right, the
+// fold the GEMM epilogue performs when it owns a whole chunk.
 __global__ void lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
                                     const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
-                                    unsigned int* status) {
+                                    int tile_stats, int ntiles, int chunk_tiles, unsigned int* status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float sm[10], ss[10];
   int sz[10];
   int depth = 0;
-  const float2* st = stats + static_cast<int64_t>(t) * C;
+  const float2* st = stats + static_cast<int64_t>(t) * (tile_stats ? ntiles : C);
   for (int c = 0; c < C; ++c) {
-    const float2 v = st[c];
+    float2 v;
+    if (tile_stats) {
+      const int t0 = c * chunk_tiles;
+      const int t1 = min(t0 + chunk_tiles, ntiles);
+      v = st[t0];
+      for (int q = t0 + 1; q < t1; ++q) {
+        const float2 w = st[q];
+        lse_merge_into(v.x, v.y, w.x, w.y);
+      }
+    } else {
+      v = st[c];
+    }
     sm[depth] = v.x;
     ss[depth] = v.y;
     sz[depth] = 1;
     ++depth;
     while (depth >= 2 && sz[depth - 1] == sz[depth - 2]) {
-      float m1 = sm[depth - 2], s1 = ss[depth - 2];
-      const float m2 = sm[depth - 1], s2 = ss[depth - 1];
-      if (m2 != -INFINITY) {
-        if (m1 == -INFINITY) {
-          m1 = m2;
-          s1 = s2;
-        } else {
-          const float mm = fmaxf(m1, m2);
-          s1 = __fadd_rn(__fmul_rn(s1, expf(__fsub_rn(m1, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
-          m1 = mm;
-        }
-      }
-      sm[depth - 2] = m1;
-      ss[depth - 2] = s1;
+      lse_merge_into(sm[depth - 2], ss[depth - 2], sm[depth - 1], ss[depth - 1]);
       sz[depth - 2] *= 2;
       --depth;
     }
   }
   while (depth >= 2) {
-    float m1 = sm[depth - 2], s1 = ss[depth - 2];
-    const float m2 = sm[depth - 1], s2 = ss[depth - 1];
-    if (m2 != -INFINITY) {
-      if (m1 == -INFINITY) {
-        m1 = m2;
-        s1 = s2;
-      } else {
-        const float mm = fmaxf(m1, m2);
-        s1 = __fadd_rn(__fmul_rn(s1, expf(__fsub_rn(m1, mm))), __fmul_rn(s2, expf(__fsub_rn(m2, mm))));
-        m1 = mm;
-      }
-    }
-    sm[depth - 2] = m1;
-    ss[depth - 2] = s1;
+    lse_merge_into(sm[depth - 2], ss[depth - 2], sm[depth - 1], ss[depth - 1]);
     sz[depth - 2] += sz[depth - 1];
     --depth;
   }
@@ -463,8 +465,9 @@ cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, 
 }
 
 cudaError_t launch_lse_finalize(const float2* stats, const float* zsel, const int32_t* ids, float* out, int T, int C,
-                                int V, cudaStream_t s) {
-  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(stats, zsel, ids, out, T, C, V, device_status_ptr());
+                                int V, int tile_stats, int ntiles, int chunk_tiles, cudaStream_t s) {
+  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(stats, zsel, ids, out, T, C, V, tile_stats, ntiles, chunk_tiles,
+                                                       device_status_ptr());
   return cudaGetLastError();
 }
 

@@ -196,9 +196,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                               const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* leaf_full = empty_bar + STAGES;
+  const int nstages = p.stages;
+  const uint32_t b_region = static_cast<uint32_t>(nstages * p.a_bytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + b_region + nstages * B_STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + MAX_STAGES;
+  uint64_t* leaf_full = empty_bar + MAX_STAGES;
   uint64_t* buf_free = leaf_full + NUM_TMEM_BUFS;
   uint64_t* drain_bar = buf_free + NUM_TMEM_BUFS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 2);
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < nstages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -266,16 +268,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ok = false;
                 break;
               }
-              uint8_t* sA = smem + stage * STAGE_BYTES;
-              uint8_t* sB = sA + A_STAGE_BYTES;
-              mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+              uint8_t* sA = smem + stage * p.a_bytes;
+              uint8_t* sB = smem + b_region + stage * B_STAGE_BYTES;
+              mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + B_STAGE_BYTES));
               tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
               tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
               tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
               ++issued;
               stage += per;
-              if (stage >= STAGES) {
-                stage -= STAGES;
+              if (stage >= nstages) {
+                stage -= nstages;
                 ++round;
               }
             }
@@ -286,11 +288,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // drain: wait (bounded) for every load this thread issued to land.  This thread's k-th
         // stage index is me + per*k; stage s was last filled in the round of its latest use.
         const uint32_t total = issued;
-        for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(STAGES / per); ++back) {
+        for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(nstages / per); ++back) {
           const uint32_t gidx = static_cast<uint32_t>(me) + static_cast<uint32_t>(per) * (total - back);
-          const uint32_t a = smem_u32(&full_bar[gidx % STAGES]);
+          const uint32_t a = smem_u32(&full_bar[gidx % static_cast<uint32_t>(nstages)]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, (gidx / STAGES) & 1u)) {
+          while (!mbar_try_wait(a, (gidx / static_cast<uint32_t>(nstages)) & 1u)) {
             if (globaltimer_ns() - t0 > p.timeout_ns) break;
           }
         }
@@ -347,9 +349,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // A: K-major, 128 rows x 128 B, 8-row atoms 1024 B apart; +32 B (2 units) per K=16.
                 // B: MN-major, 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
                 //    +2 KB (128 units) per K=16.
-                const uint32_t a_lo = (smem_base + stage * STAGE_BYTES) >> 4;
+                const uint32_t a_lo = (smem_base + stage * p.a_bytes) >> 4;
+                const uint32_t b_lo = (smem_base + b_region + stage * B_STAGE_BYTES) >> 4;
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
-                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(a_lo + (A_STAGE_BYTES >> 4));
+                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
                 const int rem = p.leaf_len - j * BK;
                 if (rem >= BK) {
                   umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
@@ -363,8 +366,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
                 umma_commit(&empty_bar[stage]);
                 stage += per;
-                if (stage >= STAGES) {
-                  stage -= STAGES;
+                if (stage >= nstages) {
+                  stage -= nstages;
                   ++round;
                 }
               }

@@ -22,15 +22,20 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 6;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
+// Shared memory: [A tiles: stages x a_bytes][B tiles: stages x 16 KB][barriers].
+// The A box has a_rows rows (128, or 16/32/64 when the whole problem has that few
+// rows); the freed space buys more pipeline stages for the weight stream.  The MMA
+// always reads 128 A rows; rows past the box hold stale data whose outputs are
+// never stored.
+constexpr int MAX_STAGES = 12;
+constexpr int A_TILE_BYTES_MAX = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BK * BN * 2;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int GEMM_BARRIER_BYTES = 512;
 constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
 
 // Logprob vocab tiling: statistics per 128-column tile, 19 tiles per chunk.
 constexpr int LP_TILE_COLS = BN;
@@ -45,6 +50,9 @@ struct GemmParams {
   int leaf_len;    // K / L, a multiple of 16
   int num_kb;      // ceil(K / BK)
   int kb_per_leaf; // ceil(leaf_len / BK)
+  int stages;      // pipeline stages (even, <= MAX_STAGES)
+  int a_rows;      // rows of the A box (16, 32, 64 or 128)
+  int a_bytes;     // a_rows * 128
   int m_blocks, n_blocks;
   int unit_mode;
   int num_units;   // GEMM / LOGPROB: host-known unit count

@@ -130,3 +130,18 @@ def test_rmsnorm_constant_row(c8):
     assert torch.all(y.float() == 1.0)
     y0 = B.rmsnorm(c8, torch.zeros_like(x), g, 1e-6)
     assert torch.all(y0.float() == 0.0)
+
+
+def test_logprob_tile_units_and_chunk_units_agree_bitwise(c8):
+    """Up to 512 rows every 128-column tile is its own work unit and the chunk fold
+    happens in the finalize kernel; above that a CTA folds a whole chunk.  Both
+    follow the same fold order, so a row's bits must not depend on which is used."""
+    T, H, V = 700, 256, 151936
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=77, device=DEV)
+    full = B.selected_logprob(c8, h, W, ids)  # chunk units
+    for lo, hi in ((0, 1), (5, 69), (100, 612), (699, 700)):  # tile units
+        part = B.selected_logprob(c8, h[lo:hi].contiguous(), W, ids[lo:hi].contiguous())
+        assert f32_same(part, full[lo:hi]), (lo, hi)
+    rows = torch.tensor([0, 350, 699], device=DEV)
+    ref = oracle.selected_logprob(bits(h[rows]), bits(W), ids[rows].cpu().numpy(), 8)
+    assert np.max(np.abs(full[rows].cpu().double().numpy() - ref["out"])) <= 1e-3
