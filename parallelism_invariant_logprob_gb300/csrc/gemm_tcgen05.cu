@@ -21,11 +21,11 @@
 // beyond the contract's leaves and nothing uses atomics.
 //
 // Structure (one CTA per SM, persistent over work units):
-//   warps 0,3 TMA producers, one thread each (warp 0 the stages of the even
+//   warps 0,3 TMA producers, one elected lane each (warp 0 the stages of the even
 //             leaves, warp 3 those of the odd leaves): A tile 128x64 (K-major)
 //             and B tile 64x128 (MN-major, two 64-column boxes), 128-byte
 //             swizzle, 6-stage ring.
-//   warps 1-2 MMA issuers, one thread each: warp 1 issues the even leaves and
+//   warps 1-2 MMA issuers, one elected lane each: warp 1 issues the even leaves and
 //             warp 2 the odd leaves of every leaf pair (one thread cannot issue
 //             128x128x16 MMAs as fast as the tensor core retires them); warp 1
 //             also owns the TMEM allocation.
@@ -161,6 +161,16 @@ __device__ __forceinline__ bool wait_ticket(volatile uint32_t* ticket, uint32_t 
 // Per-buffer phase bits (one bit per TMEM buffer) kept in a register.
 __device__ __forceinline__ uint32_t bit_of(uint32_t bits, int b) { return (bits >> b) & 1u; }
 
+// One lane of a converged warp (elected once per warp and reused, so the thread that issues a
+// warp's MMAs is also the one whose tcgen05.commit tracks them).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ int merges_after_leaf(int l) { return __ffs(l + 1) - 1; }  // trailing zeros of l+1
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -249,9 +259,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int per = (p.L >= 2) ? 2 : 1;
 
   if (warp == 0 || warp == 3) {
-    const int me = warp == 0 ? 0 : 1;  // stage parity loaded by this thread
-    if (lane == 0 && me < per) {
+    const int me = warp == 0 ? 0 : 1;  // stage parity loaded by this warp
+    if (me < per) {
       // ------------------------------------------------------------ producer
+      // The whole warp runs the loop (warp-uniform values); one elected lane issues.
+      const bool leader = elect_one();
       int stage = me;
       uint32_t round = 0;
       uint32_t issued = 0;  // stages issued by this thread
@@ -270,10 +282,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
               uint8_t* sA = smem + stage * p.a_bytes;
               uint8_t* sB = smem + b_region + stage * B_STAGE_BYTES;
-              mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + B_STAGE_BYTES));
-              tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
-              tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
-              tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
+              if (leader) {
+                mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + B_STAGE_BYTES));
+                tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
+                tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
+              }
+              __syncwarp();
               ++issued;
               stage += per;
               if (stage >= nstages) {
@@ -299,9 +314,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
     }
   } else if (warp == 1 || warp == 2) {
-    const int me = warp - 1;  // leaf parity issued by this thread
-    if (lane == 0 && me < per) {
+    const int me = warp - 1;  // leaf parity issued by this warp
+    if (me < per) {
       // ----------------------------------------------------------------- MMA
+      // The whole warp runs the loop (warp-uniform values); one elected lane issues.
+      const bool leader = elect_one();
       TreeBufs tb;
       tb.init();
       uint32_t used = 0u;      // bit b: buffer b has been used before (both issuers' leaves)
@@ -354,17 +371,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
                 const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
                 const int rem = p.leaf_len - j * BK;
-                if (rem >= BK) {
-                  umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
-                  umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
-                  umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
-                  umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
-                } else {
-                  for (int i = 0; i < rem / UMMA_K; ++i)
-                    umma_bf16(d, adesc + 2 * i, bdesc + 128 * i, kIdesc, (j != 0 || i != 0) ? 1u : 0u);
+                if (leader) {
+                  if (rem >= BK) {
+                    umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
+                    umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
+                    umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
+                    umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+                  } else {
+                    for (int i = 0; i < rem / UMMA_K; ++i)
+                      umma_bf16(d, adesc + 2 * i, bdesc + 128 * i, kIdesc, (j != 0 || i != 0) ? 1u : 0u);
+                  }
+                  if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
+                  umma_commit(&empty_bar[stage]);
                 }
-                if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
-                umma_commit(&empty_bar[stage]);
+                __syncwarp();
                 stage += per;
                 if (stage >= nstages) {
                   stage -= nstages;
@@ -378,8 +398,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      // drain: every MMA issued by this thread completes before TMEM is released
-      umma_commit(&drain_bar[me]);
+      // drain: every MMA issued by this warp completes before TMEM is released
+      if (leader) umma_commit(&drain_bar[me]);
+      __syncwarp();
       const uint32_t a = smem_u32(&drain_bar[me]);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(a, 0)) {
