@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (!ok) break;
         // ---- the root of this tile
         const int root = tb.pop();
+        bool released = false;
         const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
         if (EPI == EPI_BF16) {
           int orow = row;
@@ -516,37 +517,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else {
           // tile statistics: m = max over the tile's valid columns (order-free),
           // s = sum over ascending columns of expf(z - m); then the left fold.
+          // The whole root comes into registers first and its TMEM buffer is
+          // released before the arithmetic, so the MMAs of the next tile need not wait.
+          uint32_t v[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
+          tmem_ld_wait_only();
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          tc_fence_before();
+          mbar_arrive(&buf_free[root]);
+          tb.push_free(root);
+          released = true;
+          const int sel_off = sel - n0;
           float m = -INFINITY;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(root_addr + c * 32, v);
-            tmem_ld_wait(v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = n0 + c * 32 + i;
-              if (col < p.V) m = fmaxf(m, u2f(v[i]));
-              if (col == sel) {
-                zsel = u2f(v[i]);
-                have_sel = true;
-              }
-            }
-          }
           float s = 0.f;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(root_addr + c * 32, v);
-            tmem_ld_wait(v);
+          if (n0 + BN <= p.V) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = n0 + c * 32 + i;
-              if (col < p.V) s = __fadd_rn(s, expf(__fsub_rn(u2f(v[i]), m)));
+            for (int i = 0; i < BN; ++i) m = fmaxf(m, u2f(v[i]));
+#pragma unroll
+            for (int i = 0; i < BN; ++i) s = __fadd_rn(s, expf(__fsub_rn(u2f(v[i]), m)));
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (n0 + i < p.V) m = fmaxf(m, u2f(v[i]));
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (n0 + i < p.V) s = __fadd_rn(s, expf(__fsub_rn(u2f(v[i]), m)));
+            if (n0 >= p.V) {
+              m = -INFINITY;
+              s = 0.f;
             }
           }
-          if (n0 >= p.V) {
-            m = -INFINITY;
-            s = 0.f;
+          if (sel_off >= 0 && sel_off < BN) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (i == sel_off) zsel = u2f(v[i]);
+            have_sel = true;
           }
           if (t == 0) {
             run_m = m;
@@ -555,9 +562,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             lse_merge(run_m, run_s, m, s);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&buf_free[root]);
-        tb.push_free(root);
+        if (!released) {
+          tc_fence_before();
+          mbar_arrive(&buf_free[root]);
+          tb.push_free(root);
+        }
       }
       if (EPI == EPI_LOGPROB && ok && row_ok) {
         p.ws_stats[static_cast<int64_t>(row) * p.num_chunks + U.chunk] = make_float2(run_m, run_s);
