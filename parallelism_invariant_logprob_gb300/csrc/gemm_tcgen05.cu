@@ -472,19 +472,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int root = tb.pop();
         bool released = false;
         const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
-        if (EPI == EPI_BF16) {
-          int orow = row;
-          if (p.row_scatter != nullptr && row_ok) orow = p.row_scatter[row];
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(root_addr + c * 32, v);
-            tmem_ld_wait(v);
-            if (row_ok) {
+        if (EPI == EPI_BF16 || EPI == EPI_F32) {
+          // the root into registers, its TMEM buffer released, then convert and store
+          uint32_t v[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
+          tmem_ld_wait_only();
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          tc_fence_before();
+          mbar_arrive(&buf_free[root]);
+          tb.push_free(root);
+          released = true;
+          if (row_ok) {
+            if (EPI == EPI_BF16) {
+              const int orow = (p.row_scatter != nullptr) ? p.row_scatter[row] : row;
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int col = n0 + c * 32 + q * 8;
+              for (int q = 0; q < BN / 8; ++q) {
+                const int col = n0 + q * 8;
                 if (col < p.N) {
                   uint4 w;
                   w.x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
@@ -494,23 +500,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   *reinterpret_cast<uint4*>(dst + col) = w;
                 }
               }
-            }
-          }
-        } else if (EPI == EPI_F32) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(root_addr + c * 32, v);
-            tmem_ld_wait(v);
-            if (row_ok) {
+            } else {
               float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const int col = n0 + c * 32 + q * 4;
-                if (col < p.N) {
-                  uint4 w = make_uint4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-                  *reinterpret_cast<uint4*>(dst + col) = w;
-                }
+              for (int q = 0; q < BN / 4; ++q) {
+                const int col = n0 + q * 4;
+                if (col < p.N)
+                  *reinterpret_cast<uint4*>(dst + col) = make_uint4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
               }
             }
           }
