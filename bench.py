@@ -402,6 +402,41 @@ def secondary(c, dev, stream, peaks, rank):
     return out
 
 
+def profile_target(target: str, calls: int):
+    """Run one workload `calls` times with no timing output (the program ncu profiles)."""
+    import torch
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    c = B.Contract(LEAVES)
+    if target == "gemm":
+        X, W = inputs.gemm_inputs(M_TOKENS, 4096, 12288, seed=100, device=dev)
+        C = torch.empty(M_TOKENS, 12288, dtype=torch.bfloat16, device=dev)
+        fn = lambda: B.gemm(c, X, W, out=C)
+    elif target == "logprob":
+        h, W, ids = inputs.logprob_inputs(LP_T, LP_H, LP_V, seed=2, device=dev)
+        out = torch.empty(LP_T, dtype=torch.float32, device=dev)
+        ws = torch.empty(B.selected_logprob_workspace(c, LP_T, LP_V), dtype=torch.uint8, device=dev)
+        fn = lambda: B.selected_logprob(c, h, W, ids, out=out, ws=ws)
+    elif target == "moe":
+        T, H, E, F, k = 8192, 2048, 128, 768, 8
+        x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=3, device=dev)
+        ids, w = B.moe_route(c, logits, k)
+        om = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        wsm = torch.empty(B.grouped_gemm_moe_workspace(c, T, E, k, H, F), dtype=torch.uint8, device=dev)
+        fn = lambda: B.grouped_gemm_moe(c, x, ids, w, W1, W2, out=om, ws=wsm)
+    elif target == "rmsnorm":
+        x, g = inputs.rmsnorm_inputs(262144, 4096, seed=4, device=dev)
+        y = torch.empty_like(x)
+        fn = lambda: B.rmsnorm(c, x, g, 1e-6, out=y)
+    else:
+        raise SystemExit(f"unknown profile target {target}")
+    for _ in range(calls):
+        fn()
+    torch.cuda.synchronize()
+    assert B.last_device_status(c) == B.ISO_OK
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +445,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm"],
+                    help="run one workload --steps times without timing (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_target:
+        profile_target(args.profile_target, args.steps)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
