@@ -450,16 +450,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int m = 0; m < nm; ++m) {
             const int rb = tb.pop();
             const int lb = tb.top();
-            // left (lower leaves) += right, in place in TMEM
+            // left (lower leaves) += right, in place in TMEM, 64 columns per step
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-              uint32_t x[32], y[32];
-              tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 32), x);
-              tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(rb * BN + c * 32), y);
-              tmem_ld_wait2(x, y);
+            for (int c = 0; c < BN / 64; ++c) {
+              uint32_t x[64], y[64];
+              const uint32_t lo = tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 64);
+              const uint32_t ro = tmem_base + lane_off + static_cast<uint32_t>(rb * BN + c * 64);
+              tmem_ld32p(lo, x);
+              tmem_ld32p(lo + 32, x + 32);
+              tmem_ld32p(ro, y);
+              tmem_ld32p(ro + 32, y + 32);
+              tmem_ld_wait_only();
+              tmem_ld_tie(x);
+              tmem_ld_tie(x + 32);
+              tmem_ld_tie(y);
+              tmem_ld_tie(y + 32);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) x[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
-              tmem_st32(tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 32), x);
+              for (int i = 0; i < 64; ++i) x[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
+              tmem_st32p(lo, x);
+              tmem_st32p(lo + 32, x + 32);
             }
             tmem_st_wait();
             tc_fence_before();
