@@ -121,9 +121,11 @@ namespace {
 void set_a_rows(GemmParams& p, int a_rows) {
   p.a_rows = a_rows;
   p.a_bytes = a_rows * BK * 2;
-  int st = (GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES) / (p.a_bytes + B_STAGE_BYTES);
+  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES;
+  int st = room / (p.a_bytes + B_STAGE_BYTES);
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
+  p.epi_staged = (room - p.stages * (p.a_bytes + B_STAGE_BYTES) >= EPI_STAGE_BYTES) ? 1 : 0;
 }
 
 // Smallest A box that covers a single row block of `rows` rows.
@@ -147,6 +149,8 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.m_blocks = div_up(M, BM);
   p.n_blocks = div_up(N, BN);
   p.group_m = 8;
+  p.b_tile_cols = BN;
+  p.b_box2_off = 64;
   set_a_rows(p, 128);
   p.status = device_status_ptr();
   p.timeout_ns = wait_timeout_ns();
@@ -355,11 +359,11 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
 }
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
-//   y_slots [P x H] bf16 | x_perm [P x H] bf16 | G [P x 2F] bf16 | h [P x F] bf16 |
+//   y_slots [P x H] bf16 | x_perm [P x H] bf16 | h [P x F] bf16 |
 //   perm [P] | offsets [E+1] | counts [E] | up_prefix [E+1] | down_prefix [E+1] | part_map [E]
 namespace {
 struct MoeWs {
-  size_t y, xp, G, h, perm, offs, counts, up, dn, part, total;
+  size_t y, xp, h, perm, offs, counts, up, dn, part, total;
 };
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
@@ -368,7 +372,6 @@ MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
   size_t o = 0;
   w.y = o; o += al(P * H * 2);
   w.xp = o; o += al(P * H * 2);
-  w.G = o; o += al(P * 2 * F * 2);
   w.h = o; o += al(P * F * 2);
   w.perm = o; o += al(P * 4);
   w.offs = o; o += al((E + 1) * 4);
@@ -411,7 +414,6 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   char* base = static_cast<char*>(ws);
   uint16_t* y = reinterpret_cast<uint16_t*>(base + lay.y);
   uint16_t* xp = reinterpret_cast<uint16_t*>(base + lay.xp);
-  uint16_t* G = reinterpret_cast<uint16_t*>(base + lay.G);
   uint16_t* hb = reinterpret_cast<uint16_t*>(base + lay.h);
   int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
   int32_t* offs = reinterpret_cast<int32_t*>(base + lay.offs);
@@ -430,23 +432,27 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   if (st == ISO_OK) st = make_tmap_bf16(&tH, hb, P, F, F, BK, BM);
   if (st == ISO_OK) st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, BK);
   if (st != ISO_OK) return st;
-  const int up_nb = div_up(2 * F, BN), dn_nb = H / BN;
+  const int up_nb = F / 64, dn_nb = H / BN;
   trace("grouped_gemm_moe", T, E, k, num_partitions);
   for (int pi = 0; pi < num_partitions; ++pi) {
     if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, perm, offs, up, up_nb, dn,
                            dn_nb, s) != cudaSuccess)
       return ISO_ERR_CUDA;
     if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
-    GemmParams p = base_params(0, 2 * F, H, L);
+    // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns
+    // [F+64j, F+64j+64) and writes h columns [64j, 64j+64).
+    GemmParams p = base_params(0, F, H, L);
+    p.n_blocks = F / 64;
+    p.b_tile_cols = 64;
+    p.b_box2_off = F;
     p.unit_mode = UNIT_GROUPED;
     p.g_offsets = offs;
     p.g_unit_prefix = up;
     p.E = E;
-    p.out = G;
-    p.ldo = 2 * F;
-    st = launch_gemm(EPI_BF16, tX, tW1, p, sm_count(), s);
+    p.out = hb;
+    p.ldo = F;
+    st = launch_gemm(EPI_SWIGLU, tX, tW1, p, sm_count(), s);
     if (st != ISO_OK) return st;
-    if (launch_moe_swiglu(G, offs + E, P, F, hb, s) != cudaSuccess) return ISO_ERR_CUDA;
     GemmParams q = base_params(0, H, F, L);
     q.unit_mode = UNIT_GROUPED;
     q.g_offsets = offs;

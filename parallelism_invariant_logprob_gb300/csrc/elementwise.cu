@@ -1,6 +1,7 @@
 // elementwise.cu -- the memory-bound steps of the path: tree combine of rank
 // partials, RMSNorm, the logprob chunk tree + gather, MoE routing, permutation,
-// gather, SwiGLU and the routing-slot combine, plus the bounded-wait self test.
+// gather and the routing-slot combine, plus the bounded-wait self test.  (SwiGLU
+// runs in the epilogue of the gate/up GEMM.)
 // Every reduction has a fixed shape that depends only on the problem's row
 // length (H, k, C), never on the number of rows or on the launch geometry.
 #include <cuda_bf16.h>
@@ -357,30 +358,6 @@ __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int
   }
 }
 
-// h = bf16_rn(silu(g) * u), silu(g) = g / (1 + expf(-g)), from G = [g | u] in bf16.
-__global__ void moe_swiglu_kernel(const __nv_bfloat16* __restrict__ G, const int32_t* __restrict__ total, int F,
-                                  __nv_bfloat16* __restrict__ h) {
-  const int64_t n = static_cast<int64_t>(*total) * (F / 8);
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = idx / (F / 8);
-    const int64_t c = (idx - row * (F / 8)) * 8;
-    const uint4 gv = *reinterpret_cast<const uint4*>(G + row * 2 * F + c);
-    const uint4 uv = *reinterpret_cast<const uint4*>(G + row * 2 * F + F + c);
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float g0 = bf16_lo(gw[q]), g1 = bf16_hi(gw[q]);
-      const float s0 = __fdiv_rn(g0, __fadd_rn(1.0f, expf(-g0)));
-      const float s1 = __fdiv_rn(g1, __fadd_rn(1.0f, expf(-g1)));
-      o[q] = pack2(__fmul_rn(s0, bf16_lo(uw[q])), __fmul_rn(s1, bf16_hi(uw[q])));
-    }
-    *reinterpret_cast<uint4*>(h + row * F + c) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
 // out[t, c] = bf16_rn(tree_j rn(w[t,j] * y[t,j,c])): 8 columns per thread.
 __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w, int T, int k,
                                    int H, __nv_bfloat16* __restrict__ out) {
@@ -498,14 +475,6 @@ cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int3
   const int threads = 256;
   moe_gather_kernel<<<grid_for(max_rows * 32, threads, sm_count() * 16), threads, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), perm, total, k, H, reinterpret_cast<__nv_bfloat16*>(xp));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_moe_swiglu(const uint16_t* G, const int32_t* total, int64_t max_rows, int F, uint16_t* h,
-                              cudaStream_t s) {
-  const int threads = 256;
-  moe_swiglu_kernel<<<grid_for(max_rows * (F / 8), threads, sm_count() * 16), threads, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(G), total, F, reinterpret_cast<__nv_bfloat16*>(h));
   return cudaGetLastError();
 }
 

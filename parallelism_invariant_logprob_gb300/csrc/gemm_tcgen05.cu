@@ -9,6 +9,9 @@
 //   EPI_BF16    converted to bf16 once and stored [RL-Kernel blog, §2 trigger
 //               table "accumulate-then-convert"; §7 "GEMM"],
 //   EPI_F32     stored as fp32 (a simulated rank's subtree root), or
+//   EPI_SWIGLU  for the MoE gate/up projection: a tile holds 64 gate and the
+//               matching 64 up columns; the epilogue writes
+//               h = bf16(silu(bf16 g) * bf16 u) [RL-Kernel blog, §6 table row 04]
 //   EPI_LOGPROB reduced to per-row (max, sum exp) statistics per 128-column
 //               vocab tile, folded left to right over the tiles of a vocab
 //               chunk with the two-block LSE merge [RL-Kernel blog, §4
@@ -182,6 +185,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+// One epilogue warp writes the bf16 tile rows of its 32 TMEM lanes.  Lane r holds
+// row r as CH chunks of 8 bf16 (16 bytes) and its destination row `orow` (-1: row not
+// stored).  The rows go through the warp's staging area (32 rows x CH*16 bytes, chunk c of
+// row r at slot c ^ (r & 7): conflict-free for both the row-per-lane writes and the
+// row-contiguous reads), then out whole rows at a time: each store instruction covers
+// 512/(CH*16) complete rows, so global writes are full 128-byte lines instead of 32
+// scattered 16-byte pieces.  Columns at or past col_end are not stored.
+template <int CH>
+__device__ __forceinline__ void store_rows_staged(uint8_t* wst, int lane, const uint4 (&w)[CH], int orow,
+                                                  __nv_bfloat16* out, int64_t ldo, int n0, int col_end) {
+  constexpr int ROW_BYTES = CH * 16;
+  constexpr int ROWS_PER_STEP = 32 / CH;
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+    *reinterpret_cast<uint4*>(wst + lane * ROW_BYTES + ((c ^ (lane & 7)) << 4)) = w[c];
+  __syncwarp();
+  const int c = lane % CH;
+#pragma unroll 4
+  for (int t = 0; t < 32 / ROWS_PER_STEP; ++t) {
+    const int r = t * ROWS_PER_STEP + lane / CH;
+    const int dst_row = __shfl_sync(0xffffffffu, orow, r);
+    const uint4 x = *reinterpret_cast<const uint4*>(wst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
+    const int col = n0 + c * 8;
+    if (dst_row >= 0 && col < col_end)
+      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(dst_row) * ldo + col) = x;
+  }
+  __syncwarp();
+}
+
 // Two-block LSE merge with (-inf, 0) as the empty block.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
@@ -220,6 +252,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   // barrier two phases ahead of its current phase, which the parity wait cannot tell apart
   // from the phase before.
   volatile uint32_t* next_leaf = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  // bf16 output staging (valid when p.epi_staged): 8 KB per epilogue warp
+  uint8_t* epi_stage = smem + b_region + nstages * B_STAGE_BYTES + GEMM_BARRIER_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -272,7 +306,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         Unit U;
         decode_unit(p, u, U);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
-          const int n0 = (U.n_tile0 + t) * BN;
+          const int n0 = (U.n_tile0 + t) * p.b_tile_cols;
           for (int g = 0; g < p.L / per && ok; ++g) {
             for (int j = 0; j < p.kb_per_leaf; ++j) {
               const int kx = (g * per + me) * p.leaf_len + j * BK;
@@ -286,7 +320,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + B_STAGE_BYTES));
                 tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
                 tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
-                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + 64, U.b_row0 + kx);
+                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
               }
               __syncwarp();
               ++issued;
@@ -431,7 +465,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       float zsel = 0.f;
       bool have_sel = false;
       for (int t = 0; t < U.n_tiles && ok; ++t) {
-        const int n0 = (U.n_tile0 + t) * BN;
+        const int n0 = (U.n_tile0 + t) * p.b_tile_cols;  // first output column of this tile
         for (int l = 0; l < p.L; ++l) {
           const int b = tb.pop_free();
           tb.push(b);
@@ -481,7 +515,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int root = tb.pop();
         bool released = false;
         const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
-        if (EPI == EPI_BF16 || EPI == EPI_F32) {
+        if (EPI == EPI_SWIGLU) {
+          // columns [0,64) hold gate, [64,128) up (the second B box came from the up half):
+          // g, u = bf16_rn(root); h = bf16_rn(silu(g) * u), silu(g) = g / (1 + expf(-g)).
+          uint32_t v[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
+          tmem_ld_wait_only();
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          tc_fence_before();
+          mbar_arrive(&buf_free[root]);
+          tb.push_free(root);
+          released = true;
+          uint4 hw[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float hv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float g = __bfloat162float(__float2bfloat16_rn(u2f(v[q * 8 + i])));
+              const float u = __bfloat162float(__float2bfloat16_rn(u2f(v[64 + q * 8 + i])));
+              hv[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+            }
+            hw[q].x = pack_bf16x2(hv[0], hv[1]);
+            hw[q].y = pack_bf16x2(hv[2], hv[3]);
+            hw[q].z = pack_bf16x2(hv[4], hv[5]);
+            hw[q].w = pack_bf16x2(hv[6], hv[7]);
+          }
+          if (p.epi_staged) {
+            store_rows_staged<8>(epi_stage + quarter * (32 * 256), lane, hw, row_ok ? row : -1,
+                                 reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0, n0 + 64);
+          } else if (row_ok) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + q * 8) = hw[q];
+          }
+        } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
           // the root into registers, its TMEM buffer released, then convert and store
           uint32_t v[BN];
 #pragma unroll
@@ -493,7 +563,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           mbar_arrive(&buf_free[root]);
           tb.push_free(root);
           released = true;
-          if (row_ok) {
+          if (EPI == EPI_BF16 && p.epi_staged) {
+            uint4 w[BN / 8];
+#pragma unroll
+            for (int q = 0; q < BN / 8; ++q) {
+              w[q].x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
+              w[q].y = pack_bf16x2(u2f(v[q * 8 + 2]), u2f(v[q * 8 + 3]));
+              w[q].z = pack_bf16x2(u2f(v[q * 8 + 4]), u2f(v[q * 8 + 5]));
+              w[q].w = pack_bf16x2(u2f(v[q * 8 + 6]), u2f(v[q * 8 + 7]));
+            }
+            const int orow = row_ok ? ((p.row_scatter != nullptr) ? p.row_scatter[row] : row) : -1;
+            store_rows_staged<BN / 8>(epi_stage + quarter * (32 * 256), lane, w, orow,
+                                      reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0, p.N);
+          } else if (row_ok) {
             if (EPI == EPI_BF16) {
               const int orow = (p.row_scatter != nullptr) ? p.row_scatter[row] : row;
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
@@ -591,7 +673,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                        cudaStream_t s) {
-  static bool attr_set[3] = {false, false, false};
+  static bool attr_set[4] = {false, false, false, false};
   cudaError_t e = cudaSuccess;
   switch (epi) {
     case EPI_BF16:
@@ -611,6 +693,15 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
       }
       if (e == cudaSuccess)
         iso_leaf_tree_gemm_kernel<EPI_F32><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+      break;
+    case EPI_SWIGLU:
+      if (!attr_set[3]) {
+        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES);
+        attr_set[3] = (e == cudaSuccess);
+      }
+      if (e == cudaSuccess)
+        iso_leaf_tree_gemm_kernel<EPI_SWIGLU><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
       break;
     case EPI_LOGPROB:
       if (!attr_set[2]) {

@@ -19,8 +19,6 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32
                                int32_t* down_prefix, int down_nblocks, cudaStream_t s);
 cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int32_t* total, int64_t max_rows, int k,
                               int H, uint16_t* xp, cudaStream_t s);
-cudaError_t launch_moe_swiglu(const uint16_t* G, const int32_t* total, int64_t max_rows, int F, uint16_t* h,
-                              cudaStream_t s);
 cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,
                                cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(uint64_t timeout_ns, cudaStream_t s);

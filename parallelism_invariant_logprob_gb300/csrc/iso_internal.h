@@ -22,11 +22,14 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-// Shared memory: [A tiles: stages x a_bytes][B tiles: stages x 16 KB][barriers].
+// Shared memory: [A tiles: stages x a_bytes][B tiles: stages x 16 KB][barriers]
+// [bf16 output staging, when it fits].
 // The A box has a_rows rows (128, or 16/32/64 when the whole problem has that few
 // rows); the freed space buys more pipeline stages for the weight stream.  The MMA
 // always reads 128 A rows; rows past the box hold stale data whose outputs are
-// never stored.
+// never stored.  The staging area (8 KB per epilogue warp: 32 rows x 256 bytes)
+// lets a warp write its bf16 rows to global memory whole rows at a time; it
+// exists when the stages leave room for it (A boxes of 64 and 128 rows).
 constexpr int MAX_STAGES = 12;
 constexpr int A_TILE_BYTES_MAX = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BK * BN * 2;
@@ -36,12 +39,13 @@ constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
 constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
+constexpr int EPI_STAGE_BYTES = 4 * 32 * BN * 2;  // 4 epilogue warps x 32 rows x 128 bf16
 
 // Logprob vocab tiling: statistics per 128-column tile, 19 tiles per chunk.
 constexpr int LP_TILE_COLS = BN;
 constexpr int LP_CHUNK_TILES = 19;
 
-enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2 };
+enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2, EPI_SWIGLU = 3 };
 enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2 };
 
 struct GemmParams {
@@ -51,8 +55,11 @@ struct GemmParams {
   int num_kb;      // ceil(K / BK)
   int kb_per_leaf; // ceil(leaf_len / BK)
   int stages;      // pipeline stages (even, <= MAX_STAGES)
+  int epi_staged;  // 1: bf16 roots go out through the shared-memory staging area
   int a_rows;      // rows of the A box (16, 32, 64 or 128)
   int a_bytes;     // a_rows * 128
+  int b_tile_cols; // B columns advanced per tile (128; 64 for the SwiGLU gate/up pairing)
+  int b_box2_off;  // column offset of the second 64-column B box (64; F for SwiGLU)
   int m_blocks, n_blocks;
   int unit_mode;
   int num_units;   // GEMM / LOGPROB: host-known unit count
