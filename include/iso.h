@@ -203,8 +203,12 @@ iso_status iso_moe_route(const iso_contract* c, const float* logits, int T, int 
  * DEVICE array [E] int32; NULL selects every expert): perm lists pair indices
  * grouped by expert, ascending p inside an expert; offsets[E+1] are the group
  * boundaries (offsets[E] = number of listed pairs).  perm must hold T k
- * entries; counts_ws is device scratch of 3 E + 2 int32.  Ids outside [0, E)
- * set ISO_ERR_BAD_TOKEN_ID on the device.  E <= 256. */
+ * entries; counts_ws is device scratch of iso_moe_permute_workspace(T, E, k)
+ * bytes (3 E + 2 int32 plus a histogram of E int32 per 1024 pairs), owned by
+ * the caller and free again when the stream passes this call.  Ids outside
+ * [0, E) set ISO_ERR_BAD_TOKEN_ID on the device and are left out.  E <= 256.
+ * iso_moe_permute_workspace returns 0 for invalid sizes. */
+size_t iso_moe_permute_workspace(int T, int E, int k);
 iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T, int E, int k,
                            const int32_t* expert_partition, int partition, int32_t* perm, int32_t* offsets,
                            int32_t* counts_ws, iso_stream stream);

@@ -58,6 +58,7 @@ _SIGNATURES = {
     "iso_selected_logprob_workspace": (_sz, [_vp, _int, _int]),
     "iso_selected_logprob": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
     "iso_moe_route": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp, _vp]),
+    "iso_moe_permute_workspace": (_sz, [_int, _int, _int]),
     "iso_moe_permute": (_int, [_vp, _vp, _int, _int, _int, _vp, _int, _vp, _vp, _vp, _vp]),
     "iso_moe_combine": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
     "iso_grouped_gemm_moe_workspace": (_sz, [_vp, _int, _int, _int, _int, _int]),
@@ -230,7 +231,7 @@ def moe_permute(c: Contract, ids, E: int, expert_partition=None, partition: int 
     T, k = ids.shape
     perm = torch.empty(T * k, dtype=torch.int32, device=ids.device)
     offs = torch.empty(E + 1, dtype=torch.int32, device=ids.device)
-    cnt = torch.empty(3 * E + 2, dtype=torch.int32, device=ids.device)
+    cnt = torch.empty(int(c.lib.iso_moe_permute_workspace(T, E, k)) // 4, dtype=torch.int32, device=ids.device)
     st = c.lib.iso_moe_permute(c.handle, _ptr(ids), T, E, k, _ptr(expert_partition), partition, _ptr(perm),
                                _ptr(offs), _ptr(cnt), _stream(stream))
     c.lib.check(st, "iso_moe_permute")

@@ -324,24 +324,32 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
 iso_status iso_moe_route(const iso_contract* c, const float* logits, int T, int E, int k, int32_t* topk_ids,
                          float* topk_w, iso_stream stream) {
   if (!c || T < 0 || E <= 0 || k <= 0) return ISO_ERR_INVALID_ARG;
-  if (E > 256 || k > E || k > 32) return ISO_ERR_UNSUPPORTED;
+  if (E > MOE_MAX_EXPERTS || k > E || k > 32) return ISO_ERR_UNSUPPORTED;
   if (T == 0) return ISO_OK;
   if (!logits || !topk_ids || !topk_w) return ISO_ERR_INVALID_ARG;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
   return launch_moe_route(logits, T, E, k, topk_ids, topk_w, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
 
+size_t iso_moe_permute_workspace(int T, int E, int k) {
+  if (T < 0 || E <= 0 || k <= 0) return 0;
+  const int64_t C = moe_perm_chunks(static_cast<int64_t>(T) * k);
+  return sizeof(int32_t) * static_cast<size_t>(3 * E + 2 + C * E);
+}
+
 iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T, int E, int k,
                            const int32_t* expert_partition, int partition, int32_t* perm, int32_t* offsets,
                            int32_t* counts_ws, iso_stream stream) {
-  if (!c || T < 0 || E <= 0 || k <= 0 || E > 256) return ISO_ERR_INVALID_ARG;
+  if (!c || T < 0 || E <= 0 || k <= 0 || E > MOE_MAX_EXPERTS) return ISO_ERR_INVALID_ARG;
   if (!topk_ids || !perm || !offsets || !counts_ws) return ISO_ERR_INVALID_ARG;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
-  // unit prefixes are not needed by a caller of the plain permutation: write them over counts_ws + E.
+  // counts_ws: counts [E] | unit prefixes [E+1] x 2 (not needed by a caller of the plain
+  // permutation) | chunk histogram [chunks x E]
   int32_t* up = counts_ws + E;
   int32_t* dn = up + (E + 1);
-  return launch_moe_permute(topk_ids, static_cast<int64_t>(T) * k, E, expert_partition, partition, counts_ws, perm,
-                            offsets, up, 1, dn, 1, S(stream)) == cudaSuccess
+  int32_t* hist = dn + (E + 1);
+  return launch_moe_permute(topk_ids, static_cast<int64_t>(T) * k, E, expert_partition, partition, counts_ws, hist,
+                            perm, offsets, up, 1, dn, 1, S(stream)) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;
 }
@@ -360,10 +368,11 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
 //   y_slots [P x H] bf16 | x_perm [P x H] bf16 | h [P x F] bf16 |
-//   perm [P] | offsets [E+1] | counts [E] | up_prefix [E+1] | down_prefix [E+1] | part_map [E]
+//   perm [P] | offsets [E+1] | counts [E] | up_prefix [E+1] | down_prefix [E+1] | part_map [E] |
+//   hist [chunks x E] (the permutation's chunk histogram)
 namespace {
 struct MoeWs {
-  size_t y, xp, h, perm, offs, counts, up, dn, part, total;
+  size_t y, xp, h, perm, offs, counts, up, dn, part, hist, total;
 };
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
@@ -379,6 +388,7 @@ MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
   w.up = o; o += al((E + 1) * 4);
   w.dn = o; o += al((E + 1) * 4);
   w.part = o; o += al(E * 4);
+  w.hist = o; o += al(static_cast<size_t>(moe_perm_chunks(static_cast<int64_t>(P))) * E * 4);
   w.total = o;
   return w;
 }
@@ -394,7 +404,7 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
                                 const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
                                 int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream) {
   if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return ISO_ERR_INVALID_ARG;
-  if (E > 256 || !is_pow2(k) || k > 8) return ISO_ERR_UNSUPPORTED;
+  if (E > MOE_MAX_EXPERTS || !is_pow2(k) || k > 8) return ISO_ERR_UNSUPPORTED;
   if (T == 0) return ISO_OK;
   if (!x || !topk_ids || !topk_w || !W1 || !W2 || !out || !ws) return ISO_ERR_INVALID_ARG;
   const int L = iso_contract_leaf_count(c);
@@ -421,6 +431,7 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   int32_t* up = reinterpret_cast<int32_t*>(base + lay.up);
   int32_t* dn = reinterpret_cast<int32_t*>(base + lay.dn);
   int32_t* part = reinterpret_cast<int32_t*>(base + lay.part);
+  int32_t* hist = reinterpret_cast<int32_t*>(base + lay.hist);
   const int64_t P = static_cast<int64_t>(T) * k;
   if (expert_partition &&
       cudaMemcpyAsync(part, expert_partition, sizeof(int32_t) * E, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -435,8 +446,8 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   const int up_nb = F / 64, dn_nb = H / BN;
   trace("grouped_gemm_moe", T, E, k, num_partitions);
   for (int pi = 0; pi < num_partitions; ++pi) {
-    if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, perm, offs, up, up_nb, dn,
-                           dn_nb, s) != cudaSuccess)
+    if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, hist, perm, offs, up, up_nb,
+                           dn, dn_nb, s) != cudaSuccess)
       return ISO_ERR_CUDA;
     if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
     // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns

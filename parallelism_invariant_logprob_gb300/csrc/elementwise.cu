@@ -275,71 +275,124 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
 }
 
 // ---------------------------------------------------------------- MoE permute
-// Block e counts the pairs routed to expert e (exact integer sums).
-__global__ void moe_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
-                                 const int32_t* __restrict__ part_map, int part, int32_t* __restrict__ counts,
-                                 unsigned int* status) {
-  const int e = blockIdx.x;
-  __shared__ int warp_cnt[32];
-  int c = 0;
-  for (int64_t p = threadIdx.x; p < P; p += blockDim.x) {
-    const int id = ids[p];
-    c += (id == e);
-    if (e == 0 && (id < 0 || id >= E)) atomicOr(status, kDevBadToken);
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-  if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = c;
+// A counting sort in three passes over chunks of MOE_PERM_CHUNK pairs:
+//   hist     chunk c counts its pairs per expert                 -> hist[c][e]
+//   scan     hist[c][e] becomes the exclusive prefix over chunks; counts, offsets
+//            and the unit prefixes of the two grouped GEMMs follow from the totals
+//   scatter  chunk c writes each listed pair to offsets[e] + hist[c][e] + (its rank
+//            among the chunk's earlier pairs of expert e)
+// Every count is an exact integer and every pair's slot is determined by the pair order
+// alone, so perm lists the pairs of each expert in ascending pair order.
+
+__global__ void moe_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restrict__ hist,
+                                unsigned int* status) {
+  __shared__ int h[MOE_MAX_EXPERTS];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int tot = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += warp_cnt[i];
-    counts[e] = (part_map == nullptr || part_map[e] == part) ? tot : 0;
+  const int64_t p0 = static_cast<int64_t>(blockIdx.x) * MOE_PERM_CHUNK;
+  const int64_t p1 = min(P, p0 + MOE_PERM_CHUNK);
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int id = ids[p];
+    if (id >= 0 && id < E) atomicAdd(&h[id], 1);
+    else atomicOr(status, kDevBadToken);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = h[e];
+}
+
+// One block of 4 x MOE_MAX_EXPERTS threads: thread (g, e) walks a quarter of the chunks of
+// expert e.  Then counts (zero for experts outside the partition), offsets and the unit
+// prefixes (row blocks x n-tiles per expert) as exclusive scans over the experts.
+__global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
+    moe_scan_kernel(int32_t* __restrict__ hist, int C, int E, const int32_t* __restrict__ part_map, int part,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ up_prefix,
+                    int up_nblocks, int32_t* __restrict__ down_prefix, int down_nblocks) {
+  __shared__ int part_sum[4][MOE_MAX_EXPERTS];
+  __shared__ int scan[3][MOE_MAX_EXPERTS + 1];
+  const int g = threadIdx.x / MOE_MAX_EXPERTS;
+  const int e = threadIdx.x % MOE_MAX_EXPERTS;
+  const int per = (C + 3) / 4;
+  const int c0 = min(C, g * per), c1 = min(C, c0 + per);
+  int sum = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) sum += hist[static_cast<int64_t>(c) * E + e];
+  part_sum[g][e] = sum;
+  __syncthreads();
+  if (e < E) {
+    int run = 0;
+    for (int q = 0; q < g; ++q) run += part_sum[q][e];
+    for (int c = c0; c < c1; ++c) {
+      const int64_t i = static_cast<int64_t>(c) * E + e;
+      const int v = hist[i];
+      hist[i] = run;
+      run += v;
+    }
+  }
+  if (g == 0) {
+    int cnt = 0;
+    if (e < E) {
+      cnt = part_sum[0][e] + part_sum[1][e] + part_sum[2][e] + part_sum[3][e];
+      if (part_map != nullptr && part_map[e] != part) cnt = 0;
+      counts[e] = cnt;
+    }
+    const int mb = (cnt + BM - 1) / BM;
+    scan[0][e] = cnt;
+    scan[1][e] = mb * up_nblocks;
+    scan[2][e] = mb * down_nblocks;
+  }
+  __syncthreads();
+  // exclusive scans over the experts: thread (g < 3, e == 0) runs array g sequentially
+  if (e == 0 && g < 3) {
+    int run = 0;
+    for (int i = 0; i < E; ++i) {
+      const int v = scan[g][i];
+      scan[g][i] = run;
+      run += v;
+    }
+    scan[g][E] = run;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    offsets[i] = scan[0][i];
+    up_prefix[i] = scan[1][i];
+    down_prefix[i] = scan[2][i];
   }
 }
 
-// Block e writes its offset, its pairs in ascending pair order (stable
-// compaction with warp ballots), and the unit prefix entries of the two
-// grouped GEMMs.  Block E writes the totals.
-__global__ void moe_fill_kernel(const int32_t* __restrict__ ids, int64_t P, int E, const int32_t* __restrict__ counts,
-                                int32_t* __restrict__ perm, int32_t* __restrict__ offsets,
-                                int32_t* __restrict__ up_prefix, int up_nblocks, int32_t* __restrict__ down_prefix,
-                                int down_nblocks) {
-  const int e = blockIdx.x;
-  __shared__ int base_sh;
-  __shared__ int warp_tot[32];
-  if (threadIdx.x == 0) {
-    int off = 0, up = 0, dn = 0;
-    for (int i = 0; i < e; ++i) {
-      off += counts[i];
-      const int mb = (counts[i] + 127) / 128;
-      up += mb * up_nblocks;
-      dn += mb * down_nblocks;
-    }
-    offsets[e] = off;
-    up_prefix[e] = up;
-    down_prefix[e] = dn;
-    base_sh = off;
-  }
-  __syncthreads();
-  if (e == E) return;
-  if (counts[e] == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  int running = base_sh;
-  for (int64_t p0 = 0; p0 < P; p0 += blockDim.x) {
-    const int64_t p = p0 + threadIdx.x;
-    const bool hit = p < P && ids[p] == e;
-    const unsigned int bal = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) warp_tot[warp] = __popc(bal);
+__global__ void __launch_bounds__(MOE_PERM_THREADS)
+    moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, const int32_t* __restrict__ hist,
+                       const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ perm) {
+  constexpr int NW = MOE_PERM_THREADS / 32;
+  __shared__ int base[MOE_MAX_EXPERTS];
+  __shared__ int wcnt[NW][MOE_MAX_EXPERTS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    base[e] = offsets[e] + hist[static_cast<int64_t>(blockIdx.x) * E + e];
+  const int64_t p0 = static_cast<int64_t>(blockIdx.x) * MOE_PERM_CHUNK;
+  for (int r = 0; r < MOE_PERM_CHUNK / MOE_PERM_THREADS; ++r) {
+    for (int i = threadIdx.x; i < NW * MOE_MAX_EXPERTS; i += blockDim.x) (&wcnt[0][0])[i] = 0;
     __syncthreads();
-    int before = 0, all = 0;
-    for (int i = 0; i < nw; ++i) {
-      if (i < warp) before += warp_tot[i];
-      all += warp_tot[i];
-    }
-    if (hit) perm[running + before + __popc(bal & ((1u << lane) - 1u))] = static_cast<int32_t>(p);
-    running += all;
+    const int64_t p = p0 + r * MOE_PERM_THREADS + threadIdx.x;
+    int id = (p < P) ? ids[p] : -1;
+    if (id < 0 || id >= E || counts[id] == 0) id = -1;  // not listed (bad id, or outside the partition)
+    const unsigned int same = __match_any_sync(0xffffffffu, id);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (id >= 0 && rank == 0) wcnt[warp][id] = __popc(same);
     __syncthreads();
+    if (id >= 0) {
+      int pos = base[id] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w][id];
+      perm[pos] = static_cast<int32_t>(p);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int add = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) add += wcnt[w][e];
+      base[e] += add;
+    }
+    __syncthreads();  // wcnt is cleared for the next round only after every reader is done
   }
 }
 
@@ -358,22 +411,24 @@ __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int
   }
 }
 
-// out[t, c] = bf16_rn(tree_j rn(w[t,j] * y[t,j,c])): 8 columns per thread.
-__global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w, int T, int k,
-                                   int H, __nv_bfloat16* __restrict__ out) {
-  const int64_t nv = H / 8;
-  const int64_t n = static_cast<int64_t>(T) * nv;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = idx / nv;
-    const int64_t c = (idx - t * nv) * 8;
+// out[t, c] = bf16_rn(tree_j rn(w[t,j] * y[t,j,c])): 8 columns per thread.  Grid x covers a
+// row's 8-column vectors, grid y strides over the tokens (no per-element index division);
+// each thread has its k slot loads in flight together.
+__global__ void __launch_bounds__(256)
+    moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const float* __restrict__ w, int T, int k, int H,
+                       __nv_bfloat16* __restrict__ out) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= H / 8) return;
+  const int c = v * 8;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const int64_t slot0 = static_cast<int64_t>(t) * k;
     float acc[8][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k) {
-        const float wj = w[t * k + j];
-        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(y + (t * k + j) * H + c));
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        const float wj = w[slot0 + j];
+        const uint4 q4 = __ldcs(reinterpret_cast<const uint4*>(y + (slot0 + j) * H + c));
+        const uint32_t vw[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           acc[2 * q][j] = __fmul_rn(wj, bf16_lo(vw[q]));
@@ -387,7 +442,7 @@ __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const fl
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) o[q] = pack2(tree_sum<8>(acc[2 * q], k), tree_sum<8>(acc[2 * q + 1], k));
-    *reinterpret_cast<uint4*>(out + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    __stcs(reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H + c), make_uint4(o[0], o[1], o[2], o[3]));
   }
 }
 
@@ -458,15 +513,23 @@ cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* 
   return cudaGetLastError();
 }
 
+int64_t moe_perm_chunks(int64_t P) { return (P + MOE_PERM_CHUNK - 1) / MOE_PERM_CHUNK; }
+
 cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
-                               int32_t* counts,
-                               int32_t* perm, int32_t* offsets, int32_t* up_prefix, int up_nblocks,
-                               int32_t* down_prefix, int down_nblocks, cudaStream_t s) {
-  moe_count_kernel<<<E, 1024, 0, s>>>(ids, P, E, part_map, part, counts, device_status_ptr());
+                               int32_t* counts, int32_t* hist, int32_t* perm, int32_t* offsets, int32_t* up_prefix,
+                               int up_nblocks, int32_t* down_prefix, int down_nblocks, cudaStream_t s) {
+  const int64_t C = moe_perm_chunks(P);
+  if (C > 0) {
+    moe_hist_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, device_status_ptr());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  moe_scan_kernel<<<1, 4 * MOE_MAX_EXPERTS, 0, s>>>(hist, static_cast<int>(C), E, part_map, part, counts, offsets,
+                                                    up_prefix, up_nblocks, down_prefix, down_nblocks);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  moe_fill_kernel<<<E + 1, 1024, 0, s>>>(ids, P, E, counts, perm, offsets, up_prefix, up_nblocks, down_prefix,
-                                         down_nblocks);
+  if (e != cudaSuccess || C == 0) return e;
+  moe_scatter_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, counts, offsets,
+                                                                                perm);
   return cudaGetLastError();
 }
 
@@ -481,8 +544,12 @@ cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int3
 cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,
                                cudaStream_t s) {
   const int threads = 256;
-  moe_combine_kernel<<<grid_for(static_cast<int64_t>(T) * (H / 8), threads, sm_count() * 16), threads, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(y), w, T, k, H, reinterpret_cast<__nv_bfloat16*>(out));
+  const int gx = (H / 8 + threads - 1) / threads;
+  int gy = (sm_count() * 8 + gx - 1) / gx;
+  if (gy > T) gy = T;
+  if (gy > 65535) gy = 65535;
+  moe_combine_kernel<<<dim3(gx, gy), threads, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(y), w, T, k, H,
+                                                      reinterpret_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

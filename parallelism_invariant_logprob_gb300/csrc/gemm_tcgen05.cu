@@ -88,12 +88,18 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U)
     U.rows_valid = min(BM, p.M - U.a_row0);
     U.chunk = chunk;
   } else {
-    int lo = 0, hi = p.E;  // largest e with prefix[e] <= u
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (p.g_unit_prefix[mid] <= u) lo = mid; else hi = mid;
+    // e = the largest expert with prefix[e] <= u (prefix is nondecreasing), found by the
+    // whole warp at once: each lane tests up to 8 entries, all loads in flight together,
+    // and the ballot counts give the number of entries <= u.  Every caller is a full warp.
+    const int lane = threadIdx.x & 31;
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+      const int e = j * 32 + lane;
+      const bool le = e < p.E && p.g_unit_prefix[e] <= u;
+      cnt += __popc(__ballot_sync(0xffffffffu, le));
     }
-    const int e = lo;
+    const int e = cnt - 1;
     const int local = u - p.g_unit_prefix[e];
     const int mb = local / p.n_blocks;
     const int nb = local - mb * p.n_blocks;

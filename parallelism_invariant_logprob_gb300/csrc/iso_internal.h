@@ -39,6 +39,9 @@ constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
 constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
+constexpr int MOE_MAX_EXPERTS = 256;
+constexpr int MOE_PERM_CHUNK = 1024;   // pairs per chunk of the permutation's counting sort
+constexpr int MOE_PERM_THREADS = 256;
 constexpr int EPI_STAGE_BYTES = 4 * 32 * BN * 2;  // 4 epilogue warps x 32 rows x 128 bf16
 
 // Logprob vocab tiling: statistics per 128-column tile, 19 tiles per chunk.

@@ -56,6 +56,27 @@ def test_permute_exact(c8):
         assert np.array_equal(perm.cpu().numpy()[:o_ref[-1]], p_ref)
 
 
+@pytest.mark.parametrize("T,E,k", [(4097, 128, 8), (3000, 256, 1), (1024, 7, 2)])
+def test_permute_many_chunks_exact(c8, T, E, k):
+    """The pair list spans many 1024-pair chunks of the counting sort (and a ragged
+    last chunk); the result must still be the stable sort, with and without a
+    partition of the experts."""
+    _, _, _, logits = inputs.moe_inputs(T, 8, E, 8, seed=T + E)
+    ids, _ = B.moe_route(c8, logits.to(DEV), k)
+    perm, offs = B.moe_permute(c8, ids, E)
+    p_ref, o_ref = oracle.moe_permute(ids.cpu().numpy(), E)
+    assert np.array_equal(offs.cpu().numpy(), o_ref)
+    assert np.array_equal(perm.cpu().numpy()[:o_ref[-1]], p_ref)
+    part = inputs.random_partition(E, 4, seed=E).to(DEV)
+    for p in range(4):
+        perm, offs = B.moe_permute(c8, ids, E, expert_partition=part, partition=p)
+        mask = (part.cpu().numpy() == p).astype(np.uint8)
+        p_ref, o_ref = oracle.moe_permute(ids.cpu().numpy(), E, mask)
+        assert np.array_equal(offs.cpu().numpy(), o_ref)
+        assert np.array_equal(perm.cpu().numpy()[:o_ref[-1]], p_ref)
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
 def test_combine_vs_oracle(c8):
     T, k, H = 50, 8, 256
     y = inputs.normal_bf16((T, k, H), 1.0, seed=5)
