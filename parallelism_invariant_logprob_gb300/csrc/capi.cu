@@ -121,11 +121,26 @@ namespace {
 void set_a_rows(GemmParams& p, int a_rows) {
   p.a_rows = a_rows;
   p.a_bytes = a_rows * BK * 2;
+  const int b_bytes = p.pair ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
   const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES;
-  int st = room / (p.a_bytes + B_STAGE_BYTES);
+  int st = room / (p.a_bytes + b_bytes);
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
-  p.epi_staged = (room - p.stages * (p.a_bytes + B_STAGE_BYTES) >= EPI_STAGE_BYTES) ? 1 : 0;
+  p.epi_staged = (room - p.stages * (p.a_bytes + b_bytes) >= EPI_STAGE_BYTES) ? 1 : 0;
+}
+
+// CTA pairs (M = 256 per MMA): units of 256 rows, 128-row A boxes, half the B tile per CTA.
+// A pair moves fewer bytes per MMA (more stages in flight), but the next tile's first leaves
+// wait at every tile boundary until both CTAs' epilogues have merged the last leaf (all four
+// TMEM buffers hold the tree there).  Measured on GB300: a win with leaves of 1536 k
+// (K = 12288, 8 leaves: 1317 -> 1469 TFLOP/s), a loss with leaves of 512 k or fewer.
+constexpr int kPairMinLeafLen = 1024;
+bool use_pair(int rows, int K, int L) { return rows > BM && K / L >= kPairMinLeafLen; }
+
+void set_pair(GemmParams& p, int rows) {
+  p.pair = 1;
+  p.m_blocks = div_up(rows, 2 * BM);
+  set_a_rows(p, 128);
 }
 
 // Smallest A box that covers a single row block of `rows` rows.
@@ -175,7 +190,10 @@ iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t 
                     int N, int K, int L, cudaStream_t s) {
   if (!ensure_device_state()) return ISO_ERR_CUDA;
   GemmParams p = base_params(M, N, K, L);
-  if (p.m_blocks == 1) set_a_rows(p, a_rows_for(M));
+  if (p.m_blocks == 1)
+    set_a_rows(p, a_rows_for(M));
+  else if (use_pair(M, K, L))
+    set_pair(p, M);
   CUtensorMap tA, tB;
   iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, static_cast<uint32_t>(p.a_rows));
   if (st != ISO_OK) return st;
@@ -185,9 +203,8 @@ iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t 
   p.num_units = p.m_blocks * p.n_blocks;
   p.out = C;
   p.ldo = ldc;
-  const int grid = p.num_units < sm_count() ? p.num_units : sm_count();
   trace(epi == EPI_BF16 ? "gemm" : "gemm_partial", M, N, K, L);
-  return launch_gemm(epi, tA, tB, p, grid, s);
+  return launch_gemm(epi, tA, tB, p, p.num_units, s);
 }
 
 }  // namespace
@@ -294,7 +311,10 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (ws_bytes < iso_selected_logprob_workspace(c, T, V)) return ISO_ERR_WORKSPACE;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
   GemmParams p = base_params(T, V, H, L);
-  if (p.m_blocks == 1) set_a_rows(p, a_rows_for(T));
+  if (p.m_blocks == 1)
+    set_a_rows(p, a_rows_for(T));
+  else if (use_pair(T, H, L))
+    set_pair(p, T);
   CUtensorMap tA, tB;
   iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
   if (st != ISO_OK) return st;
@@ -311,9 +331,8 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   p.ws_stats = stats;
   p.ws_zsel = zsel;
   p.V = V;
-  const int grid = p.num_units < sm_count() ? p.num_units : sm_count();
   trace(tiles ? "selected_logprob[tile units]" : "selected_logprob[chunk units]", T, H, V, p.num_chunks);
-  st = launch_gemm(EPI_LOGPROB, tA, tB, p, grid, S(stream));
+  st = launch_gemm(EPI_LOGPROB, tA, tB, p, p.num_units, S(stream));
   if (st != ISO_OK) return st;
   return launch_lse_finalize(stats, zsel, ids, out, T, lp_num_chunks(V), V, tiles ? 1 : 0, lp_num_tiles(V),
                              LP_CHUNK_TILES, S(stream)) == cudaSuccess
@@ -349,7 +368,7 @@ iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T
   int32_t* dn = up + (E + 1);
   int32_t* hist = dn + (E + 1);
   return launch_moe_permute(topk_ids, static_cast<int64_t>(T) * k, E, expert_partition, partition, counts_ws, hist,
-                            perm, offsets, up, 1, dn, 1, S(stream)) == cudaSuccess
+                            perm, offsets, up, 1, dn, 1, BM, S(stream)) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;
 }
@@ -365,6 +384,11 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
   if (!ensure_device_state()) return ISO_ERR_CUDA;
   return launch_moe_combine(y_slots, topk_w, T, k, H, out, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
+
+// The expert layer's grouped GEMMs run on single CTAs (units of 128 rows of one expert): its
+// leaves (H / L, F / L) are short, where CTA pairs lose (1.12 -> 1.84 ms per layer measured
+// at T = 8192, H = 2048, F = 768, E = 128, k = 8).
+constexpr bool kMoePairs = false;
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
 //   y_slots [P x H] bf16 | x_perm [P x H] bf16 | h [P x F] bf16 |
@@ -444,10 +468,11 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   if (st == ISO_OK) st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, BK);
   if (st != ISO_OK) return st;
   const int up_nb = F / 64, dn_nb = H / BN;
+  const int unit_rows = kMoePairs ? 2 * BM : BM;  // rows of an expert per grouped work unit
   trace("grouped_gemm_moe", T, E, k, num_partitions);
   for (int pi = 0; pi < num_partitions; ++pi) {
     if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, hist, perm, offs, up, up_nb,
-                           dn, dn_nb, s) != cudaSuccess)
+                           dn, dn_nb, unit_rows, s) != cudaSuccess)
       return ISO_ERR_CUDA;
     if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
     // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns
@@ -462,6 +487,10 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
     p.E = E;
     p.out = hb;
     p.ldo = F;
+    if (kMoePairs) {
+      p.pair = 1;
+      set_a_rows(p, 128);
+    }
     st = launch_gemm(EPI_SWIGLU, tX, tW1, p, sm_count(), s);
     if (st != ISO_OK) return st;
     GemmParams q = base_params(0, H, F, L);
@@ -472,6 +501,10 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
     q.out = y;
     q.ldo = H;
     q.row_scatter = perm;
+    if (kMoePairs) {
+      q.pair = 1;
+      set_a_rows(q, 128);
+    }
     st = launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s);
     if (st != ISO_OK) return st;
   }

@@ -306,7 +306,7 @@ __global__ void moe_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int 
 __global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
     moe_scan_kernel(int32_t* __restrict__ hist, int C, int E, const int32_t* __restrict__ part_map, int part,
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ up_prefix,
-                    int up_nblocks, int32_t* __restrict__ down_prefix, int down_nblocks) {
+                    int up_nblocks, int32_t* __restrict__ down_prefix, int down_nblocks, int unit_rows) {
   __shared__ int part_sum[4][MOE_MAX_EXPERTS];
   __shared__ int scan[3][MOE_MAX_EXPERTS + 1];
   const int g = threadIdx.x / MOE_MAX_EXPERTS;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
       if (part_map != nullptr && part_map[e] != part) cnt = 0;
       counts[e] = cnt;
     }
-    const int mb = (cnt + BM - 1) / BM;
+    const int mb = (cnt + unit_rows - 1) / unit_rows;
     scan[0][e] = cnt;
     scan[1][e] = mb * up_nblocks;
     scan[2][e] = mb * down_nblocks;
@@ -517,7 +517,8 @@ int64_t moe_perm_chunks(int64_t P) { return (P + MOE_PERM_CHUNK - 1) / MOE_PERM_
 
 cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
                                int32_t* counts, int32_t* hist, int32_t* perm, int32_t* offsets, int32_t* up_prefix,
-                               int up_nblocks, int32_t* down_prefix, int down_nblocks, cudaStream_t s) {
+                               int up_nblocks, int32_t* down_prefix, int down_nblocks, int unit_rows,
+                               cudaStream_t s) {
   const int64_t C = moe_perm_chunks(P);
   if (C > 0) {
     moe_hist_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, device_status_ptr());
@@ -525,7 +526,7 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32
     if (e != cudaSuccess) return e;
   }
   moe_scan_kernel<<<1, 4 * MOE_MAX_EXPERTS, 0, s>>>(hist, static_cast<int>(C), E, part_map, part, counts, offsets,
-                                                    up_prefix, up_nblocks, down_prefix, down_nblocks);
+                                                    up_prefix, up_nblocks, down_prefix, down_nblocks, unit_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || C == 0) return e;
   moe_scatter_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, counts, offsets,

@@ -39,6 +39,8 @@
 // assignment is a FIFO free list replayed identically by the MMA thread and
 // the epilogue, so both sides agree without exchanging buffer ids.
 #include <cuda_bf16.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include "iso_internal.h"
 #include "iso_ptx.cuh"
@@ -61,7 +63,9 @@ __device__ __forceinline__ int unit_count(const GemmParams& p) {
   return p.num_units;
 }
 
-__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U) {
+// Unit u of the launch.  With CTA pairs (cl = 2) a unit covers 2 x 128 rows: the CTA of
+// rank r takes the 128-row block 2 mb + r of it (rows_valid <= 0: a block past the rows).
+__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U, int cl, int rank) {
   if (p.unit_mode == UNIT_GEMM) {
     const int per_group = p.group_m * p.n_blocks;
     const int g = u / per_group;
@@ -70,7 +74,7 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U)
     const int gsz = min(p.group_m, p.m_blocks - gm0);
     const int mb = gm0 + r % gsz;
     const int nb = r / gsz;
-    U.a_row0 = mb * BM;
+    U.a_row0 = (mb * cl + rank) * BM;
     U.b_row0 = 0;
     U.n_tile0 = nb;
     U.n_tiles = 1;
@@ -81,7 +85,7 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U)
     // share its W columns in L2.
     const int chunk = u / p.m_blocks;
     const int rb = u - chunk * p.m_blocks;
-    U.a_row0 = rb * BM;
+    U.a_row0 = (rb * cl + rank) * BM;
     U.b_row0 = 0;
     U.n_tile0 = chunk * p.chunk_tiles;
     U.n_tiles = min(p.chunk_tiles, p.n_blocks - U.n_tile0);
@@ -105,11 +109,11 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U)
     const int nb = local - mb * p.n_blocks;
     const int off = p.g_offsets[e];
     const int ne = p.g_offsets[e + 1] - off;
-    U.a_row0 = off + mb * BM;
+    U.a_row0 = off + (mb * cl + rank) * BM;
     U.b_row0 = e * p.K;
     U.n_tile0 = nb;
     U.n_tiles = 1;
-    U.rows_valid = min(BM, ne - mb * BM);
+    U.rows_valid = min(BM, ne - (mb * cl + rank) * BM);
     U.chunk = 0;
   }
 }
@@ -235,18 +239,42 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 
 }  // namespace
 
-// M = 128, N = 128, A K-major, B MN-major, bf16 x bf16 -> fp32.
+// M = 128 (one CTA) or 256 (CTA pair), N = 128, A K-major, B MN-major, bf16 x bf16 -> fp32.
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+constexpr uint32_t kIdescPair = idesc_bf16_f32(2 * BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
 
-template <int EPI>
+// An epilogue warp is done with TMEM buffer b (its tcgen05 accesses completed and fenced).
+// One CTA: every epilogue thread arrives (count 128).  CTA pair: the MMA issuer sits in rank
+// 0, so one lane per warp of either CTA arrives on rank 0's barrier (count 8).
+template <bool PAIR>
+__device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int lane) {
+  if (PAIR) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(cluster_addr(&buf_free[b], 0));
+  } else {
+    mbar_arrive(&buf_free[b]);
+  }
+}
+
+// PAIR: launched as clusters of two CTAs (ranks 0, 1); rank 0 issues M = 256 MMAs over both,
+// each CTA loads its own 128 A rows and one 64-column half of the B tile (the gate or up half
+// for SwiGLU), with the loads of both counted on rank 0's stage barrier; the MMA commits
+// arrive on the barriers of both CTAs.  Per CTA a stage is then 24 KB instead of 32 KB, so
+// more stages fit and each SM moves three quarters of the bytes per MMA.
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     iso_leaf_tree_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int BSTAGE = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // B bytes per stage in this CTA
+  constexpr int CL = PAIR ? 2 : 1;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int nstages = p.stages;
   const uint32_t b_region = static_cast<uint32_t>(nstages * p.a_bytes);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + b_region + nstages * B_STAGE_BYTES);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + b_region + nstages * BSTAGE);
   uint64_t* empty_bar = full_bar + MAX_STAGES;
   uint64_t* leaf_full = empty_bar + MAX_STAGES;
   uint64_t* buf_free = leaf_full + NUM_TMEM_BUFS;
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   // from the phase before.
   volatile uint32_t* next_leaf = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   // bf16 output staging (valid when p.epi_staged): 8 KB per epilogue warp
-  uint8_t* epi_stage = smem + b_region + nstages * B_STAGE_BYTES + GEMM_BARRIER_BYTES;
+  uint8_t* epi_stage = smem + b_region + nstages * BSTAGE + GEMM_BARRIER_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -273,7 +301,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < NUM_TMEM_BUFS; ++b) {
       mbar_init(&leaf_full[b], 1);
-      mbar_init(&buf_free[b], 128);
+      mbar_init(&buf_free[b], PAIR ? 8 : 128);
     }
     mbar_init(&drain_bar[0], 1);
     mbar_init(&drain_bar[1], 1);
@@ -283,11 +311,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nunits = unit_count(p);
@@ -308,25 +342,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t round = 0;
       uint32_t issued = 0;  // stages issued by this thread
       bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      for (int u = unit0; u < nunits && ok; u += unit_step) {
         Unit U;
-        decode_unit(p, u, U);
+        decode_unit(p, u, U, CL, rank);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           const int n0 = (U.n_tile0 + t) * p.b_tile_cols;
           for (int g = 0; g < p.L / per && ok; ++g) {
             for (int j = 0; j < p.kb_per_leaf; ++j) {
               const int kx = (g * per + me) * p.leaf_len + j * BK;
-              if (!mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
+              const bool freed =
+                  PAIR ? mbar_wait_cluster(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)
+                       : mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status);
+              if (!freed) {
                 ok = false;
                 break;
               }
               uint8_t* sA = smem + stage * p.a_bytes;
-              uint8_t* sB = smem + b_region + stage * B_STAGE_BYTES;
+              uint8_t* sB = smem + b_region + stage * BSTAGE;
               if (leader) {
-                mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + B_STAGE_BYTES));
-                tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
-                tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
-                tma_load_2d(sB + B_STAGE_BYTES / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
+                if (PAIR) {
+                  // both CTAs' bytes complete on rank 0's barrier, which rank 0 arms for both
+                  const uint32_t fb = cluster_addr(&full_bar[stage], 0);
+                  if (rank == 0)
+                    mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(2 * (p.a_bytes + BSTAGE)));
+                  tma_load_2d_pair(sA, &tmA, fb, kx, U.a_row0);
+                  tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);
+                } else {
+                  mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + BSTAGE));
+                  tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
+                  tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+                  tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
+                }
               }
               __syncwarp();
               ++issued;
@@ -339,8 +385,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // drain: wait (bounded) for every load this thread issued to land.  This thread's k-th
+      if (!ok && rank == 0) {
+        // drain: wait (bounded) for every load this thread issued to land (rank 0's barriers
+        // also count the peer's loads of the stages it armed).  This thread's k-th
         // stage index is me + per*k; stage s was last filled in the round of its latest use.
         const uint32_t total = issued;
         for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(nstages / per); ++back) {
@@ -355,7 +402,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (warp == 1 || warp == 2) {
     const int me = warp - 1;  // leaf parity issued by this warp
-    if (me < per) {
+    if (me < per && rank == 0) {
       // ----------------------------------------------------------------- MMA
       // The whole warp runs the loop (warp-uniform values); one elected lane issues.
       const bool leader = elect_one();
@@ -371,9 +418,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(0, 8192, 1024);
       uint32_t seq = 0;  // sequence number of the current leaf (all tiles, both threads' leaves)
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      for (int u = unit0; u < nunits && ok; u += unit_step) {
         Unit U;
-        decode_unit(p, u, U);
+        decode_unit(p, u, U, CL, rank);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           for (int leaf = 0; leaf < p.L && ok; ++leaf, ++seq) {
             // replay of the tree bookkeeping (identical in both issuers and the epilogue)
@@ -389,7 +436,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 break;
               }
               if (reuse) {
-                if (!mbar_wait(&buf_free[b], wpar, p.timeout_ns, abort_flag, p.status)) {
+                const bool got = PAIR ? mbar_wait_cluster(&buf_free[b], wpar, p.timeout_ns, abort_flag, p.status)
+                                      : mbar_wait(&buf_free[b], wpar, p.timeout_ns, abort_flag, p.status);
+                if (!got) {
                   ok = false;
                   break;
                 }
@@ -398,7 +447,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               if (per == 2) *next_leaf = seq + 1u;
               const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
               for (int j = 0; j < p.kb_per_leaf; ++j) {
-                if (!mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)) {
+                const bool landed = PAIR ? mbar_wait_cluster(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status)
+                                         : mbar_wait(&full_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status);
+                if (!landed) {
                   ok = false;
                   break;
                 }
@@ -407,22 +458,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // B: MN-major, 64-column chunks 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO);
                 //    +2 KB (128 units) per K=16.
                 const uint32_t a_lo = (smem_base + stage * p.a_bytes) >> 4;
-                const uint32_t b_lo = (smem_base + b_region + stage * B_STAGE_BYTES) >> 4;
+                const uint32_t b_lo = (smem_base + b_region + stage * BSTAGE) >> 4;
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
                 const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
                 const int rem = p.leaf_len - j * BK;
                 if (leader) {
-                  if (rem >= BK) {
-                    umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
-                    umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
-                    umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
-                    umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+                  if (PAIR) {
+                    if (rem >= BK) {
+                      umma_bf16_pair(d, adesc, bdesc, kIdescPair, j != 0 ? 1u : 0u);
+                      umma_bf16_pair(d, adesc + 2, bdesc + 128, kIdescPair, 1u);
+                      umma_bf16_pair(d, adesc + 4, bdesc + 256, kIdescPair, 1u);
+                      umma_bf16_pair(d, adesc + 6, bdesc + 384, kIdescPair, 1u);
+                    } else {
+                      for (int i = 0; i < rem / UMMA_K; ++i)
+                        umma_bf16_pair(d, adesc + 2 * i, bdesc + 128 * i, kIdescPair, (j != 0 || i != 0) ? 1u : 0u);
+                    }
+                    if (j == p.kb_per_leaf - 1) umma_commit_pair(&leaf_full[b], 3);
+                    umma_commit_pair(&empty_bar[stage], 3);
                   } else {
-                    for (int i = 0; i < rem / UMMA_K; ++i)
-                      umma_bf16(d, adesc + 2 * i, bdesc + 128 * i, kIdesc, (j != 0 || i != 0) ? 1u : 0u);
+                    if (rem >= BK) {
+                      umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
+                      umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
+                      umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
+                      umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+                    } else {
+                      for (int i = 0; i < rem / UMMA_K; ++i)
+                        umma_bf16(d, adesc + 2 * i, bdesc + 128 * i, kIdesc, (j != 0 || i != 0) ? 1u : 0u);
+                    }
+                    if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
+                    umma_commit(&empty_bar[stage]);
                   }
-                  if (j == p.kb_per_leaf - 1) umma_commit(&leaf_full[b]);
-                  umma_commit(&empty_bar[stage]);
                 }
                 __syncwarp();
                 stage += per;
@@ -439,7 +504,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       // drain: every MMA issued by this warp completes before TMEM is released
-      if (leader) umma_commit(&drain_bar[me]);
+      if (leader) {
+        if (PAIR)
+          umma_commit_pair(&drain_bar[me], 1);
+        else
+          umma_commit(&drain_bar[me]);
+      }
       __syncwarp();
       const uint32_t a = smem_u32(&drain_bar[me]);
       const uint64_t t0 = globaltimer_ns();
@@ -460,9 +530,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tb.init();
     uint32_t fill_par = 0u;  // bit b: parity of the next leaf_full phase of buffer b
     bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+    for (int u = unit0; u < nunits && ok; u += unit_step) {
       Unit U;
-      decode_unit(p, u, U);
+      decode_unit(p, u, U, CL, rank);
       const bool row_ok = row_in_tile < U.rows_valid;
       const int row = U.a_row0 + row_in_tile;
       float run_m = -INFINITY, run_s = 0.f;  // logprob: running chunk statistics
@@ -477,8 +547,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tb.push(b);
           // One thread polls the barrier; the other epilogue warps sleep in a hardware named
           // barrier so they take no issue slots from the TMA and MMA threads.
-          if (threadIdx.x == 128)
-            (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+          if (threadIdx.x == 128) {
+            if (PAIR)
+              (void)mbar_wait_cluster(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+            else
+              (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+          }
           named_bar_sync(1, 128);
           if (*abort_flag) {
             ok = false;
@@ -512,7 +586,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&buf_free[rb]);
+            release_tmem_buf<PAIR>(buf_free, rb, lane);
             tb.push_free(rb);
           }
         }
@@ -531,7 +605,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
           tc_fence_before();
-          mbar_arrive(&buf_free[root]);
+          release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
           uint4 hw[8];
@@ -566,7 +640,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
           tc_fence_before();
-          mbar_arrive(&buf_free[root]);
+          release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
           if (EPI == EPI_BF16 && p.epi_staged) {
@@ -619,7 +693,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
           tc_fence_before();
-          mbar_arrive(&buf_free[root]);
+          release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
           const int sel_off = sel - n0;
@@ -657,7 +731,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         if (!released) {
           tc_fence_before();
-          mbar_arrive(&buf_free[root]);
+          release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
         }
       }
@@ -670,59 +744,107 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) {
+    // After an abort the peer's last loads may still be landing in this CTA's shared memory
+    // (their completion is counted on rank 0, which may have stopped waiting): give them time.
+    if (*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+    cluster_sync_all();  // neither CTA leaves while the other may still touch its memory
+  }
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+namespace {
+
+template <int EPI, bool PAIR>
+iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
+                      cudaStream_t s) {
+  static int attr_dev = -1;  // device whose function attributes are set
+  static int slots = 0;      // CTAs (pairs: clusters) resident at once on that device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
+  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR>;
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
+      return ISO_ERR_CUDA;
+    slots = sm_count();
+    if (PAIR) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+        return ISO_ERR_CUDA;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
+      cfg.blockDim = dim3(GEMM_THREADS);
+      cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return ISO_ERR_CUDA;
+      slots = clusters;
+    }
+    attr_dev = dev;
+    const char* tr = getenv("ISO_TRACE");
+    if (tr && tr[0] == '1')
+      fprintf(stderr, "[iso] gemm kernel epi=%d pair=%d: %d %s resident\n", EPI, PAIR ? 1 : 0, slots,
+              PAIR ? "CTA pairs" : "CTAs");
+  }
+  const int units = max_units < slots ? max_units : slots;
+  if (units <= 0) return ISO_OK;
+  if (!PAIR) {
+    kern<<<units, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return ISO_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+}  // namespace
+
+iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                        cudaStream_t s) {
-  static bool attr_set[4] = {false, false, false, false};
-  cudaError_t e = cudaSuccess;
+  const bool pair = p.pair != 0;
   switch (epi) {
     case EPI_BF16:
-      if (!attr_set[0]) {
-        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES);
-        attr_set[0] = (e == cudaSuccess);
-      }
-      if (e == cudaSuccess)
-        iso_leaf_tree_gemm_kernel<EPI_BF16><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
-      break;
+      return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s)
+                  : launch_one<EPI_BF16, false>(tmA, tmB, p, max_units, s);
     case EPI_F32:
-      if (!attr_set[1]) {
-        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES);
-        attr_set[1] = (e == cudaSuccess);
-      }
-      if (e == cudaSuccess)
-        iso_leaf_tree_gemm_kernel<EPI_F32><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
-      break;
+      return pair ? launch_one<EPI_F32, true>(tmA, tmB, p, max_units, s)
+                  : launch_one<EPI_F32, false>(tmA, tmB, p, max_units, s);
     case EPI_SWIGLU:
-      if (!attr_set[3]) {
-        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES);
-        attr_set[3] = (e == cudaSuccess);
-      }
-      if (e == cudaSuccess)
-        iso_leaf_tree_gemm_kernel<EPI_SWIGLU><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
-      break;
+      return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s)
+                  : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s);
     case EPI_LOGPROB:
-      if (!attr_set[2]) {
-        e = cudaFuncSetAttribute(iso_leaf_tree_gemm_kernel<EPI_LOGPROB>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
-        attr_set[2] = (e == cudaSuccess);
-      }
-      if (e == cudaSuccess)
-        iso_leaf_tree_gemm_kernel<EPI_LOGPROB><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
-      break;
+      return pair ? launch_one<EPI_LOGPROB, true>(tmA, tmB, p, max_units, s)
+                  : launch_one<EPI_LOGPROB, false>(tmA, tmB, p, max_units, s);
     default:
       return ISO_ERR_INVALID_ARG;
   }
-  if (e != cudaSuccess) return ISO_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
 
 }  // namespace iso

@@ -59,6 +59,7 @@ struct GemmParams {
   int kb_per_leaf; // ceil(leaf_len / BK)
   int stages;      // pipeline stages (even, <= MAX_STAGES)
   int epi_staged;  // 1: bf16 roots go out through the shared-memory staging area
+  int pair;        // 1: clusters of two CTAs, M = 256 MMAs; a unit covers 2 x 128 rows
   int a_rows;      // rows of the A box (16, 32, 64 or 128)
   int a_bytes;     // a_rows * 128
   int b_tile_cols; // B columns advanced per tile (128; 64 for the SwiGLU gate/up pairing)
@@ -97,8 +98,9 @@ bool trace_enabled();
 iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                           uint32_t box_cols, uint32_t box_rows);
 
-// Launchers (gemm_tcgen05.cu).
-iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+// Launchers (gemm_tcgen05.cu).  max_units bounds the number of CTAs (p.pair: CTA pairs)
+// worth launching; the grid is that or the number that fit on the GPU at once.
+iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                        cudaStream_t s);
 
 }  // namespace iso

@@ -154,6 +154,39 @@ def test_config2_shapes_sampled_rows_and_ranks(c8, K, N):
         assert same_bits(B.tree_combine(c8, S), full), R
 
 
+@pytest.mark.parametrize("M", [129, 200, 257, 384])
+def test_cta_pair_units_ragged_exact(c8, M):
+    """Leaves of 1024 k (K = 8192, 8 leaves) run on CTA pairs: a unit is 256 rows, the
+    second CTA's 128 rows may be partly or wholly past M.  Exact integer inputs: the bits
+    must equal the oracle's, and every row must equal its single-row (one CTA) result."""
+    K, N = 8192, 136
+    A = inputs.small_int_bf16((M, K), -3, 3, seed=M)
+    Bm = inputs.small_int_bf16((K, N), -3, 3, seed=N + M)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    C = B.gemm(c8, Ad, Bd)
+    assert np.array_equal(bits(C), oracle.gemm(bits(A), bits(Bm), 8)), first_diff(
+        C, torch.from_numpy(oracle.gemm(bits(A), bits(Bm), 8).view(np.int16)).view(torch.bfloat16))
+    for r in (0, 128, M - 1):
+        assert same_bits(B.gemm(c8, Ad[r:r + 1].contiguous(), Bd), C[r:r + 1]), r
+
+
+def test_cta_pair_normal_inputs_and_partials(c8):
+    """Normal inputs through CTA pairs: tolerance against the oracle on sampled rows, and
+    the R-rank partial + combine path (also on pairs while K / (8 / R) >= 1024) reproduces the
+    single pass bit for bit."""
+    M, K, N = 300, 8192, 256
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=4)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c8, Ad, Bd)
+    rows = torch.tensor([0, 127, 128, 255, 256, 299])
+    check_row_tolerance(full[rows.to(DEV)], oracle.gemm_root(bits(A[rows]), bits(Bm), 8))
+    for R in (2, 4):
+        Kl = K // R
+        S = torch.stack([B.gemm_leaf_partial(c8, r, R, Ad[:, r * Kl:(r + 1) * Kl].contiguous(),
+                                             Bd[r * Kl:(r + 1) * Kl]) for r in range(R)])
+        assert same_bits(B.tree_combine(c8, S), full), R
+
+
 @pytest.mark.slow
 def test_config2_full_size_m4096_sampled(c8):
     K, N, M = 4096, 4096, 4096

@@ -132,6 +132,22 @@ def test_rmsnorm_constant_row(c8):
     assert torch.all(y0.float() == 0.0)
 
 
+@pytest.mark.parametrize("T", [400, 600])
+def test_logprob_cta_pairs_match_single_rows(c8, T):
+    """H = 8192 with 8 leaves (1024 k each) runs the LM head on CTA pairs (256-row units;
+    T = 400 with one 128-column tile per unit, T = 600 with whole chunks); every row must
+    equal its own single-row (one CTA) result, and sampled rows the oracle."""
+    H, V = 8192, 128 * 19 * 2 + 40
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=8, device=DEV)
+    full = B.selected_logprob(c8, h, W, ids)
+    for t in (0, 255, 256, T - 1):
+        one = B.selected_logprob(c8, h[t:t + 1].contiguous(), W, ids[t:t + 1].contiguous())
+        assert f32_same(one, full[t:t + 1]), t
+    rows = torch.tensor([0, 300, T - 1], device=DEV)
+    ref = oracle.selected_logprob(bits(h[rows]), bits(W), ids[rows].cpu().numpy(), 8)
+    assert np.max(np.abs(full[rows].cpu().double().numpy() - ref["out"])) <= 1e-3
+
+
 def test_logprob_tile_units_and_chunk_units_agree_bitwise(c8):
     """Up to 512 rows every 128-column tile is its own work unit and the chunk fold
     happens in the finalize kernel; above that a CTA folds a whole chunk.  Both
