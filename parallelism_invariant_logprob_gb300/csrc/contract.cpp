@@ -125,9 +125,10 @@ std::string serialize(const iso_contract& c) {
   char buf[2048];
   snprintf(buf, sizeof buf,
            "{\"identity\":\"numerical_policy\",\"contract_version\":1,"
-           "\"impl\":{\"id\":\"iso_leaf_tree_tcgen05\",\"version\":1,\"arch\":\"sm_103a\"},"
+           "\"impl\":{\"id\":\"iso_leaf_tree_tcgen05\",\"version\":2,\"arch\":\"sm_103a\"},"
            "\"gemm\":{\"leaves\":%d,\"rank_to_leaf\":\"contiguous\","
-           "\"leaf_chain\":{\"instr\":\"tcgen05.mma.cta_group::1.kind::f16\",\"m\":128,\"n\":128,\"k\":16,"
+           "\"leaf_chain\":{\"instr\":\"tcgen05.mma.kind::f16\",\"rows_per_cta\":128,"
+           "\"cta_group\":\"1(m=128)|2(m=256)\",\"n\":128,\"k\":16,"
            "\"order\":\"ascending_k\",\"first\":\"overwrite\"},"
            "\"tree\":\"%s\",\"tree_add\":\"fp32_rn\",\"acc_dtype\":\"%s\",\"out_dtype\":\"%s\","
            "\"convert\":\"once_at_root_rn\"},"
