@@ -67,8 +67,11 @@ __global__ void tree_combine_kernel(const float* __restrict__ S, int64_t lds, in
 // One warp per row.  Lane l owns the 8-element vectors v = l, l+32, l+64, ...
 // and sums x^2 over them in ascending order (rn multiply, rn add); an xor
 // shuffle tree 16,8,4,2,1 completes the row sum, identical in every lane.
+// Two blocks (16 warps, 16 rows in flight) per SM for rows of up to 4096: with the compiler's
+// free choice one 174-register block per SM kept too few bytes in flight for HBM (5.3 TB/s at
+// T = 262144, H = 4096 on GB300; 6.1 TB/s with this bound, bitwise identical output).
 template <int VPL>  // vectors per lane when H == 256*VPL (kept in registers); 0 = generic
-__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+__global__ void __launch_bounds__(256, (VPL > 0 && VPL <= 16) ? 2 : 1) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
                                float eps, __nv_bfloat16* __restrict__ y, int T, int H) {
   const int lane = threadIdx.x & 31;
   const int warps_per_block = blockDim.x >> 5;
