@@ -235,8 +235,9 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
       v[i] = e < E ? logits[t * E + e] : -INFINITY;
       taken[i] = e >= E;
     }
-    float sel_l[32];
-    int sel_e[32];
+    // lane j keeps the j-th selection (k <= 32), so nothing goes to local memory
+    float my_l = -INFINITY;
+    int my_e = 0;
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
@@ -260,19 +261,18 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
         if (lane + 32 * i == be) taken[i] = true;
-      if (j < 32) {
-        sel_l[j] = bv;
-        sel_e[j] = be;
+      if (lane == j) {
+        my_l = bv;
+        my_e = be;
       }
     }
-    if (lane == 0) {
-      const float m = sel_l[0];
-      float s = 0.f;
-      for (int j = 0; j < k; ++j) s = __fadd_rn(s, expf(__fsub_rn(sel_l[j], m)));
-      for (int j = 0; j < k; ++j) {
-        ids[t * k + j] = sel_e[j];
-        w[t * k + j] = __fdiv_rn(expf(__fsub_rn(sel_l[j], m)), s);
-      }
+    const float m = __shfl_sync(0xffffffffu, my_l, 0);
+    const float ex = lane < k ? expf(__fsub_rn(my_l, m)) : 0.f;
+    float s = 0.f;  // slot order: s = ((e_0 + e_1) + e_2) + ...
+    for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(0xffffffffu, ex, j));
+    if (lane < k) {
+      ids[t * k + lane] = my_e;
+      w[t * k + lane] = __fdiv_rn(ex, s);
     }
   }
 }
@@ -399,7 +399,8 @@ __global__ void __launch_bounds__(MOE_PERM_THREADS)
   }
 }
 
-// x_perm[i] = x[perm[i] / k]: one warp per row, 16-byte vectors.
+// x_perm[i] = x[perm[i] / k]: one warp per row, 16-byte vectors, 8 loads per lane in flight
+// before their stores (one load at a time per lane left the copy latency-bound).
 __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm,
                                   const int32_t* __restrict__ total, int k, int H, __nv_bfloat16* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
@@ -410,7 +411,15 @@ __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int
     const int t = perm[i] / k;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(i) * H);
-    for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 8) {
+      uint4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (v0 + 32 * u < nvec) r[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (v0 + 32 * u < nvec) dst[v0 + 32 * u] = r[u];
+    }
   }
 }
 
