@@ -154,11 +154,17 @@ iso_status iso_rmsnorm(const iso_contract* c, const iso_bf16* x, const iso_bf16*
  * [VeXact paper, §2 Eq. (1): delta_t compares exactly these values]
  * h: [T x H] bf16 row-major; W: [H x V] bf16 row-major (the LM head as K x N);
  * ids: [T] int32; out: [T] fp32.  H % (16 L) == 0; V % 8 == 0; V <= 622592.
- * ws: device workspace of at least iso_selected_logprob_workspace(c, T, V)
- * bytes, 16-byte aligned (ISO_ERR_WORKSPACE otherwise).  A token id outside
- * [0, V) yields out[t] = NaN and sets ISO_ERR_BAD_TOKEN_ID in the device
- * status word. */
+ * ws: device workspace, 16-byte aligned, of at least
+ * iso_selected_logprob_min_workspace(c, T, V) bytes (ISO_ERR_WORKSPACE
+ * otherwise).  With iso_selected_logprob_workspace(c, T, V) bytes or more
+ * the call also stores per-tile statistics and runs one 128-column tile per
+ * work unit, which balances the GPU better; with less it runs one vocab
+ * chunk per unit.  Both schedules fold the same statistics in the same order,
+ * so the results are bit-identical.  A token id outside [0, V) yields
+ * out[t] = NaN and sets ISO_ERR_BAD_TOKEN_ID in the device status word.
+ * Both size queries return 0 for invalid arguments. */
 size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V);
+size_t iso_selected_logprob_min_workspace(const iso_contract* c, int T, int V);
 iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
                                 float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream);
 
@@ -172,9 +178,10 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
  * minus the workspace: the scratch is one fixed device array of
  * ISO_LOGPROB_STATIC_SCRATCH_BYTES compiled into the library, present on
  * every GPU that loads it until the process exits.  Nothing is allocated.
- * Limit: calls with iso_selected_logprob_workspace(c, T, V) larger than
+ * Limit: calls with iso_selected_logprob_min_workspace(c, T, V) larger than
  * ISO_LOGPROB_STATIC_SCRATCH_BYTES return ISO_ERR_WORKSPACE and launch
- * nothing (8 MiB: up to 16,512 tokens at V = 151936).
+ * nothing (8 MiB: up to 16,512 tokens at V = 151936); up to 820 tokens the
+ * array also holds the per-tile statistics of the faster schedule.
  * The first call on a device looks up the array's device address; make that
  * first call before any stream capture.  All calls on a device share the one
  * array: calls whose kernels may overlap on the GPU (unordered streams) race

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "iso_selected_logprob": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
     "iso_moe_route": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp, _vp]),
     "iso_moe_permute_workspace": (_sz, [_int, _int, _int]),
+    "iso_selected_logprob_min_workspace": (_sz, [_vp, _int, _int]),
     "iso_moe_permute": (_int, [_vp, _vp, _int, _int, _int, _vp, _int, _vp, _vp, _vp, _vp]),
     "iso_moe_combine": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
     "iso_grouped_gemm_moe_workspace": (_sz, [_vp, _int, _int, _int, _int, _int]),
@@ -199,6 +200,10 @@ def rmsnorm(c: Contract, x, gamma, eps: float, out=None, stream=None):
 
 def selected_logprob_workspace(c: Contract, T: int, V: int) -> int:
     return int(c.lib.iso_selected_logprob_workspace(c.handle, T, V))
+
+
+def selected_logprob_min_workspace(c: Contract, T: int, V: int) -> int:
+    return int(c.lib.iso_selected_logprob_min_workspace(c.handle, T, V))
 
 
 def selected_logprob(c: Contract, h, W, ids, out=None, ws=None, stream=None):

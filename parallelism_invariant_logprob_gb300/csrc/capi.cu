@@ -298,20 +298,31 @@ iso_status iso_rmsnorm(const iso_contract* c, const iso_bf16* x, const iso_bf16*
 static int lp_num_tiles(int V) { return div_up(V, LP_TILE_COLS); }
 static int lp_num_chunks(int V) { return div_up(lp_num_tiles(V), LP_CHUNK_TILES); }
 
-// Few row blocks leave most SMs idle when one CTA owns a whole chunk (T = 1: 63 units).
-// Then every 128-column tile is its own work unit and the finalize kernel folds the
-// tile statistics of each chunk left to right -- the same fold, so the same bits.
-static const int kLpTileModeMaxT = 512;
-static bool lp_tile_mode(int T) { return T <= kLpTileModeMaxT; }
+// Work units of the LM-head GEMM.  Tile units: every 128-column tile of a row block is its
+// own unit; its statistics go to a per-tile array and a fold kernel forms each chunk's entry by
+// folding the chunk's tiles left to right.  Chunk units: one CTA owns a whole chunk of a row
+// block and folds its tiles itself.  Same fold, same bits.  Tile units balance the last wave
+// (a chunk unit is ~290 us at T = 4096) and keep every SM busy at small T; measured on GB300 at
+// H = 4096, V = 151936: T = 4096 3.85 -> 3.57 ms, T = 1024 1.21 -> 1.06 ms.  They need the
+// per-tile statistics array ([tiles][T] fp32 pairs, 38 MB at T = 4096), so a workspace
+// without room for it runs chunk units.
 
-static size_t lp_stats_bytes(int T, int V) {
-  const size_t per_row = lp_tile_mode(T) ? static_cast<size_t>(lp_num_tiles(V)) : static_cast<size_t>(lp_num_chunks(V));
-  return ((static_cast<size_t>(T) * per_row * sizeof(float2)) + 255) & ~size_t(255);
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+// Workspace: [tile statistics, tile mode only] [chunk statistics] [z_sel], each 256-aligned.
+static size_t lp_tile_stats_bytes(int T, int V) { return al256(static_cast<size_t>(T) * lp_num_tiles(V) * sizeof(float2)); }
+static size_t lp_chunk_ws_bytes(int T, int V) {
+  return al256(static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)) + al256(static_cast<size_t>(T) * sizeof(float));
 }
+static size_t lp_full_ws_bytes(int T, int V) { return lp_tile_stats_bytes(T, V) + lp_chunk_ws_bytes(T, V); }
 
 size_t iso_selected_logprob_workspace(const iso_contract* c, int T, int V) {
   if (!c || T < 0 || V <= 0) return 0;
-  return lp_stats_bytes(T, V) + ((static_cast<size_t>(T) * sizeof(float) + 255) & ~size_t(255));
+  return lp_full_ws_bytes(T, V);
+}
+
+size_t iso_selected_logprob_min_workspace(const iso_contract* c, int T, int V) {
+  if (!c || T < 0 || V <= 0) return 0;
+  return lp_chunk_ws_bytes(T, V);
 }
 
 iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
@@ -324,7 +335,7 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (V % 8 != 0 || lp_num_chunks(V) > 256) return ISO_ERR_SHAPE;
   if (H % 8 != 0) return ISO_ERR_ALIGNMENT;
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
-  if (ws_bytes < iso_selected_logprob_workspace(c, T, V)) return ISO_ERR_WORKSPACE;
+  if (ws_bytes < lp_chunk_ws_bytes(T, V)) return ISO_ERR_WORKSPACE;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
   GemmParams p = base_params(T, V, H, L);
   if (p.m_blocks == 1)
@@ -336,21 +347,24 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (st != ISO_OK) return st;
   st = make_tmap_bf16(&tB, W, H, V, V, 64, BK);
   if (st != ISO_OK) return st;
-  const bool tiles = lp_tile_mode(T);
-  float2* stats = static_cast<float2*>(ws);
-  float* zsel = reinterpret_cast<float*>(static_cast<char*>(ws) + lp_stats_bytes(T, V));
+  const bool tiles = ws_bytes >= lp_full_ws_bytes(T, V);
+  char* wsb = static_cast<char*>(ws);
+  float2* tile_stats = tiles ? reinterpret_cast<float2*>(wsb) : nullptr;
+  char* rest = wsb + (tiles ? lp_tile_stats_bytes(T, V) : 0);
+  float2* chunk_stats = reinterpret_cast<float2*>(rest);
+  float* zsel = reinterpret_cast<float*>(rest + al256(static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)));
   p.unit_mode = UNIT_LOGPROB;
-  p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;           // tiles per work unit
+  p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;                 // tiles per work unit
   p.num_chunks = tiles ? lp_num_tiles(V) : lp_num_chunks(V);  // statistics entries per row
   p.num_units = p.m_blocks * p.num_chunks;
   p.ids = ids;
-  p.ws_stats = stats;
+  p.ws_stats = tiles ? tile_stats : chunk_stats;
   p.ws_zsel = zsel;
   p.V = V;
   trace(tiles ? "selected_logprob[tile units]" : "selected_logprob[chunk units]", T, H, V, p.num_chunks);
   st = launch_gemm(EPI_LOGPROB, tA, tB, p, p.num_units, S(stream));
   if (st != ISO_OK) return st;
-  return launch_lse_finalize(stats, zsel, ids, out, T, lp_num_chunks(V), V, tiles ? 1 : 0, lp_num_tiles(V),
+  return launch_lse_finalize(tile_stats, chunk_stats, zsel, ids, out, T, lp_num_chunks(V), V, lp_num_tiles(V),
                              LP_CHUNK_TILES, S(stream)) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;

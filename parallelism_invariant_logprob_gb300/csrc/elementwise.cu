@@ -162,35 +162,41 @@ __device__ __forceinline__ void lse_merge_into(float& m1, float& s1, float m2, f
   m1 = mm;
 }
 
+// Statistics are stored entry-major ([entry][T]: consecutive rows adjacent), so both the
+// GEMM epilogue's writes and the reads here are coalesced.
+//
+// Tile statistics -> chunk statistics: thread (c, t) folds the tiles of chunk c for row t left
+// to right -- the fold the GEMM epilogue performs when one CTA owns a whole chunk.
+__global__ void lse_fold_tiles_kernel(const float2* __restrict__ tile_stats, float2* __restrict__ chunk_stats, int T,
+                                      int C, int ntiles, int chunk_tiles) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(C) * T) return;
+  const int c = static_cast<int>(idx / T);
+  const int t = static_cast<int>(idx - static_cast<int64_t>(c) * T);
+  const int t0 = c * chunk_tiles;
+  const int t1 = min(t0 + chunk_tiles, ntiles);
+  float2 v = tile_stats[static_cast<int64_t>(t0) * T + t];
+  for (int q = t0 + 1; q < t1; ++q) {
+    const float2 w = tile_stats[static_cast<int64_t>(q) * T + t];
+    lse_merge_into(v.x, v.y, w.x, w.y);
+  }
+  chunk_stats[idx] = v;
+}
+
 // Per row: the C chunk statistics are merged by the balanced pairwise tree
 // with the odd node carried up, evaluated as a binary counter (merge two
 // equal-size subtrees as soon as both exist, then collapse right to left),
 // which builds exactly that tree.  lse = m + logf(s); out = z_sel - lse.
-// When `tile_stats` is set, `stats` holds one entry per 128-column tile and
-// each chunk's entry is first formed by folding its tiles left to right, the
-// fold the GEMM epilogue performs when it owns a whole chunk.
 __global__ void lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
                                     const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
-                                    int tile_stats, int ntiles, int chunk_tiles, unsigned int* status) {
+                                    unsigned int* status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float sm[10], ss[10];
   int sz[10];
   int depth = 0;
-  const float2* st = stats + static_cast<int64_t>(t) * (tile_stats ? ntiles : C);
   for (int c = 0; c < C; ++c) {
-    float2 v;
-    if (tile_stats) {
-      const int t0 = c * chunk_tiles;
-      const int t1 = min(t0 + chunk_tiles, ntiles);
-      v = st[t0];
-      for (int q = t0 + 1; q < t1; ++q) {
-        const float2 w = st[q];
-        lse_merge_into(v.x, v.y, w.x, w.y);
-      }
-    } else {
-      v = st[c];
-    }
+    const float2 v = stats[static_cast<int64_t>(c) * T + t];
     sm[depth] = v.x;
     ss[depth] = v.y;
     sz[depth] = 1;
@@ -514,10 +520,16 @@ cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_finalize(const float2* stats, const float* zsel, const int32_t* ids, float* out, int T, int C,
-                                int V, int tile_stats, int ntiles, int chunk_tiles, cudaStream_t s) {
-  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(stats, zsel, ids, out, T, C, V, tile_stats, ntiles, chunk_tiles,
-                                                       device_status_ptr());
+cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, const float* zsel, const int32_t* ids,
+                                float* out, int T, int C, int V, int ntiles, int chunk_tiles, cudaStream_t s) {
+  if (tile_stats != nullptr) {
+    const int64_t n = static_cast<int64_t>(C) * T;
+    lse_fold_tiles_kernel<<<static_cast<unsigned int>((n + 255) / 256), 256, 0, s>>>(tile_stats, chunk_stats, T, C,
+                                                                                       ntiles, chunk_tiles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(chunk_stats, zsel, ids, out, T, C, V, device_status_ptr());
   return cudaGetLastError();
 }
 

@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       if (EPI == EPI_LOGPROB && ok && row_ok) {
-        p.ws_stats[static_cast<int64_t>(row) * p.num_chunks + U.chunk] = make_float2(run_m, run_s);
+        p.ws_stats[static_cast<int64_t>(U.chunk) * p.M + row] = make_float2(run_m, run_s);
         if (have_sel) p.ws_zsel[row] = zsel;
       }
     }

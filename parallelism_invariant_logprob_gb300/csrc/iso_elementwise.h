@@ -8,10 +8,10 @@ cudaError_t launch_tree_combine(const float* S, int64_t lds, int64_t rank_stride
                                 int M, int N, cudaStream_t s);
 cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* y, int T, int H,
                            cudaStream_t s);
-// stats: [T][C] chunk statistics, or (tile_stats != 0) [T][ntiles] per-tile statistics that are
-// folded into chunks of chunk_tiles tiles left to right first.
-cudaError_t launch_lse_finalize(const float2* stats, const float* zsel, const int32_t* ids, float* out, int T, int C,
-                                int V, int tile_stats, int ntiles, int chunk_tiles, cudaStream_t s);
+// chunk_stats: [C][T] chunk statistics (m, s).  With tile_stats ([ntiles][T] per-tile statistics)
+// the chunk entries are first formed by folding chunk_tiles tiles left to right into chunk_stats.
+cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, const float* zsel, const int32_t* ids,
+                                float* out, int T, int C, int V, int ntiles, int chunk_tiles, cudaStream_t s);
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 // Chunks of the permutation's counting sort for P pairs; hist holds chunks x E int32.
 int64_t moe_perm_chunks(int64_t P);

@@ -73,7 +73,7 @@ struct GemmParams {
   const int32_t* row_scatter;  // grouped down projection: destination row of each permuted row
   // logprob
   const int32_t* ids;
-  float2* ws_stats;  // [T][C] (m, s)
+  float2* ws_stats;  // [entries][T] (m, s): entries = vocab chunks, or tiles with one tile per unit
   float* ws_zsel;    // [T]
   int V;
   int chunk_tiles;

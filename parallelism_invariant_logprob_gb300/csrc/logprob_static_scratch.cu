@@ -57,7 +57,7 @@ extern "C" iso_status iso_selected_logprob_static_scratch(const iso_contract* c,
                                                           iso_stream stream) {
   if (!c || T < 0 || H <= 0 || V <= 0) return ISO_ERR_INVALID_ARG;
   if (T == 0) return ISO_OK;
-  const size_t need = iso_selected_logprob_workspace(c, T, V);
+  const size_t need = iso_selected_logprob_min_workspace(c, T, V);
   if (need == 0 || need > static_cast<size_t>(ISO_LOGPROB_STATIC_SCRATCH_BYTES)) return ISO_ERR_WORKSPACE;
   void* scratch = nullptr;
   const iso_status st = scratch_for_current_device(&scratch);

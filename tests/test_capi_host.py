@@ -100,9 +100,10 @@ def test_host_validation_launches_nothing(lib):
     assert lib.iso_gemm_leaf_partial(c.handle, 2, 2, fake, 1024, fake, 512, fake, 512, 4, 512, 1024, s0) == 1
     assert lib.iso_tree_combine(c.handle, 3, fake, 512, 4 * 512, fake, 512, 4, 512, s0) == 4
     # logprob: workspace too small, V not a multiple of 8, H not a multiple of 16 L
-    need = lib.iso_selected_logprob_workspace(c.handle, 4, 2440)
-    assert need > 0
+    need = lib.iso_selected_logprob_min_workspace(c.handle, 4, 2440)
+    assert 0 < need < lib.iso_selected_logprob_workspace(c.handle, 4, 2440)
     assert lib.iso_selected_logprob(c.handle, fake, fake, fake, fake, 4, 512, 2440, fake, need - 1, s0) == 7
+    assert lib.iso_selected_logprob_min_workspace(None, 4, 2440) == 0
     assert lib.iso_selected_logprob(c.handle, fake, fake, fake, fake, 4, 512, 2441, fake, need, s0) == 2
     assert lib.iso_selected_logprob(c.handle, fake, fake, fake, fake, 4, 520, 2440, fake, need, s0) == 2
     # rmsnorm: H not a multiple of 8

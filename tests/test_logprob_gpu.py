@@ -149,15 +149,28 @@ def test_logprob_cta_pairs_match_single_rows(c8, T):
 
 
 def test_logprob_tile_units_and_chunk_units_agree_bitwise(c8):
-    """Up to 512 rows every 128-column tile is its own work unit and the chunk fold
-    happens in the finalize kernel; above that a CTA folds a whole chunk.  Both
-    follow the same fold order, so a row's bits must not depend on which is used."""
+    """With the full workspace every 128-column tile is its own work unit and a fold kernel
+    folds each chunk's tiles left to right; with the minimum workspace one CTA folds a whole
+    chunk.  Same fold, same order: the bits must agree, for the whole batch and row subsets."""
     T, H, V = 700, 256, 151936
     h, W, ids = inputs.logprob_inputs(T, H, V, seed=77, device=DEV)
-    full = B.selected_logprob(c8, h, W, ids)  # chunk units
-    for lo, hi in ((0, 1), (5, 69), (100, 612), (699, 700)):  # tile units
-        part = B.selected_logprob(c8, h[lo:hi].contiguous(), W, ids[lo:hi].contiguous())
-        assert f32_same(part, full[lo:hi]), (lo, hi)
+    full = B.selected_logprob(c8, h, W, ids)  # tile units
+    ws_min = torch.empty(B.selected_logprob_min_workspace(c8, T, V), dtype=torch.uint8, device=DEV)
+    assert ws_min.numel() < B.selected_logprob_workspace(c8, T, V)
+    assert f32_same(B.selected_logprob(c8, h, W, ids, ws=ws_min), full)  # chunk units
+    for lo, hi in ((0, 1), (5, 69), (100, 612), (699, 700)):
+        hs, ids_s = h[lo:hi].contiguous(), ids[lo:hi].contiguous()
+        assert f32_same(B.selected_logprob(c8, hs, W, ids_s), full[lo:hi]), (lo, hi)
+        wsm = torch.empty(B.selected_logprob_min_workspace(c8, hi - lo, V), dtype=torch.uint8, device=DEV)
+        assert f32_same(B.selected_logprob(c8, hs, W, ids_s, ws=wsm), full[lo:hi]), (lo, hi)
     rows = torch.tensor([0, 350, 699], device=DEV)
     ref = oracle.selected_logprob(bits(h[rows]), bits(W), ids[rows].cpu().numpy(), 8)
     assert np.max(np.abs(full[rows].cpu().double().numpy() - ref["out"])) <= 1e-3
+
+
+def test_logprob_workspace_below_minimum_is_rejected(c8):
+    T, H, V = 8, 128, 2440
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=5, device=DEV)
+    small = torch.empty(B.selected_logprob_min_workspace(c8, T, V) - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(B.IsoError):
+        B.selected_logprob(c8, h, W, ids, ws=small)
