@@ -363,6 +363,12 @@ def secondary(c, dev, stream, peaks, rank):
             gm[f"M{M}_K{K}_N{N}"] = dict(ms=tt, tflops=2.0 * M * K * N / (tt * 1e-3) / 1e12,
                                          hbm_gbs=byt / (tt * 1e-3) / 1e9, cublas_ms=tb,
                                          overhead_vs_cublas=tt / tb)
+            if M <= 128:  # iso_gemm_ws: the same bits, leaf groups spread over more SMs
+                wsg = torch.empty(max(B.gemm_workspace(c, M, N, K), 16), dtype=torch.uint8, device=dev)
+                tw = time_call(lambda: B.gemm_ws(c, Xm, Wt, out=Cm, ws=wsg, stream=stream), 5, 2, stream, flush)
+                gm[f"M{M}_K{K}_N{N}"].update(ws_ms=tw, ws_hbm_gbs=byt / (tw * 1e-3) / 1e9,
+                                             ws_hbm_frac=byt / (tw * 1e-3) / 1e9 / peaks["hbm"],
+                                             ws_overhead_vs_cublas=tw / tb)
         # simulated TP: R ranks' partials + combine at M = 4096
         for R in (2, 8):
             Kl = K // R

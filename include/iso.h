@@ -112,6 +112,22 @@ iso_status iso_last_device_status(iso_stream stream);
 iso_status iso_gemm(const iso_contract* c, const iso_bf16* A, int64_t lda, const iso_bf16* B, int64_t ldb,
                     iso_bf16* C, int64_t ldc, int M, int N, int K, iso_stream stream);
 
+/* iso_gemm with scratch: the same C, bit for bit, as iso_gemm.  For one row
+ * block (M <= 128) with fewer 128-column tiles than SMs, the leaves are split
+ * into R groups of L/R (R a power of two, R x tiles <= SMs, R as large as ws
+ * allows): each group's fp32 subtree root for every tile goes to ws and the
+ * tree combine applies the top log2 R levels of the contract's tree, so more
+ * SMs stream B (decode-size problems are bound by reading B).  This is the
+ * partial + combine schedule of simulated ranks [IsoExec blog,
+ * "Parallelism-invariant kernels"] run inside one call.  ws: device scratch,
+ * 16-byte aligned, owned by the caller, in use until the stream passes the
+ * call; iso_gemm_workspace(c, M, N, K) bytes allow the largest split (0 when
+ * the split does not apply); with less (or ws == NULL) the call is iso_gemm.
+ * Errors as iso_gemm; iso_gemm_workspace returns 0 for invalid arguments. */
+size_t iso_gemm_workspace(const iso_contract* c, int M, int N, int K);
+iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, const iso_bf16* B, int64_t ldb,
+                       iso_bf16* C, int64_t ldc, int M, int N, int K, void* ws, size_t ws_bytes, iso_stream stream);
+
 /* ------------------------------------------------- simulated tensor parallel
  * iso_gemm_leaf_partial: rank `rank` of `num_ranks` owns the contiguous leaves
  * [rank L/R, (rank+1) L/R) (rank-to-leaf map fixed by the contract) and

@@ -59,6 +59,8 @@ _SIGNATURES = {
     "iso_selected_logprob": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
     "iso_moe_route": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp, _vp]),
     "iso_moe_permute_workspace": (_sz, [_int, _int, _int]),
+    "iso_gemm_workspace": (_sz, [_vp, _int, _int, _int]),
+    "iso_gemm_ws": (_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int, _int, _vp, _sz, _vp]),
     "iso_selected_logprob_min_workspace": (_sz, [_vp, _int, _int]),
     "iso_moe_permute": (_int, [_vp, _vp, _int, _int, _int, _vp, _int, _vp, _vp, _vp, _vp]),
     "iso_moe_combine": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
@@ -150,6 +152,25 @@ def _stream(stream=None):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return _vp(s.cuda_stream)
+
+
+def gemm_workspace(c: Contract, M: int, N: int, K: int) -> int:
+    return int(c.lib.iso_gemm_workspace(c.handle, M, N, K))
+
+
+def gemm_ws(c: Contract, A, B, out=None, ws=None, stream=None):
+    """iso_gemm_ws: iso_gemm's bits, with leaf groups spread over more SMs for small M."""
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    if ws is None:
+        ws = torch.empty(max(gemm_workspace(c, M, N, K), 16), dtype=torch.uint8, device=A.device)
+    st = c.lib.iso_gemm_ws(c.handle, _ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(out), out.stride(0), M, N, K,
+                           _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    c.lib.check(st, "iso_gemm_ws")
+    return out
 
 
 def gemm(c: Contract, A, B, out=None, stream=None):

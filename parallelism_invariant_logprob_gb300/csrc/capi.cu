@@ -253,6 +253,53 @@ iso_status iso_gemm(const iso_contract* c, const iso_bf16* A, int64_t lda, const
   return run_gemm(EPI_BF16, A, lda, B, ldb, C, ldc, M, N, K, L, S(stream));
 }
 
+size_t iso_gemm_workspace(const iso_contract* c, int M, int N, int K) {
+  if (!c || M < 0 || N <= 0 || K <= 0) return 0;
+  if (M > BM) return 0;  // the leaf split serves problems of one row block
+  const int L = iso_contract_leaf_count(c);
+  return static_cast<size_t>(L) * static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+}
+
+iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, const iso_bf16* B, int64_t ldb,
+                       iso_bf16* C, int64_t ldc, int M, int N, int K, void* ws, size_t ws_bytes, iso_stream stream) {
+  if (!c) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  iso_status st = check_gemm_args(A, lda, B, ldb, C, ldc, 8, M, N, K, L);
+  if (st != ISO_OK || M == 0) return st;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  // Leaf groups: with one row block and fewer column tiles than SMs, R groups of L/R leaves run
+  // as separate units (R = the largest power of two <= L with R x tiles <= SMs); each writes
+  // its group's fp32 subtree root to ws and the tree combine applies the top log2 R levels --
+  // iso_gemm_leaf_partial + iso_tree_combine over R simulated ranks, the same bits as iso_gemm.
+  const int n_tiles = div_up(N, BN);
+  int R = 1;
+  if (M <= BM && ws != nullptr && aligned16(ws))
+    while (R * 2 <= L && n_tiles * R * 2 <= sm_count() &&
+           ws_bytes >= static_cast<size_t>(R) * 2 * static_cast<size_t>(M) * N * sizeof(float))
+      R *= 2;
+  if (R == 1) return run_gemm(EPI_BF16, A, lda, B, ldb, C, ldc, M, N, K, L, S(stream));
+  GemmParams p = base_params(M, N, K / R, L / R);
+  set_a_rows(p, a_rows_for(M));
+  CUtensorMap tA, tB;
+  st = make_tmap_bf16(&tA, A, M, K, lda, BK, static_cast<uint32_t>(p.a_rows));
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
+  if (st != ISO_OK) return st;
+  float* S_all = static_cast<float*>(ws);
+  p.unit_mode = UNIT_LEAF_SPLIT;
+  p.num_units = R * p.n_blocks;
+  p.out = S_all;
+  p.ldo = N;
+  p.out_group_stride = static_cast<int64_t>(M) * N;
+  trace("gemm[leaf groups]", M, N, K, R);
+  st = launch_gemm(EPI_F32, tA, tB, p, p.num_units, S(stream));
+  if (st != ISO_OK) return st;
+  return launch_tree_combine(S_all, N, static_cast<int64_t>(M) * N, R, reinterpret_cast<uint16_t*>(C), ldc, M, N,
+                             S(stream)) == cudaSuccess
+             ? ISO_OK
+             : ISO_ERR_CUDA;
+}
+
 iso_status iso_gemm_leaf_partial(const iso_contract* c, int rank, int num_ranks, const iso_bf16* A_r, int64_t lda,
                                  const iso_bf16* B_r, int64_t ldb, float* S_r, int64_t lds, int M, int N,
                                  int K_local, iso_stream stream) {

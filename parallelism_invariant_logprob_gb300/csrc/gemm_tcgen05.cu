@@ -51,7 +51,8 @@ namespace {
 
 struct Unit {
   int a_row0;      // first A row of this unit
-  int b_row0;      // first B row (K offset of the expert in grouped mode)
+  int a_col0;      // first A column (the K offset of a leaf group; 0 otherwise)
+  int b_row0;      // first B row (K offset of the expert in grouped mode, or of a leaf group)
   int n_tile0;     // first 128-column tile
   int n_tiles;     // tiles in this unit
   int rows_valid;  // rows of the 128 that are real
@@ -75,17 +76,29 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U,
     const int mb = gm0 + r % gsz;
     const int nb = r / gsz;
     U.a_row0 = (mb * cl + rank) * BM;
+    U.a_col0 = 0;
     U.b_row0 = 0;
     U.n_tile0 = nb;
     U.n_tiles = 1;
     U.rows_valid = min(BM, p.M - U.a_row0);
     U.chunk = 0;
+  } else if (p.unit_mode == UNIT_LEAF_SPLIT) {
+    // group-major: the n-tiles of one leaf group run together and share its A columns
+    const int r = u / p.n_blocks;
+    U.a_row0 = 0;
+    U.a_col0 = r * p.K;
+    U.b_row0 = r * p.K;
+    U.n_tile0 = u - r * p.n_blocks;
+    U.n_tiles = 1;
+    U.rows_valid = min(BM, p.M);
+    U.chunk = r;
   } else if (p.unit_mode == UNIT_LOGPROB) {
     // chunk-major: the row blocks working on one vocab chunk run together and
     // share its W columns in L2.
     const int chunk = u / p.m_blocks;
     const int rb = u - chunk * p.m_blocks;
     U.a_row0 = (rb * cl + rank) * BM;
+    U.a_col0 = 0;
     U.b_row0 = 0;
     U.n_tile0 = chunk * p.chunk_tiles;
     U.n_tiles = min(p.chunk_tiles, p.n_blocks - U.n_tile0);
@@ -110,6 +123,7 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U,
     const int off = p.g_offsets[e];
     const int ne = p.g_offsets[e + 1] - off;
     U.a_row0 = off + (mb * cl + rank) * BM;
+    U.a_col0 = 0;
     U.b_row0 = e * p.K;
     U.n_tile0 = nb;
     U.n_tiles = 1;
@@ -365,11 +379,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   const uint32_t fb = cluster_addr(&full_bar[stage], 0);
                   if (rank == 0)
                     mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(2 * (p.a_bytes + BSTAGE)));
-                  tma_load_2d_pair(sA, &tmA, fb, kx, U.a_row0);
+                  tma_load_2d_pair(sA, &tmA, fb, U.a_col0 + kx, U.a_row0);
                   tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);
                 } else {
                   mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + BSTAGE));
-                  tma_load_2d(sA, &tmA, &full_bar[stage], kx, U.a_row0);
+                  tma_load_2d(sA, &tmA, &full_bar[stage], U.a_col0 + kx, U.a_row0);
                   tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
                   tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
                 }
@@ -672,7 +686,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
               }
             } else {
-              float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ldo;
+              float* dst = reinterpret_cast<float*>(p.out) + U.chunk * p.out_group_stride +
+                           static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
               for (int q = 0; q < BN / 4; ++q) {
                 const int col = n0 + q * 4;

@@ -49,7 +49,7 @@ constexpr int LP_TILE_COLS = BN;
 constexpr int LP_CHUNK_TILES = 19;
 
 enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2, EPI_SWIGLU = 3 };
-enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2 };
+enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2, UNIT_LEAF_SPLIT = 3 };
 
 struct GemmParams {
   int M, N, K;     // K = contraction length handled by this launch
@@ -82,6 +82,10 @@ struct GemmParams {
   const int32_t* g_offsets;      // [E+1]
   const int32_t* g_unit_prefix;  // [E+1]
   int E;
+  // leaf split (one row block): unit u = (group r, n-tile); group r covers K [r K, (r+1) K) of the
+  // full problem (K here is the group's length) and writes its fp32 subtree root to
+  // out + r * out_group_stride
+  int64_t out_group_stride;
   // error reporting
   unsigned int* status;
   uint64_t timeout_ns;

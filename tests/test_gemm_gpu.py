@@ -187,6 +187,31 @@ def test_cta_pair_normal_inputs_and_partials(c8):
         assert same_bits(B.tree_combine(c8, S), full), R
 
 
+@pytest.mark.parametrize("M,N,K,L", [(1, 4096, 4096, 8), (7, 136, 2048, 4), (64, 4096, 4096, 8),
+                                     (128, 12288, 4096, 8), (100, 1024, 8192, 8), (33, 512, 1024, 2)])
+def test_gemm_ws_leaf_groups_match_single_pass_bitwise(M, N, K, L):
+    """iso_gemm_ws spreads the leaves of one row block over more SMs (groups of L/R leaves,
+    fp32 group roots, then the top tree levels); the bits must be iso_gemm's, for every
+    split the heuristic picks (including none) and with a workspace too small to split."""
+    c = B.Contract(L)
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=M + N)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    ref = B.gemm(c, Ad, Bd)
+    assert same_bits(B.gemm_ws(c, Ad, Bd), ref), first_diff(B.gemm_ws(c, Ad, Bd), ref)
+    small = torch.empty(M * N * 4, dtype=torch.uint8, device=DEV)  # room for one group: no split
+    assert same_bits(B.gemm_ws(c, Ad, Bd, ws=small), ref)
+    assert B.last_device_status(c) == B.ISO_OK
+
+
+def test_gemm_ws_exact_integers_equal_oracle():
+    M, N, K = 5, 1024, 4096
+    c = B.Contract(8)
+    A = inputs.small_int_bf16((M, K), -3, 3, seed=11)
+    Bm = inputs.small_int_bf16((K, N), -3, 3, seed=12)
+    C = B.gemm_ws(c, A.to(DEV), Bm.to(DEV))
+    assert np.array_equal(bits(C), oracle.gemm(bits(A), bits(Bm), 8))
+
+
 @pytest.mark.slow
 def test_config2_full_size_m4096_sampled(c8):
     K, N, M = 4096, 4096, 4096
