@@ -184,6 +184,37 @@ size_t iso_selected_logprob_min_workspace(const iso_contract* c, int T, int V);
 iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
                                 float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream);
 
+/* ------------------------------------------------ vocab-parallel logprob
+ * [RL-Kernel blog, §7 "LogP": each tensor-parallel shard computes its local
+ *  statistics, then they are merged in a fixed vocab tile order; §4 "Causal
+ *  Chain: How Block Merge Order Alters LSE": the two-block merge]
+ * Shard r owns the vocabulary columns [v0, v0 + V_r) of V: v0 a multiple of
+ * the 2432-column chunk, V_r a multiple of it unless the shard ends at V, and
+ * the shards in rank order cover [0, V) contiguously.
+ *
+ * iso_selected_logprob_partial: W_r [H x V_r] bf16 (the shard's columns,
+ * leading dimension ldw >= V_r, ldw % 8 == 0); h, ids as iso_selected_logprob
+ * (ids are full-vocabulary ids).  Writes the shard's chunk statistics
+ * stats_r [C_r x T] (m, s) fp32 pairs, chunk-major (C_r = chunks of the
+ * shard), and z_sel_r[t] = the logit at ids[t] for the rows whose id falls in
+ * the shard (other rows are left untouched).  ws (optional, 16-byte aligned,
+ * iso_selected_logprob_partial_workspace bytes) enables one-tile work units.
+ *
+ * iso_selected_logprob_combine: stats [C x T] pairs = the shards' stats_r
+ * concatenated in rank order (an all-gather of the chunk-major blocks);
+ * zsel [num_shards x T] = the shards' z_sel_r; shard_v0: HOST array of the
+ * num_shards first columns (increasing, shard_v0[0] = 0, <= 64 shards).
+ * out[t] = z_sel(owner of ids[t])[t] - lse over the chunk tree: bit for bit
+ * the output of iso_selected_logprob on the whole vocabulary.  Ids outside
+ * [0, V) yield NaN and ISO_ERR_BAD_TOKEN_ID in the device status word. */
+size_t iso_selected_logprob_partial_workspace(const iso_contract* c, int T, int V_r);
+iso_status iso_selected_logprob_partial(const iso_contract* c, const iso_bf16* h, const iso_bf16* W_r, int64_t ldw,
+                                        const int32_t* ids, int T, int H, int V, int v0, int V_r, float* stats_r,
+                                        float* zsel_r, void* ws, size_t ws_bytes, iso_stream stream);
+iso_status iso_selected_logprob_combine(const iso_contract* c, int num_shards, const int* shard_v0,
+                                        const float* stats, const float* zsel, const int32_t* ids, float* out, int T,
+                                        int V, iso_stream stream);
+
 /* ------------------------------------------ logprob without allocation
  * No counterpart on the pages: this entry point exists for callers of this
  * library that cannot allocate device memory -- code behind a plugin or

@@ -60,6 +60,10 @@ _SIGNATURES = {
     "iso_moe_route": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp, _vp]),
     "iso_moe_permute_workspace": (_sz, [_int, _int, _int]),
     "iso_gemm_workspace": (_sz, [_vp, _int, _int, _int]),
+    "iso_selected_logprob_partial_workspace": (_sz, [_vp, _int, _int]),
+    "iso_selected_logprob_partial": (_int, [_vp, _vp, _vp, _i64, _vp, _int, _int, _int, _int, _int, _vp, _vp, _vp,
+                                            _sz, _vp]),
+    "iso_selected_logprob_combine": (_int, [_vp, _int, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp]),
     "iso_gemm_ws": (_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int, _int, _vp, _sz, _vp]),
     "iso_selected_logprob_min_workspace": (_sz, [_vp, _int, _int]),
     "iso_moe_permute": (_int, [_vp, _vp, _int, _int, _int, _vp, _int, _vp, _vp, _vp, _vp]),
@@ -221,6 +225,43 @@ def rmsnorm(c: Contract, x, gamma, eps: float, out=None, stream=None):
 
 def selected_logprob_workspace(c: Contract, T: int, V: int) -> int:
     return int(c.lib.iso_selected_logprob_workspace(c.handle, T, V))
+
+
+LP_CHUNK_COLS = 128 * 19  # vocabulary columns per statistics chunk
+
+
+def selected_logprob_partial(c: Contract, h, W_r, ids, V: int, v0: int, stats_r=None, zsel_r=None, ws=None,
+                             stream=None):
+    """One vocab shard's chunk statistics [C_r x T x 2] and its selected logits [T]."""
+    import torch
+    T, H = h.shape
+    V_r = W_r.shape[1]
+    C_r = ((V_r + 127) // 128 + 18) // 19
+    if stats_r is None:
+        stats_r = torch.empty(C_r, T, 2, dtype=torch.float32, device=h.device)
+    if zsel_r is None:
+        zsel_r = torch.zeros(T, dtype=torch.float32, device=h.device)
+    if ws is None:
+        ws = torch.empty(max(int(c.lib.iso_selected_logprob_partial_workspace(c.handle, T, V_r)), 16),
+                         dtype=torch.uint8, device=h.device)
+    st = c.lib.iso_selected_logprob_partial(c.handle, _ptr(h), _ptr(W_r), W_r.stride(0), _ptr(ids), T, H, V, v0, V_r,
+                                            _ptr(stats_r), _ptr(zsel_r), _ptr(ws), ws.numel() * ws.element_size(),
+                                            _stream(stream))
+    c.lib.check(st, "iso_selected_logprob_partial")
+    return stats_r, zsel_r
+
+
+def selected_logprob_combine(c: Contract, shard_v0, stats, zsel, ids, V: int, out=None, stream=None):
+    """Chunk tree over the gathered shard statistics [C x T x 2]; zsel [num_shards x T]."""
+    import torch
+    T = ids.shape[0]
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=ids.device)
+    v0 = (ctypes.c_int * len(shard_v0))(*shard_v0)
+    st = c.lib.iso_selected_logprob_combine(c.handle, len(shard_v0), v0, _ptr(stats), _ptr(zsel), _ptr(ids), _ptr(out),
+                                            T, V, _stream(stream))
+    c.lib.check(st, "iso_selected_logprob_combine")
+    return out
 
 
 def selected_logprob_min_workspace(c: Contract, T: int, V: int) -> int:

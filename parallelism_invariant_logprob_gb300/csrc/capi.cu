@@ -372,6 +372,44 @@ size_t iso_selected_logprob_min_workspace(const iso_contract* c, int T, int V) {
   return lp_chunk_ws_bytes(T, V);
 }
 
+// The statistics pass of the selected-token logprob over the vocabulary columns [sel_base,
+// sel_base + Vl) held by W ([H x Vl], leading dimension ldw): chunk statistics [Cl x T] into
+// chunk_stats and z at each row's id (when the id falls in these columns) into zsel.  With
+// tile_stats (room for [tiles x T]) every 128-column tile is its own unit and a fold kernel forms
+// the chunk entries; otherwise one CTA folds a whole chunk.  Same fold, same bits.
+static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, int64_t ldw,
+                                    const int32_t* ids, int T, int H, int Vl, int sel_base, float2* chunk_stats,
+                                    float* zsel, float2* tile_stats, cudaStream_t s) {
+  const int L = iso_contract_leaf_count(c);
+  GemmParams p = base_params(T, Vl, H, L);
+  if (p.m_blocks == 1)
+    set_a_rows(p, a_rows_for(T));
+  else if (use_pair(T, H, L))
+    set_pair(p, T);
+  CUtensorMap tA, tB;
+  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, W, H, Vl, ldw, 64, BK);
+  if (st != ISO_OK) return st;
+  const bool tiles = tile_stats != nullptr;
+  p.unit_mode = UNIT_LOGPROB;
+  p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;                   // tiles per work unit
+  p.num_chunks = tiles ? lp_num_tiles(Vl) : lp_num_chunks(Vl);  // statistics entries per row
+  p.num_units = p.m_blocks * p.num_chunks;
+  p.ids = ids;
+  p.ws_stats = tiles ? tile_stats : chunk_stats;
+  p.ws_zsel = zsel;
+  p.V = Vl;
+  p.sel_base = sel_base;
+  trace(tiles ? "selected_logprob[tile units]" : "selected_logprob[chunk units]", T, H, Vl, p.num_chunks);
+  st = launch_gemm(EPI_LOGPROB, tA, tB, p, p.num_units, s);
+  if (st != ISO_OK || !tiles) return st;
+  return launch_lse_fold_tiles(tile_stats, chunk_stats, T, lp_num_chunks(Vl), lp_num_tiles(Vl), LP_CHUNK_TILES, s) ==
+                 cudaSuccess
+             ? ISO_OK
+             : ISO_ERR_CUDA;
+}
+
 iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
                                 float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream) {
   if (!c || T < 0 || H <= 0 || V <= 0) return ISO_ERR_INVALID_ARG;
@@ -384,35 +422,66 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
   if (ws_bytes < lp_chunk_ws_bytes(T, V)) return ISO_ERR_WORKSPACE;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
-  GemmParams p = base_params(T, V, H, L);
-  if (p.m_blocks == 1)
-    set_a_rows(p, a_rows_for(T));
-  else if (use_pair(T, H, L))
-    set_pair(p, T);
-  CUtensorMap tA, tB;
-  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
-  if (st != ISO_OK) return st;
-  st = make_tmap_bf16(&tB, W, H, V, V, 64, BK);
-  if (st != ISO_OK) return st;
   const bool tiles = ws_bytes >= lp_full_ws_bytes(T, V);
   char* wsb = static_cast<char*>(ws);
   float2* tile_stats = tiles ? reinterpret_cast<float2*>(wsb) : nullptr;
   char* rest = wsb + (tiles ? lp_tile_stats_bytes(T, V) : 0);
   float2* chunk_stats = reinterpret_cast<float2*>(rest);
   float* zsel = reinterpret_cast<float*>(rest + al256(static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)));
-  p.unit_mode = UNIT_LOGPROB;
-  p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;                 // tiles per work unit
-  p.num_chunks = tiles ? lp_num_tiles(V) : lp_num_chunks(V);  // statistics entries per row
-  p.num_units = p.m_blocks * p.num_chunks;
-  p.ids = ids;
-  p.ws_stats = tiles ? tile_stats : chunk_stats;
-  p.ws_zsel = zsel;
-  p.V = V;
-  trace(tiles ? "selected_logprob[tile units]" : "selected_logprob[chunk units]", T, H, V, p.num_chunks);
-  st = launch_gemm(EPI_LOGPROB, tA, tB, p, p.num_units, S(stream));
+  iso_status st = run_logprob_stats(c, h, W, V, ids, T, H, V, 0, chunk_stats, zsel, tile_stats, S(stream));
   if (st != ISO_OK) return st;
-  return launch_lse_finalize(tile_stats, chunk_stats, zsel, ids, out, T, lp_num_chunks(V), V, lp_num_tiles(V),
-                             LP_CHUNK_TILES, S(stream)) == cudaSuccess
+  ShardBounds one;
+  one.n = 1;
+  one.chunk0[0] = 0;
+  return launch_lse_combine(chunk_stats, zsel, ids, out, T, lp_num_chunks(V), V, one, S(stream)) == cudaSuccess
+             ? ISO_OK
+             : ISO_ERR_CUDA;
+}
+
+size_t iso_selected_logprob_partial_workspace(const iso_contract* c, int T, int V_r) {
+  if (!c || T < 0 || V_r <= 0) return 0;
+  return lp_tile_stats_bytes(T, V_r);
+}
+
+iso_status iso_selected_logprob_partial(const iso_contract* c, const iso_bf16* h, const iso_bf16* W_r, int64_t ldw,
+                                        const int32_t* ids, int T, int H, int V, int v0, int V_r, float* stats_r,
+                                        float* zsel_r, void* ws, size_t ws_bytes, iso_stream stream) {
+  constexpr int kChunkCols = LP_TILE_COLS * LP_CHUNK_TILES;
+  if (!c || T < 0 || H <= 0 || V <= 0 || V_r <= 0 || v0 < 0) return ISO_ERR_INVALID_ARG;
+  if (v0 % kChunkCols != 0 || v0 + V_r > V || (v0 + V_r != V && V_r % kChunkCols != 0)) return ISO_ERR_SHAPE;
+  if (T == 0) return ISO_OK;
+  if (!h || !W_r || !ids || !stats_r || !zsel_r) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  if (H % (UMMA_K * L) != 0) return ISO_ERR_SHAPE;
+  if (V % 8 != 0 || V_r % 8 != 0 || lp_num_chunks(V) > 256) return ISO_ERR_SHAPE;
+  if (ldw < V_r || ldw % 8 != 0 || H % 8 != 0) return ISO_ERR_ALIGNMENT;
+  if (!aligned16(h) || !aligned16(W_r) || !aligned16(stats_r) || (ws && !aligned16(ws))) return ISO_ERR_ALIGNMENT;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  float2* tile_stats =
+      (ws != nullptr && ws_bytes >= lp_tile_stats_bytes(T, V_r)) ? static_cast<float2*>(ws) : nullptr;
+  return run_logprob_stats(c, h, W_r, ldw, ids, T, H, V_r, v0, reinterpret_cast<float2*>(stats_r), zsel_r, tile_stats,
+                           S(stream));
+}
+
+iso_status iso_selected_logprob_combine(const iso_contract* c, int num_shards, const int* shard_v0,
+                                        const float* stats, const float* zsel, const int32_t* ids, float* out, int T,
+                                        int V, iso_stream stream) {
+  constexpr int kChunkCols = LP_TILE_COLS * LP_CHUNK_TILES;
+  if (!c || T < 0 || V <= 0 || !shard_v0) return ISO_ERR_INVALID_ARG;
+  if (num_shards < 1 || num_shards > kMaxVocabShards) return ISO_ERR_UNSUPPORTED;
+  if (V % 8 != 0 || lp_num_chunks(V) > 256) return ISO_ERR_SHAPE;
+  ShardBounds sb;
+  sb.n = num_shards;
+  for (int r = 0; r < num_shards; ++r) {
+    if (shard_v0[r] % kChunkCols != 0 || shard_v0[r] >= V) return ISO_ERR_SHAPE;
+    if ((r == 0 && shard_v0[r] != 0) || (r > 0 && shard_v0[r] <= shard_v0[r - 1])) return ISO_ERR_SHAPE;
+    sb.chunk0[r] = shard_v0[r] / kChunkCols;
+  }
+  if (T == 0) return ISO_OK;
+  if (!stats || !zsel || !ids || !out) return ISO_ERR_INVALID_ARG;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  return launch_lse_combine(reinterpret_cast<const float2*>(stats), zsel, ids, out, T, lp_num_chunks(V), V, sb,
+                            S(stream)) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;
 }

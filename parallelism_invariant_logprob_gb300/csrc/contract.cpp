@@ -137,7 +137,7 @@ std::string serialize(const iso_contract& c) {
            "\"tile_stat\":\"max;ascending_sum_expf(z-m)_fp32_rn\","
            "\"chunk_fold\":\"left_to_right_two_block_merge\",\"chunk_tree\":\"pairwise_odd_carried\","
            "\"merge\":\"m=fmaxf;s=rn(rn(s1*expf(m1-m))+rn(s2*expf(m2-m)))\",\"lse\":\"m+logf(s)\","
-           "\"out\":\"rn(z_sel-lse)\"},"
+           "\"out\":\"rn(z_sel-lse)\",\"vocab_parallel\":\"contiguous_chunk_aligned_shards_in_rank_order\"},"
            "\"rmsnorm\":{\"map\":\"warp_per_row;lane_owns_8_element_vectors_v_mod_32\","
            "\"lane_sum\":\"ascending_rn(acc+rn(x*x))\",\"tree\":\"shfl_xor_16_8_4_2_1\","
            "\"scale\":\"rn(1/sqrt_rn(rn(ss/H)+eps))\",\"out\":\"bf16_rn(rn(rn(x*r)*gamma))\"},"

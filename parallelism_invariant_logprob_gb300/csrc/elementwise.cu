@@ -187,9 +187,11 @@ __global__ void lse_fold_tiles_kernel(const float2* __restrict__ tile_stats, flo
 // with the odd node carried up, evaluated as a binary counter (merge two
 // equal-size subtrees as soon as both exist, then collapse right to left),
 // which builds exactly that tree.  lse = m + logf(s); out = z_sel - lse.
+// zsel holds one [T] array per vocab shard; a row's selected logit comes from the shard whose
+// chunk range [chunk0[r], chunk0[r+1]) holds the id's chunk (one shard: chunk0 = {0, C}).
 __global__ void lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
                                     const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
-                                    unsigned int* status) {
+                                    ShardBounds shards, unsigned int* status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float sm[10], ss[10];
@@ -218,8 +220,12 @@ __global__ void lse_finalize_kernel(const float2* __restrict__ stats, const floa
     atomicOr(status, kDevBadToken);
     return;
   }
+  const int chunk = id / (LP_TILE_COLS * LP_CHUNK_TILES);
+  int owner = 0;
+  for (int r = 1; r < shards.n; ++r)
+    if (shards.chunk0[r] <= chunk) owner = r;
   const float lse = __fadd_rn(sm[0], logf(ss[0]));
-  out[t] = __fsub_rn(zsel[t], lse);
+  out[t] = __fsub_rn(zsel[static_cast<int64_t>(owner) * T + t], lse);
 }
 
 // ------------------------------------------------------------------ MoE route
@@ -523,13 +529,28 @@ cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, 
 cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, const float* zsel, const int32_t* ids,
                                 float* out, int T, int C, int V, int ntiles, int chunk_tiles, cudaStream_t s) {
   if (tile_stats != nullptr) {
-    const int64_t n = static_cast<int64_t>(C) * T;
-    lse_fold_tiles_kernel<<<static_cast<unsigned int>((n + 255) / 256), 256, 0, s>>>(tile_stats, chunk_stats, T, C,
-                                                                                       ntiles, chunk_tiles);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_lse_fold_tiles(tile_stats, chunk_stats, T, C, ntiles, chunk_tiles, s);
     if (e != cudaSuccess) return e;
   }
-  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(chunk_stats, zsel, ids, out, T, C, V, device_status_ptr());
+  ShardBounds one;
+  one.n = 1;
+  one.chunk0[0] = 0;
+  return launch_lse_combine(chunk_stats, zsel, ids, out, T, C, V, one, s);
+}
+
+cudaError_t launch_lse_combine(const float2* chunk_stats, const float* zsel, const int32_t* ids, float* out, int T,
+                               int C, int V, const ShardBounds& shards, cudaStream_t s) {
+  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(chunk_stats, zsel, ids, out, T, C, V, shards,
+                                                       device_status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_fold_tiles(const float2* tile_stats, float2* chunk_stats, int T, int C, int ntiles,
+                                  int chunk_tiles, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(C) * T;
+  if (n == 0) return cudaSuccess;
+  lse_fold_tiles_kernel<<<static_cast<unsigned int>((n + 255) / 256), 256, 0, s>>>(tile_stats, chunk_stats, T, C,
+                                                                                     ntiles, chunk_tiles);
   return cudaGetLastError();
 }
 

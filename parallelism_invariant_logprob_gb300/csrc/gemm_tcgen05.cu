@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int row = U.a_row0 + row_in_tile;
       float run_m = -INFINITY, run_s = 0.f;  // logprob: running chunk statistics
       int sel = -1;
-      if (EPI == EPI_LOGPROB && row_ok) sel = p.ids[row];
+      if (EPI == EPI_LOGPROB && row_ok) sel = p.ids[row] - p.sel_base;  // this launch's column of the id
       float zsel = 0.f;
       bool have_sel = false;
       for (int t = 0; t < U.n_tiles && ok; ++t) {

@@ -12,6 +12,18 @@ cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, 
 // the chunk entries are first formed by folding chunk_tiles tiles left to right into chunk_stats.
 cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, const float* zsel, const int32_t* ids,
                                 float* out, int T, int C, int V, int ntiles, int chunk_tiles, cudaStream_t s);
+// Vocab shards: shard r owns chunks [chunk0[r], chunk0[r+1]) (chunk0[n] implied = C).
+constexpr int kMaxVocabShards = 64;
+struct ShardBounds {
+  int n;
+  int chunk0[kMaxVocabShards];
+};
+// Tile statistics [ntiles][T] -> chunk statistics [C][T] (left fold of each chunk's tiles).
+cudaError_t launch_lse_fold_tiles(const float2* tile_stats, float2* chunk_stats, int T, int C, int ntiles,
+                                  int chunk_tiles, cudaStream_t s);
+// Chunk tree over chunk_stats [C][T], lse, and out = zsel[owner shard][t] - lse.
+cudaError_t launch_lse_combine(const float2* chunk_stats, const float* zsel, const int32_t* ids, float* out, int T,
+                               int C, int V, const ShardBounds& shards, cudaStream_t s);
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 // Chunks of the permutation's counting sort for P pairs; hist holds chunks x E int32.
 int64_t moe_perm_chunks(int64_t P);

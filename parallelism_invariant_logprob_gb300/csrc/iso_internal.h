@@ -76,6 +76,7 @@ struct GemmParams {
   float2* ws_stats;  // [entries][T] (m, s): entries = vocab chunks, or tiles with one tile per unit
   float* ws_zsel;    // [T]
   int V;
+  int sel_base;      // vocabulary column of this launch's column 0 (a vocab shard's first column)
   int chunk_tiles;
   int num_chunks;
   // grouped

@@ -174,3 +174,43 @@ def test_logprob_workspace_below_minimum_is_rejected(c8):
     small = torch.empty(B.selected_logprob_min_workspace(c8, T, V) - 256, dtype=torch.uint8, device=DEV)
     with pytest.raises(B.IsoError):
         B.selected_logprob(c8, h, W, ids, ws=small)
+
+
+# ------------------------------------------------------------ vocab-parallel
+@pytest.mark.parametrize("T,H,splits", [
+    (300, 512, [0]),
+    (300, 512, [0, 2432]),
+    (700, 256, [0, 2432 * 20, 2432 * 40]),
+    (64, 512, [0, 2432 * 10, 2432 * 31, 2432 * 50]),
+])
+def test_vocab_parallel_partial_combine_equals_single_call_bitwise(c8, T, H, splits):
+    """Shards of the vocabulary (simulated ranks on column slices of W) compute their chunk
+    statistics and owned selected logits; the combine over the rank-ordered concatenation
+    must give the single call's bits, with one-tile or whole-chunk units per shard."""
+    V = 151936
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=T + H, device=DEV)
+    ref = B.selected_logprob(c8, h, W, ids)
+    bounds = splits + [V]
+    for tile_units in (True, False):
+        stats, zs = [], []
+        for r in range(len(splits)):
+            v0, v1 = bounds[r], bounds[r + 1]
+            ws = None if tile_units else torch.empty(16, dtype=torch.uint8, device=DEV)
+            s_r, z_r = B.selected_logprob_partial(c8, h, W[:, v0:v1], ids, V, v0, ws=ws)
+            stats.append(s_r)
+            zs.append(z_r)
+        out = B.selected_logprob_combine(c8, splits, torch.cat(stats, 0), torch.stack(zs), ids, V)
+        assert f32_same(out, ref), (splits, tile_units)
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
+def test_vocab_parallel_rejects_unaligned_shards(c8):
+    T, H, V = 4, 128, 151936
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=3, device=DEV)
+    with pytest.raises(B.IsoError):
+        B.selected_logprob_partial(c8, h, W[:, 128:4992], ids, V, 128)  # v0 not chunk-aligned
+    with pytest.raises(B.IsoError):
+        B.selected_logprob_partial(c8, h, W[:, 0:2560], ids, V, 0)  # ragged shard that does not end at V
+    stats = torch.zeros(63, T, 2, device=DEV)
+    with pytest.raises(B.IsoError):
+        B.selected_logprob_combine(c8, [0, 2500], stats, torch.zeros(2, T, device=DEV), ids, V)
