@@ -23,6 +23,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
       matmul + SwiGLU, one-hot gates, equal gates)
   delta          : pinned (worked examples printed in the VeXact paper, Table 1,
       and the RL-Kernel blog, §1 "Minimal Example")
+  mismatch       : pinned (Table 1 deltas and mismatch count, identical inputs,
+      closed forms of r_corr, K1, K3 and the tau_tok truncation, math.fsum
+      brute-force sequence sums, both sides of the tau_seq rejection, the
+      small-delta expansion of K3)
 """
 from __future__ import annotations
 
@@ -72,6 +76,8 @@ def _load():
                                          _int, _u16p, _u16p, _f64p, _int]
     lib.iso_oracle_moe_combine.argtypes = [_u16p, _f64p, _int, _int, _int, _u16p, _f64p]
     lib.iso_oracle_delta.argtypes = [_f64p, _f64p, _i64, _f64p]
+    lib.iso_oracle_mismatch.argtypes = [_f32p, _f32p, _i32p, _int, ctypes.c_double, ctypes.c_double, _f64p, _f64p,
+                                        _f64p, _f64p, _u8p, _u8p, _f64p, _i32p]
     _lib = lib
     return lib
 
@@ -279,6 +285,32 @@ def moe_combine(y_slots, w, exact=False):
 
 
 # ----------------------------------------------------------------- delta_t
+def mismatch(logp_train, logp_rollout, offsets, tau_tok=2.0, tau_seq=0.001):
+    """Mismatch diagnostics over packed sequences (VeXact paper, Eq. 1, 6, 7; K1/K3 of §4.1):
+    per token delta, min(r_corr, tau_tok); per sequence sum K1, sum K3, the rejection
+    masks S <= tau_seq, max |delta| and the count of tokens whose logprobs differ."""
+    lib = _load()
+    a = _c(logp_train, np.float32)
+    b = _c(logp_rollout, np.float32)
+    off = _c(offsets, np.int32)
+    B = off.size - 1
+    N = a.size
+    d = np.empty(N, np.float64)
+    w = np.empty(N, np.float64)
+    k1 = np.empty(B, np.float64)
+    k3 = np.empty(B, np.float64)
+    a1 = np.empty(B, np.uint8)
+    a3 = np.empty(B, np.uint8)
+    mx = np.empty(B, np.float64)
+    nm = np.empty(B, np.int32)
+    rc = lib.iso_oracle_mismatch(_p(a, _f32p), _p(b, _f32p), _p(off, _i32p), B, tau_tok, tau_seq, _p(d, _f64p),
+                                 _p(w, _f64p), _p(k1, _f64p), _p(k3, _f64p), _p(a1, _u8p), _p(a3, _u8p),
+                                 _p(mx, _f64p), _p(nm, _i32p))
+    _check(rc, "mismatch")
+    return dict(delta=d, tis_weight=w, seq_k1=k1, seq_k3=k3, accept_k1=a1, accept_k3=a3, seq_max_abs_delta=mx,
+                seq_mismatches=nm)
+
+
 def delta(logp_train, logp_rollout):
     lib = _load()
     a = _c(logp_train, np.float64)

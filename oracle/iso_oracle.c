@@ -23,7 +23,9 @@
  *     blog, §7 "LogP"].
  *   - selected-token logprob = log-softmax over the vocabulary gathered at
  *     the chosen token: [RL-Kernel blog, §1 table; §4 "Right Linear LogP
- *     box"]; delta_t: [VeXact paper, §2 Eq. (1)].
+ *     box"]; delta_t: [VeXact paper, §2 Eq. (1)]; mismatch diagnostics
+ *     (K1, K3, truncated importance weights, sequence rejection): [VeXact
+ *     paper, §4.1, §4.2 Eq. (6)-(7), Appendix A.4].
  *   - RMSNorm reduction over the hidden dimension: [RL-Kernel blog, §4
  *     table]; batch-invariant RMSNorm: [VeXact paper, §3.1].
  *   - MoE: deterministic top-k routing, packed gate/up -> SwiGLU -> down as
@@ -555,4 +557,47 @@ int iso_oracle_moe_combine(const uint16_t* y_slots, const double* w, int T, int 
 
 void iso_oracle_delta(const double* logp_train, const double* logp_rollout, int64_t n, double* delta) {
   for (int64_t i = 0; i < n; ++i) delta[i] = logp_train[i] - logp_rollout[i];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mismatch diagnostics over packed sequences of (train, rollout) logprobs  */
+/* [VeXact paper, §2 Eq. (1): delta_t; §4.1 "KL estimators are not          */
+/*  sufficient indicators": K1(r) = -log r, K3(r) = (r - 1) - log r;        */
+/*  §4.2 Eq. (6): truncated importance weight min(r_corr, tau_tok),         */
+/*  Eq. (7): sequence rejection 1[S_seq <= tau_seq] with                    */
+/*  S_seq = sum_t K(q_t), q_t = r_corr,t = pi_train / pi_rollout;           */
+/*  Appendix A.4: tau_tok = 2, tau_seq = 0.001]                             */
+/* Sequence b holds tokens [offsets[b], offsets[b+1]).  Everything is       */
+/* computed in double, summed in ascending token order.                     */
+/* ------------------------------------------------------------------------ */
+
+int iso_oracle_mismatch(const float* logp_train, const float* logp_rollout, const int32_t* offsets, int B,
+                        double tau_tok, double tau_seq, double* delta, double* tis_weight, double* seq_k1,
+                        double* seq_k3, uint8_t* accept_k1, uint8_t* accept_k3, double* seq_max_abs_delta,
+                        int32_t* seq_mismatches) {
+  if (B < 0 || !offsets) return -1;
+  for (int b = 0; b < B; ++b) {
+    if (offsets[b + 1] < offsets[b]) return -2;
+    double s1 = 0.0, s3 = 0.0, mx = 0.0;
+    int32_t nmis = 0;
+    for (int32_t t = offsets[b]; t < offsets[b + 1]; ++t) {
+      const double d = (double)logp_train[t] - (double)logp_rollout[t]; /* Eq. (1) */
+      const double r = exp(d);                                           /* r_corr */
+      const double k1 = -log(r);
+      const double k3 = (r - 1.0) - log(r);
+      delta[t] = d;
+      tis_weight[t] = r < tau_tok ? r : tau_tok; /* min(r_corr, tau_tok) */
+      s1 += k1;
+      s3 += k3;
+      if (fabs(d) > mx) mx = fabs(d);
+      if (logp_train[t] != logp_rollout[t]) ++nmis;
+    }
+    seq_k1[b] = s1;
+    seq_k3[b] = s3;
+    accept_k1[b] = s1 <= tau_seq ? 1 : 0;
+    accept_k3[b] = s3 <= tau_seq ? 1 : 0;
+    seq_max_abs_delta[b] = mx;
+    seq_mismatches[b] = nmis;
+  }
+  return 0;
 }

@@ -346,3 +346,80 @@ def test_delta_matches_rlkernel_minimal_example():
     assert abs(math.exp(d) - fx["ratio_single_token_approx"]) < 5e-4
     assert abs(fx["tokens"] * d - fx["cumulative_delta"]) < 1e-9
     assert abs(math.exp(fx["tokens"] * d) - fx["ratio_cumulative_approx"]) < 5e-3
+
+
+# ------------------------------------------------------- mismatch diagnostics
+# VeXact paper: delta_t (§2 Eq. 1), K1 / K3 (§4.1), TIS min(r_corr, tau_tok) (§4.2 Eq. 6),
+# sequence rejection 1[sum_t K(r_corr,t) <= tau_seq] (Eq. 7-11, tau_tok = 2, tau_seq = 0.001).
+def _f32(x):
+    return float(np.float32(x))
+
+
+def test_mismatch_table1_delta_and_identity_rows():
+    g = json.load(open(os.path.join(GOLDEN, "vexact_table1_delta.json")))
+    tr = np.array(g["logp_train"], np.float32)
+    ro = np.array(g["logp_rollout"], np.float32)
+    r = oracle.mismatch(tr, ro, [0, len(tr)])
+    assert np.allclose(np.round(r["delta"], 3), g["delta"], atol=1e-12)
+    # the printed 3-decimal values differ in 3 of 8 positions
+    assert r["seq_mismatches"][0] == 3
+    assert r["seq_max_abs_delta"][0] == pytest.approx(0.133, abs=1e-6)
+    same = oracle.mismatch(tr, tr, [0, 4, 8])
+    assert np.all(same["delta"] == 0) and np.all(same["tis_weight"] == 1.0)
+    assert np.all(same["seq_k1"] == 0) and np.all(same["seq_k3"] == 0)
+    assert list(same["accept_k1"]) == [1, 1] and list(same["accept_k3"]) == [1, 1]
+    assert list(same["seq_mismatches"]) == [0, 0]
+
+
+def test_mismatch_closed_forms_and_truncation():
+    # rollout assigns a third of the training probability: r_corr = 3 -> weight truncated at tau_tok = 2
+    tr = np.array([0.0, -1.0, -0.5], np.float32)
+    ro = np.array([_f32(-math.log(3.0)), -1.25, -0.25], np.float32)
+    r = oracle.mismatch(tr, ro, [0, 3])
+    d = [float(tr[i]) - float(ro[i]) for i in range(3)]
+    assert list(r["delta"]) == d  # train minus rollout, in that order
+    rc = [math.exp(x) for x in d]
+    assert r["tis_weight"][0] == 2.0 and rc[0] > 2.0
+    assert r["tis_weight"][1] == pytest.approx(rc[1], rel=1e-15) and rc[1] < 2.0
+    assert r["tis_weight"][2] == pytest.approx(rc[2], rel=1e-15) and rc[2] < 1.0
+    k1 = math.fsum(-x for x in d)
+    k3 = math.fsum((math.exp(x) - 1.0) - x for x in d)
+    assert r["seq_k1"][0] == pytest.approx(k1, abs=1e-15)
+    assert r["seq_k3"][0] == pytest.approx(k3, rel=1e-14)
+    assert r["seq_k3"][0] > 0  # K3 is a non-negative estimator
+    assert r["seq_k1"][0] == pytest.approx(-0.0 - sum(d), abs=1e-15)
+
+
+def test_mismatch_sequence_sums_brute_force_and_masks():
+    rng = np.random.default_rng(7)
+    lens = [0, 1, 5, 300, 17, 2049]
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n = int(offs[-1])
+    ro = (-np.abs(rng.standard_normal(n)) * 2).astype(np.float32)
+    tr = (ro + (rng.standard_normal(n) * 1e-3)).astype(np.float32)
+    r = oracle.mismatch(tr, ro, offs)
+    for b in range(len(lens)):
+        seg = range(offs[b], offs[b + 1])
+        d = [float(tr[t]) - float(ro[t]) for t in seg]
+        s1 = math.fsum(-x for x in d)
+        s3 = math.fsum((math.exp(x) - 1.0) - x for x in d)
+        assert r["seq_k1"][b] == pytest.approx(s1, abs=1e-12)
+        assert r["seq_k3"][b] == pytest.approx(s3, rel=1e-9, abs=1e-18)
+        assert r["accept_k1"][b] == (1 if s1 <= 0.001 else 0)
+        assert r["accept_k3"][b] == (1 if s3 <= 0.001 else 0)
+        assert r["seq_max_abs_delta"][b] == (max(abs(x) for x in d) if d else 0.0)
+        assert r["seq_mismatches"][b] == sum(1 for t in seg if tr[t] != ro[t])
+    assert r["accept_k1"][0] == 1 and r["seq_k1"][0] == 0.0  # an empty sequence is accepted
+    # K3 ~ delta^2 / 2 for small delta
+    small = oracle.mismatch(np.array([1e-3], np.float32), np.array([0.0], np.float32), [0, 1])
+    dd = float(np.float32(1e-3))
+    assert small["seq_k3"][0] == pytest.approx(dd * dd / 2 + dd ** 3 / 6, rel=1e-6)
+
+
+def test_mismatch_rejection_threshold_sides():
+    # S_K1 = -sum(delta): 0.0005 is accepted, 0.002 is rejected (tau_seq = 0.001)
+    ro = np.zeros(4, np.float32)
+    acc = oracle.mismatch(np.full(4, -0.000125, np.float32), ro, [0, 4])
+    rej = oracle.mismatch(np.full(4, -0.0005, np.float32), ro, [0, 4])
+    assert acc["accept_k1"][0] == 1 and acc["seq_k1"][0] == pytest.approx(0.0005, rel=1e-6)
+    assert rej["accept_k1"][0] == 0 and rej["seq_k1"][0] == pytest.approx(0.002, rel=1e-6)
