@@ -395,6 +395,21 @@ def secondary(c, dev, stream, peaks, rank):
                           roofline_frac=byt / (peaks["hbm"] * 1e9) / (tt * 1e-3), bound="hbm")
     del x, y
 
+    # mismatch diagnostics over a packed rollout batch: 64 sequences, lengths ~ U[1, 8192] (seed 4)
+    g = torch.Generator().manual_seed(4)
+    lens = torch.randint(1, 8193, (64,), generator=g)
+    offs = torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(lens, 0)]).to(torch.int32).to(dev)
+    n = int(lens.sum())
+    lp_r = (-torch.abs(torch.randn(n, generator=g)) * 2).to(dev)
+    lp_t = lp_r + (torch.rand(n, generator=g) < 0.5).to(dev) * torch.randn(n, generator=g).to(dev) * 1e-3
+    dg = B.mismatch_diagnostics(c, lp_t, lp_r, offs, stream=stream)
+    tt = time_call(lambda: B.mismatch_diagnostics(c, lp_t, lp_r, offs, stream=stream, out=dg), 5, 2, stream, flush)
+    byt = 16.0 * n + 4.0 * 65 + 33.0 * 64  # 2 fp32 in + 2 fp32 out per token; offsets; per-sequence outputs
+    # bound by FP64 arithmetic (one block per sequence; this part has ~2 FP64 ops per clock per SM),
+    # not by its 16 bytes per token of traffic, so no HBM fraction is claimed
+    out["diagnostics"] = dict(workload=f"64 packed sequences, {n} tokens", ms=tt, tokens_per_s=n / (tt * 1e-3),
+                              hbm_gbs=byt / (tt * 1e-3) / 1e9, bound="fp64")
+
     # MoE expert layer: T=8192, H=2048, E=128, F=768, k=8
     T, H, E, F, k = 8192, 2048, 128, 768, 8
     xm, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=3, device=dev)

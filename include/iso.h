@@ -290,6 +290,30 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
                                 const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
                                 int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream);
 
+/* ------------------------------------------------- mismatch diagnostics
+ * [VeXact paper, §2 Eq. (1): delta_t = log pi_train - log pi_rollout; §4.1:
+ *  the K1(r) = -log r and K3(r) = (r - 1) - log r estimators; §4.2 Eq. (6):
+ *  truncated importance weight min(r_corr, tau_tok); Eq. (7)-(11): sequence
+ *  rejection 1[sum_t K(r_corr,t) <= tau_seq], r_corr = pi_train / pi_rollout;
+ *  Appendix A.4 uses tau_tok = 2, tau_seq = 0.001]
+ * logp_train, logp_rollout: [N] fp32, the selected-token logprobs of B packed
+ * sequences; seq_offsets: DEVICE [B+1] int32, sequence b = tokens
+ * [offsets[b], offsets[b+1]), nondecreasing, offsets[B] <= N.
+ * Per token (either may be NULL to skip): delta [N] fp32, tis_weight [N] fp32.
+ * Per sequence: seq_k1, seq_k3 [B] fp64 (sums of K1, K3 of r_corr),
+ * accept_k1, accept_k3 [B] uint8 (1 when the sum <= tau_seq), max |delta|
+ * [B] fp32, sum |delta| [B] fp64, count of tokens whose two logprobs differ
+ * [B] int32.  delta and r are evaluated in double (log r_corr = delta_t, so
+ * K1 = -delta_t, K3 = (r_corr - 1) - delta_t); each sequence is summed in a
+ * fixed order (thread-strided ascending sums, a shuffle tree per warp, warps
+ * in order), so results depend only on the sequence.  tau_tok > 0, tau_seq >= 0, else
+ * ISO_ERR_INVALID_ARG. */
+iso_status iso_mismatch_diagnostics(const iso_contract* c, const float* logp_train, const float* logp_rollout,
+                                    const int32_t* seq_offsets, int B, int N, double tau_tok, double tau_seq,
+                                    float* delta, float* tis_weight, double* seq_k1, double* seq_k3,
+                                    uint8_t* accept_k1, uint8_t* accept_k3, float* seq_max_abs_delta,
+                                    double* seq_sum_abs_delta, int32_t* seq_mismatches, iso_stream stream);
+
 /* --------------------------------------------------------- failure checks
  * Launches one kernel whose only job is a bounded wait on an mbarrier that
  * nothing ever completes; after timeout_ns it gives up, sets

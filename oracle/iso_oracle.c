@@ -568,7 +568,9 @@ void iso_oracle_delta(const double* logp_train, const double* logp_rollout, int6
 /*  S_seq = sum_t K(q_t), q_t = r_corr,t = pi_train / pi_rollout;           */
 /*  Appendix A.4: tau_tok = 2, tau_seq = 0.001]                             */
 /* Sequence b holds tokens [offsets[b], offsets[b+1]).  Everything is       */
-/* computed in double, summed in ascending token order.                     */
+/* computed in double, summed in ascending token order.  Since r_corr is    */
+/* pi_train / pi_rollout, log r_corr is delta_t itself: K1 = -delta_t and   */
+/* K3 = (r_corr - 1) - delta_t.                                             */
 /* ------------------------------------------------------------------------ */
 
 int iso_oracle_mismatch(const float* logp_train, const float* logp_rollout, const int32_t* offsets, int B,
@@ -583,8 +585,9 @@ int iso_oracle_mismatch(const float* logp_train, const float* logp_rollout, cons
     for (int32_t t = offsets[b]; t < offsets[b + 1]; ++t) {
       const double d = (double)logp_train[t] - (double)logp_rollout[t]; /* Eq. (1) */
       const double r = exp(d);                                           /* r_corr */
-      const double k1 = -log(r);
-      const double k3 = (r - 1.0) - log(r);
+      /* log r_corr = log pi_train - log pi_rollout = delta_t exactly */
+      const double k1 = -d;
+      const double k3 = (r - 1.0) - d;
       delta[t] = d;
       tis_weight[t] = r < tau_tok ? r : tau_tok; /* min(r_corr, tau_tok) */
       s1 += k1;

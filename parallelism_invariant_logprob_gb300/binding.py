@@ -60,6 +60,8 @@ _SIGNATURES = {
     "iso_moe_route": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp, _vp]),
     "iso_moe_permute_workspace": (_sz, [_int, _int, _int]),
     "iso_gemm_workspace": (_sz, [_vp, _int, _int, _int]),
+    "iso_mismatch_diagnostics": (_int, [_vp, _vp, _vp, _vp, _int, _int, ctypes.c_double, ctypes.c_double, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "iso_selected_logprob_partial_workspace": (_sz, [_vp, _int, _int]),
     "iso_selected_logprob_partial": (_int, [_vp, _vp, _vp, _i64, _vp, _int, _int, _int, _int, _int, _vp, _vp, _vp,
                                             _sz, _vp]),
@@ -262,6 +264,31 @@ def selected_logprob_combine(c: Contract, shard_v0, stats, zsel, ids, V: int, ou
                                             T, V, _stream(stream))
     c.lib.check(st, "iso_selected_logprob_combine")
     return out
+
+
+def mismatch_diagnostics(c: Contract, logp_train, logp_rollout, offsets, tau_tok=2.0, tau_seq=0.001, stream=None,
+                         out=None):
+    """Per token delta and min(r_corr, tau_tok); per sequence sums of K1 / K3, rejection masks,
+    max and sum of |delta| and the count of differing tokens (all device tensors).  `out`: a
+    dict returned by an earlier call of the same sizes, reused as the output buffers."""
+    import torch
+    N = logp_train.numel()
+    B = offsets.numel() - 1
+    dev = logp_train.device
+    r = out if out is not None else dict(delta=torch.empty(N, dtype=torch.float32, device=dev),
+             tis_weight=torch.empty(N, dtype=torch.float32, device=dev),
+             seq_k1=torch.empty(B, dtype=torch.float64, device=dev), seq_k3=torch.empty(B, dtype=torch.float64, device=dev),
+             accept_k1=torch.empty(B, dtype=torch.uint8, device=dev), accept_k3=torch.empty(B, dtype=torch.uint8, device=dev),
+             seq_max_abs_delta=torch.empty(B, dtype=torch.float32, device=dev),
+             seq_sum_abs_delta=torch.empty(B, dtype=torch.float64, device=dev),
+             seq_mismatches=torch.empty(B, dtype=torch.int32, device=dev))
+    st = c.lib.iso_mismatch_diagnostics(c.handle, _ptr(logp_train), _ptr(logp_rollout), _ptr(offsets), B, N, tau_tok,
+                                        tau_seq, _ptr(r["delta"]), _ptr(r["tis_weight"]), _ptr(r["seq_k1"]),
+                                        _ptr(r["seq_k3"]), _ptr(r["accept_k1"]), _ptr(r["accept_k3"]),
+                                        _ptr(r["seq_max_abs_delta"]), _ptr(r["seq_sum_abs_delta"]),
+                                        _ptr(r["seq_mismatches"]), _stream(stream))
+    c.lib.check(st, "iso_mismatch_diagnostics")
+    return r
 
 
 def selected_logprob_min_workspace(c: Contract, T: int, V: int) -> int:

@@ -62,6 +62,8 @@ void trace(const char* what, int a, int b, int c, int d) {
 
 }  // namespace
 
+bool device_ready() { return ensure_device_state(); }
+
 unsigned int* device_status_ptr() {
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return nullptr;

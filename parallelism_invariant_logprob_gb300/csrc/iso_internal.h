@@ -93,6 +93,7 @@ struct GemmParams {
 };
 
 // Library-wide state, per device.
+bool device_ready();                // per-device state looked up (status word address, SM count)
 unsigned int* device_status_ptr();  // device address of the status word (current device)
 uint64_t wait_timeout_ns();
 int sm_count();
