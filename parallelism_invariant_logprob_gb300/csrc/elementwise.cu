@@ -183,37 +183,52 @@ __global__ void lse_fold_tiles_kernel(const float2* __restrict__ tile_stats, flo
   chunk_stats[idx] = v;
 }
 
-// Per row: the C chunk statistics are merged by the balanced pairwise tree
-// with the odd node carried up, evaluated as a binary counter (merge two
-// equal-size subtrees as soon as both exist, then collapse right to left),
-// which builds exactly that tree.  lse = m + logf(s); out = z_sel - lse.
+// Per row: the C chunk statistics are merged by the balanced pairwise tree with the odd node
+// carried up: level by level, node i of the next level is node 2i (left, lower chunks) merged
+// with node 2i+1, and an odd last node passes up unchanged.  One warp per row holds the row's
+// nodes in shared memory and merges each level's pairs in parallel (log2 C levels).
+// lse = m + logf(s); out = z_sel - lse.
 // zsel holds one [T] array per vocab shard; a row's selected logit comes from the shard whose
 // chunk range [chunk0[r], chunk0[r+1]) holds the id's chunk (one shard: chunk0 = {0, C}).
-__global__ void lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
-                                    const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
-                                    ShardBounds shards, unsigned int* status) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  float sm[10], ss[10];
-  int sz[10];
-  int depth = 0;
-  for (int c = 0; c < C; ++c) {
-    const float2 v = stats[static_cast<int64_t>(c) * T + t];
-    sm[depth] = v.x;
-    ss[depth] = v.y;
-    sz[depth] = 1;
-    ++depth;
-    while (depth >= 2 && sz[depth - 1] == sz[depth - 2]) {
-      lse_merge_into(sm[depth - 2], ss[depth - 2], sm[depth - 1], ss[depth - 1]);
-      sz[depth - 2] *= 2;
-      --depth;
+constexpr int kFinalizeWarps = 8;
+constexpr int kFinalizeMaxChunks = 256;
+
+__global__ void __launch_bounds__(32 * kFinalizeWarps)
+    lse_finalize_kernel(const float2* __restrict__ stats, const float* __restrict__ zsel,
+                        const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
+                        ShardBounds shards, unsigned int* status) {
+  __shared__ float2 node[kFinalizeWarps][kFinalizeMaxChunks];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int t = blockIdx.x * kFinalizeWarps + w;
+  if (t >= T) return;  // whole warps leave together
+  float2* nd = node[w];
+  for (int c = lane; c < C; c += 32) nd[c] = stats[static_cast<int64_t>(c) * T + t];
+  __syncwarp();
+  for (int n = C; n > 1; n = (n + 1) >> 1) {
+    const int pairs = n >> 1;
+    float2 res[kFinalizeMaxChunks / 64];
+#pragma unroll
+    for (int q = 0; q < kFinalizeMaxChunks / 64; ++q) {
+      const int i = lane + 32 * q;
+      if (i < pairs) {
+        float2 a = nd[2 * i];
+        const float2 b2 = nd[2 * i + 1];
+        lse_merge_into(a.x, a.y, b2.x, b2.y);
+        res[q] = a;
+      }
     }
+    const float2 carry = (n & 1) ? nd[n - 1] : make_float2(0.f, 0.f);
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kFinalizeMaxChunks / 64; ++q) {
+      const int i = lane + 32 * q;
+      if (i < pairs) nd[i] = res[q];
+    }
+    if ((n & 1) && lane == 0) nd[pairs] = carry;
+    __syncwarp();
   }
-  while (depth >= 2) {
-    lse_merge_into(sm[depth - 2], ss[depth - 2], sm[depth - 1], ss[depth - 1]);
-    sz[depth - 2] += sz[depth - 1];
-    --depth;
-  }
+  if (lane != 0) return;
   const int id = ids[t];
   if (id < 0 || id >= V) {
     out[t] = __int_as_float(0x7fc00000);
@@ -224,7 +239,7 @@ __global__ void lse_finalize_kernel(const float2* __restrict__ stats, const floa
   int owner = 0;
   for (int r = 1; r < shards.n; ++r)
     if (shards.chunk0[r] <= chunk) owner = r;
-  const float lse = __fadd_rn(sm[0], logf(ss[0]));
+  const float lse = __fadd_rn(nd[0].x, logf(nd[0].y));
   out[t] = __fsub_rn(zsel[static_cast<int64_t>(owner) * T + t], lse);
 }
 
@@ -540,8 +555,8 @@ cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, c
 
 cudaError_t launch_lse_combine(const float2* chunk_stats, const float* zsel, const int32_t* ids, float* out, int T,
                                int C, int V, const ShardBounds& shards, cudaStream_t s) {
-  lse_finalize_kernel<<<(T + 127) / 128, 128, 0, s>>>(chunk_stats, zsel, ids, out, T, C, V, shards,
-                                                       device_status_ptr());
+  lse_finalize_kernel<<<(T + kFinalizeWarps - 1) / kFinalizeWarps, 32 * kFinalizeWarps, 0, s>>>(
+      chunk_stats, zsel, ids, out, T, C, V, shards, device_status_ptr());
   return cudaGetLastError();
 }
 
