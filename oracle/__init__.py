@@ -23,6 +23,9 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
       matmul + SwiGLU, one-hot gates, equal gates)
   delta          : pinned (worked examples printed in the VeXact paper, Table 1,
       and the RL-Kernel blog, §1 "Minimal Example")
+  attention      : pinned (numpy softmax(QK^T)V brute force per head with the GQA
+      map, one visible key -> that value row, equal scores -> mean of the visible
+      values, causality: keys past a row's position do not change it)
   mismatch       : pinned (Table 1 deltas and mismatch count, identical inputs,
       closed forms of r_corr, K1, K3 and the tau_tok truncation, math.fsum
       brute-force sequence sums, both sides of the tau_seq rejection, the
@@ -76,6 +79,8 @@ def _load():
                                          _int, _u16p, _u16p, _f64p, _int]
     lib.iso_oracle_moe_combine.argtypes = [_u16p, _f64p, _int, _int, _int, _u16p, _f64p]
     lib.iso_oracle_delta.argtypes = [_f64p, _f64p, _i64, _f64p]
+    lib.iso_oracle_attention.argtypes = [_u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _int, _int, _int, _int,
+                                         ctypes.c_double, _f64p, _u16p, _f64p]
     lib.iso_oracle_mismatch.argtypes = [_f32p, _f32p, _i32p, _int, ctypes.c_double, ctypes.c_double, _f64p, _f64p,
                                         _f64p, _f64p, _u8p, _u8p, _f64p, _i32p]
     _lib = lib
@@ -285,6 +290,29 @@ def moe_combine(y_slots, w, exact=False):
 
 
 # ----------------------------------------------------------------- delta_t
+def attention(Q, K, V, q_start, k_start, pos0, scale):
+    """Causal attention over packed sequences (plain definition in double).  Q [Tq, Hq, d],
+    K and V [Tk, Hkv, d] as bf16 bit patterns; returns dict(out (bf16 bits), out_exact, lse)."""
+    lib = _load()
+    Q = _c(Q, np.uint16)
+    K = _c(K, np.uint16)
+    V = _c(V, np.uint16)
+    qs = _c(q_start, np.int32)
+    ks = _c(k_start, np.int32)
+    p0 = _c(pos0, np.int32)
+    Tq, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    B = qs.size - 1
+    oe = np.empty((Tq, Hq, d), np.float64)
+    o = np.empty((Tq, Hq, d), np.uint16)
+    lse = np.empty((Tq, Hq), np.float64)
+    rc = lib.iso_oracle_attention(_p(Q, _u16p), _p(K, _u16p), _p(V, _u16p), _p(qs, _i32p), _p(ks, _i32p),
+                                  _p(p0, _i32p), B, Hq, Hkv, d, float(scale), _p(oe, _f64p), _p(o, _u16p),
+                                  _p(lse, _f64p))
+    _check(rc, "attention")
+    return dict(out=o, out_exact=oe, lse=lse)
+
+
 def mismatch(logp_train, logp_rollout, offsets, tau_tok=2.0, tau_seq=0.001):
     """Mismatch diagnostics over packed sequences (VeXact paper, Eq. 1, 6, 7; K1/K3 of §4.1):
     per token delta, min(r_corr, tau_tok); per sequence sum K1, sum K3, the rejection

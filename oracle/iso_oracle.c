@@ -604,3 +604,68 @@ int iso_oracle_mismatch(const float* logp_train, const float* logp_rollout, cons
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Causal attention over packed variable-length sequences                    */
+/* [RL-Kernel blog, §4 "Focus: The Shared Dependency of Attention and Linear */
+/*  LogP on LogSumExp": softmax over the visible keys, LSE statistic;        */
+/*  §6 table row 03 and §7 "Attention": no KV split, fixed chunking; VeXact  */
+/*  paper, §3.1: KV splitting disabled]                                      */
+/* Q [Tq x Hq x d], K and V [Tk x Hkv x d] bf16; query head h reads KV head  */
+/* h / (Hq / Hkv).  Sequence b owns query rows [q_start[b], q_start[b+1])    */
+/* and keys [k_start[b], k_start[b+1]); its query row r sits at position     */
+/* p = pos0[b] + (r - q_start[b]) and sees the keys k_start[b] .. k_start[b] */
+/* + p.  The plain definition in double: s_j = scale * (q . k_j),            */
+/* m = max_j s_j, l = sum_j exp(s_j - m), out = sum_j exp(s_j - m) v_j / l,  */
+/* lse = m + log(l).                                                         */
+/* ------------------------------------------------------------------------ */
+
+int iso_oracle_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* q_start,
+                         const int32_t* k_start, const int32_t* pos0, int B, int Hq, int Hkv, int d, double scale,
+                         double* out_exact, uint16_t* out, double* lse) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+  const int group = Hq / Hkv;
+  double* s = NULL;
+  int cap = 0;
+  for (int b = 0; b < B; ++b) {
+    for (int32_t r = q_start[b]; r < q_start[b + 1]; ++r) {
+      const int32_t p = pos0[b] + (r - q_start[b]);
+      const int32_t nvis = p + 1;
+      if (p < 0 || k_start[b] + nvis > k_start[b + 1]) {
+        free(s);
+        return -2;
+      }
+      if (nvis > cap) {
+        free(s);
+        cap = nvis;
+        s = (double*)malloc(sizeof(double) * (size_t)cap);
+        if (!s) return -3;
+      }
+      for (int h = 0; h < Hq; ++h) {
+        const int g = h / group;
+        const uint16_t* q = Q + ((int64_t)r * Hq + h) * d;
+        double m = -INFINITY;
+        for (int32_t j = 0; j < nvis; ++j) {
+          const uint16_t* k = K + ((int64_t)(k_start[b] + j) * Hkv + g) * d;
+          double dot = 0.0;
+          for (int e = 0; e < d; ++e) dot += iso_oracle_bf16_to_double(q[e]) * iso_oracle_bf16_to_double(k[e]);
+          s[j] = scale * dot;
+          if (s[j] > m) m = s[j];
+        }
+        double l = 0.0;
+        for (int32_t j = 0; j < nvis; ++j) l += exp(s[j] - m);
+        double* o = out_exact + ((int64_t)r * Hq + h) * d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        for (int32_t j = 0; j < nvis; ++j) {
+          const double w = exp(s[j] - m) / l;
+          const uint16_t* v = V + ((int64_t)(k_start[b] + j) * Hkv + g) * d;
+          for (int e = 0; e < d; ++e) o[e] += w * iso_oracle_bf16_to_double(v[e]);
+        }
+        for (int e = 0; e < d; ++e) out[((int64_t)r * Hq + h) * d + e] = iso_oracle_double_to_bf16(o[e]);
+        lse[(int64_t)r * Hq + h] = m + log(l);
+      }
+    }
+  }
+  free(s);
+  return 0;
+}

@@ -423,3 +423,66 @@ def test_mismatch_rejection_threshold_sides():
     rej = oracle.mismatch(np.full(4, -0.0005, np.float32), ro, [0, 4])
     assert acc["accept_k1"][0] == 1 and acc["seq_k1"][0] == pytest.approx(0.0005, rel=1e-6)
     assert rej["accept_k1"][0] == 0 and rej["seq_k1"][0] == pytest.approx(0.002, rel=1e-6)
+
+
+# ------------------------------------------------------------------- attention
+# RL-Kernel blog §4: softmax over the visible keys (causal), the LSE statistic.
+def _bf16_np(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def _from_bits(b):
+    return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).float().double().numpy()
+
+
+def _attn_case(seed, lens_q, lens_k, pos0, Hq=4, Hkv=2, d=16):
+    rng = np.random.default_rng(seed)
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    Q = _bf16_np(rng.standard_normal((Tq, Hq, d)))
+    K = _bf16_np(rng.standard_normal((Tk, Hkv, d)))
+    V = _bf16_np(rng.standard_normal((Tk, Hkv, d)))
+    qs = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    ks = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    return Q, K, V, qs, ks, np.array(pos0, np.int32)
+
+
+def test_attention_matches_numpy_brute_force():
+    Q, K, V, qs, ks, p0 = _attn_case(3, [5, 3], [5, 9], [0, 6])
+    scale = 0.25
+    r = oracle.attention(Q, K, V, qs, ks, p0, scale)
+    Qf, Kf, Vf = _from_bits(Q), _from_bits(K), _from_bits(V)
+    for b in range(2):
+        for i in range(qs[b + 1] - qs[b]):
+            row, p = qs[b] + i, p0[b] + i
+            for h in range(4):
+                g = h // 2  # 4 query heads over 2 KV heads
+                keys = Kf[ks[b]:ks[b] + p + 1, g]
+                s = scale * (keys @ Qf[row, h])
+                w = np.exp(s - s.max())
+                want = (w[:, None] * Vf[ks[b]:ks[b] + p + 1, g]).sum(0) / w.sum()
+                assert np.allclose(r["out_exact"][row, h], want, rtol=1e-12, atol=1e-12)
+                assert r["lse"][row, h] == pytest.approx(s.max() + math.log(w.sum()), abs=1e-12)
+    # bf16 output is the round-to-nearest of the exact value (round_bf16 is pinned above)
+    assert np.array_equal(r["out"], oracle.round_bf16(r["out_exact"]))
+
+
+def test_attention_special_cases():
+    Q, K, V, qs, ks, p0 = _attn_case(4, [6], [6], [0])
+    r = oracle.attention(Q, K, V, qs, ks, p0, 0.3)
+    # position 0 sees one key: the output is that value row exactly
+    assert np.array_equal(r["out"][0], V[0, [0, 0, 1, 1]])
+    # zero queries give equal scores: the mean of the visible values, lse = log(count)
+    Z = np.zeros_like(Q)
+    rz = oracle.attention(Z, K, V, qs, ks, p0, 0.3)
+    Vf = _from_bits(V)
+    for i in range(6):
+        assert np.allclose(rz["out_exact"][i, 0], Vf[:i + 1, 0].mean(0), atol=1e-12)
+        assert rz["lse"][i, 0] == pytest.approx(math.log(i + 1), abs=1e-12)
+    # causality: changing keys / values past a row's position leaves the row unchanged
+    K2, V2 = K.copy(), V.copy()
+    K2[4:] ^= 0x0100
+    V2[4:] ^= 0x0100
+    r2 = oracle.attention(Q, K2, V2, qs, ks, p0, 0.3)
+    assert np.array_equal(r2["out_exact"][:4], r["out_exact"][:4])
+    assert not np.array_equal(r2["out_exact"][4:], r["out_exact"][4:])
