@@ -94,7 +94,8 @@ int iso_contract_leaf_count(const iso_contract* c);
 iso_status iso_sha256(const void* data, size_t n, uint8_t digest[32]);
 const char* iso_status_string(iso_status s);
 /* Synchronizes `stream`, then reads and clears the current device's status
- * word: ISO_OK, ISO_ERR_DEVICE_TIMEOUT or ISO_ERR_BAD_TOKEN_ID. */
+ * word: ISO_OK, ISO_ERR_DEVICE_TIMEOUT, ISO_ERR_BAD_TOKEN_ID or ISO_ERR_SHAPE
+ * (a device-side shape check failed, e.g. iso_attention's sequence table). */
 iso_status iso_last_device_status(iso_stream stream);
 
 /* ---------------------------------------------------------------- iso_gemm
@@ -313,6 +314,36 @@ iso_status iso_mismatch_diagnostics(const iso_contract* c, const float* logp_tra
                                     float* delta, float* tis_weight, double* seq_k1, double* seq_k3,
                                     uint8_t* accept_k1, uint8_t* accept_k3, float* seq_max_abs_delta,
                                     double* seq_sum_abs_delta, int32_t* seq_mismatches, iso_stream stream);
+
+/* ------------------------------------------------------------ attention
+ * [RL-Kernel blog, §4 "Focus: The Shared Dependency of Attention and Linear
+ *  LogP on LogSumExp": softmax over the visible keys and its LSE statistic;
+ *  §6 table row 03 and §7 "Attention": no KV split, fixed block partitioning
+ *  and a fixed rescale-merge order; VeXact paper, §3.1: KV splitting
+ *  disabled so prefill and decode reduce alike]
+ * Causal attention over B packed variable-length sequences with grouped KV
+ * heads.  Q [Tq x Hq x d], K and V [Tk x Hkv x d]: bf16, row-major, DEVICE,
+ * 16-byte aligned (ISO_ERR_ALIGNMENT).  q_start, k_start: DEVICE [B+1] int32;
+ * pos0: DEVICE [B] int32.  Sequence b owns query rows [q_start[b],
+ * q_start[b+1]) and keys [k_start[b], k_start[b+1]); its query row r sits at
+ * position p = pos0[b] + (r - q_start[b]) and attends to keys k_start[b] ..
+ * k_start[b] + p, so k_start[b] + pos0[b] + (rows of b) <= k_start[b+1].
+ * Query head h reads KV head h / (Hq / Hkv) (Hq % Hkv != 0: ISO_ERR_SHAPE).
+ * d == 128 (else ISO_ERR_UNSUPPORTED).  max_q_rows >= the largest query row
+ * count of a sequence (it sizes the grid).  out [Tq x Hq x d] bf16 =
+ * softmax(scale q.k) V; lse [Tq x Hq] fp32 = m + log l (NULL to skip).
+ * The merge runs over fixed 128-key chunks of each sequence, in ascending
+ * order, one online-softmax step per chunk; nothing depends on the other
+ * rows of the call, so a row's bits are the same in a prefill (many rows) and
+ * a decode call (one row at the same position), whatever the batch.  Keys
+ * past a row's position inside its last chunk are masked but still read: K
+ * and V must hold finite values in every row [0, Tk).  A sequence table that
+ * breaks the rules above sets ISO_ERR_SHAPE in the device status word and its
+ * rows are left unwritten.  Empty calls (B, Tq or max_q_rows 0) are no-ops. */
+iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, const iso_bf16* K, const iso_bf16* V,
+                         const int32_t* q_start, const int32_t* k_start, const int32_t* pos0, int B, int Tq,
+                         int Tk, int Hq, int Hkv, int d, int max_q_rows, float scale, iso_bf16* out, float* lse,
+                         iso_stream stream);
 
 /* --------------------------------------------------------- failure checks
  * Launches one kernel whose only job is a bounded wait on an mbarrier that

@@ -24,6 +24,8 @@ STATUS_NAMES = {
     7: "ISO_ERR_WORKSPACE", 8: "ISO_ERR_CUDA", 9: "ISO_ERR_DEVICE_TIMEOUT", 10: "ISO_ERR_NOT_IMPLEMENTED",
     11: "ISO_ERR_BAD_TOKEN_ID",
 }
+for _code, _name in STATUS_NAMES.items():
+    globals()[_name] = _code
 ISO_TREE_BALANCED_BINARY = 0
 ISO_F32, ISO_BF16 = 0, 1
 
@@ -75,6 +77,8 @@ _SIGNATURES = {
                                     _vp, _sz, _vp]),
     "iso_selftest_bounded_wait": (_int, [_u64, _vp]),
     "iso_selected_logprob_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
+    "iso_attention": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _int,
+                             ctypes.c_float, _vp, _vp, _vp]),
 }
 
 
@@ -289,6 +293,29 @@ def mismatch_diagnostics(c: Contract, logp_train, logp_rollout, offsets, tau_tok
                                         _ptr(r["seq_mismatches"]), _stream(stream))
     c.lib.check(st, "iso_mismatch_diagnostics")
     return r
+
+
+def attention(c: Contract, Q, K, V, q_start, k_start, pos0, scale: float, max_q_rows: int | None = None,
+              out=None, lse=None, want_lse: bool = True, stream=None):
+    """Causal attention over packed sequences.  Q [Tq, Hq, d], K and V [Tk, Hkv, d] bf16;
+    q_start, k_start [B+1] and pos0 [B] int32 device tensors.  Returns (out, lse); lse is
+    None when want_lse is False.  max_q_rows defaults to the largest q_start difference
+    (read back from the device)."""
+    import torch
+    Tq, Hq, d = Q.shape
+    Tk, Hkv = K.shape[0], K.shape[1]
+    B = q_start.numel() - 1
+    if max_q_rows is None:
+        max_q_rows = int((q_start[1:] - q_start[:-1]).max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty(Tq, Hq, d, dtype=torch.bfloat16, device=Q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(Tq, Hq, dtype=torch.float32, device=Q.device)
+    st = c.lib.iso_attention(c.handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(q_start), _ptr(k_start), _ptr(pos0), B, Tq,
+                             Tk, Hq, Hkv, d, max_q_rows, float(scale), _ptr(out), _ptr(lse) if lse is not None else None,
+                             _stream(stream))
+    c.lib.check(st, "iso_attention")
+    return out, lse
 
 
 def selected_logprob_min_workspace(c: Contract, T: int, V: int) -> int:

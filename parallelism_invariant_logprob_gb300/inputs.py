@@ -15,6 +15,8 @@ datasets and model weights are not used):
   moe       x ~ N(0,1) bf16 [T,H]; W1 ~ N(0,0.02^2) bf16 [E,H,2F];
             W2 ~ N(0,0.02^2) bf16 [E,F,H]; router logits ~ N(0,1) fp32 [T,E]
   rollout   64 sequence lengths ~ U[1,8192]; states ~ N(0,1) bf16 [sum,H]
+  attention packed sequences (query rows at positions pos0.., keys = cache +
+            own rows + unseen tail); Q, K, V ~ N(0,1) bf16 [T, heads, 128]
 Exact-integer variants draw small integers so every summation order is exact.
 """
 from __future__ import annotations
@@ -85,3 +87,22 @@ def random_partition(E: int, P: int, seed: int) -> torch.Tensor:
     """A seeded expert -> partition map (int32 [E]) with values in [0, P)."""
     g = _gen(seed, "cpu")
     return torch.randint(0, P, (E,), generator=g, dtype=torch.int32)
+
+
+def attention_inputs(q_lens, pos0, Hq: int, Hkv: int, d: int, seed: int, extra_keys=None):
+    """Packed causal-attention inputs (CPU tensors).  Sequence b has q_lens[b] query rows at
+    positions pos0[b], pos0[b]+1, ... and pos0[b] + q_lens[b] + extra_keys[b] keys (the KV
+    cache of earlier positions, then the keys of its query rows, then keys no row sees).
+    Q, K, V ~ N(0,1) bf16; returns Q, K, V, q_start, k_start, pos0 (int32)."""
+    B = len(q_lens)
+    extra = list(extra_keys) if extra_keys is not None else [0] * B
+    k_lens = [int(pos0[b]) + int(q_lens[b]) + int(extra[b]) for b in range(B)]
+    q_start = torch.zeros(B + 1, dtype=torch.int32)
+    k_start = torch.zeros(B + 1, dtype=torch.int32)
+    q_start[1:] = torch.tensor([int(v) for v in q_lens], dtype=torch.int64).cumsum(0).to(torch.int32)
+    k_start[1:] = torch.tensor(k_lens, dtype=torch.int64).cumsum(0).to(torch.int32)
+    Tq, Tk = int(q_start[-1]), int(k_start[-1])
+    Q = normal_bf16((Tq, Hq, d), 1.0, seed * 3 + 0)
+    K = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 1)
+    V = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 2)
+    return Q, K, V, q_start, k_start, torch.tensor([int(v) for v in pos0], dtype=torch.int32)

@@ -1,0 +1,186 @@
+"""GPU parity and invariance of iso_attention, the causal attention kernel with a fixed
+KV-chunk merge (RL-Kernel blog, §4 "Focus: The Shared Dependency of Attention and Linear LogP
+on LogSumExp", §6 row 03 and §7 "Attention"; VeXact paper, §3.1: KV splitting disabled).
+
+Tolerance, from the arithmetic: the kernel rounds the softmax weights P to bf16 before the
+P.V product (relative error <= 2^-9 per weight, so <= 2^-9 max|v| on the weighted sum) and
+rounds the output to bf16 (<= 2^-9 |out|); the fp32 score and sum errors are far smaller.  So
+|out - exact| <= 2^-8 (max|V| + |exact|) element by element, and |lse - exact| <= 1e-4.  The
+lse bound also catches a single key let in or left out at any tested length (that moves lse
+by log(1 + e^(s - lse)) >= ~1e-3 here)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parallelism_invariant_logprob_gb300 import binding as B
+from parallelism_invariant_logprob_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+D = 128
+SCALE = 1.0 / math.sqrt(D)
+
+
+def _bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _same_bits(a, b):
+    return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+@pytest.fixture(scope="module")
+def c8():
+    return B.Contract(8)
+
+
+def _run(c, Q, K, V, qs, ks, p0, **kw):
+    return B.attention(c, Q.to(DEV), K.to(DEV), V.to(DEV), qs.to(DEV), ks.to(DEV), p0.to(DEV), SCALE, **kw)
+
+
+def _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0):
+    ref = oracle.attention(_bits(Q), _bits(K), _bits(V), qs.numpy(), ks.numpy(), p0.numpy(), SCALE)
+    got = out.float().cpu().numpy().astype(np.float64)
+    vmax = float(V.float().abs().max())
+    err = np.abs(got - ref["out_exact"])
+    bound = 2.0 ** -8 * (vmax + np.abs(ref["out_exact"]))
+    assert np.all(err <= bound), float((err - bound).max())
+    lerr = np.abs(lse.cpu().numpy().astype(np.float64) - ref["lse"])
+    assert lerr.max() <= 1e-4, float(lerr.max())
+    return ref
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (4, 1)])
+def test_attention_vs_oracle_ragged(c8, Hq, Hkv):
+    # several tiles and KV chunks, ragged tails, a KV cache before the rows (pos0 > 0),
+    # keys past the last row, a one-row sequence and an empty one
+    q_lens = [130, 1, 0, 257, 64]
+    pos0 = [0, 300, 7, 5, 190]
+    extra = [3, 0, 2, 129, 0]
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, pos0, Hq, Hkv, D, seed=21, extra_keys=extra)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0)
+
+
+def test_attention_exact_tile_and_chunk_boundaries(c8):
+    # rows and positions that sit exactly on the 128-row tile and 128-key chunk grid
+    q_lens = [128, 256, 127, 129]
+    pos0 = [0, 128, 1, 127]
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, pos0, 2, 1, D, seed=22)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0)
+
+
+def test_attention_prefill_equals_decode_bitwise(c8):
+    # prefill over 300 rows of one sequence, then each sampled row alone as a decode step
+    # (one query row, its KV prefix only): the same bits
+    Hq, Hkv = 8, 2
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs([300], [0], Hq, Hkv, D, seed=23)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    out, lse = B.attention(c8, Qd, Kd, Vd, qs.to(DEV), ks.to(DEV), p0.to(DEV), SCALE)
+    for r in (0, 1, 126, 127, 128, 129, 200, 255, 256, 299):
+        one = torch.tensor([0, 1], dtype=torch.int32, device=DEV)
+        kv = torch.tensor([0, r + 1], dtype=torch.int32, device=DEV)
+        o1, l1 = B.attention(c8, Qd[r:r + 1].contiguous(), Kd[:r + 1].contiguous(), Vd[:r + 1].contiguous(), one, kv,
+                             torch.tensor([r], dtype=torch.int32, device=DEV), SCALE)
+        assert _same_bits(o1[0], out[r]), r
+        assert torch.equal(l1[0], lse[r]), r
+
+
+def test_attention_batch_composition_invariant(c8):
+    # a sequence's rows are the same bits alone, packed with others, or after other sequences
+    Hq, Hkv = 4, 2
+    q_lens, pos0, extra = [77, 140, 3, 200], [10, 0, 250, 60], [0, 5, 1, 0]
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, pos0, Hq, Hkv, D, seed=24, extra_keys=extra)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    for b in range(len(q_lens)):
+        q0, q1, k0, k1 = int(qs[b]), int(qs[b + 1]), int(ks[b]), int(ks[b + 1])
+        o1, l1 = _run(c8, Q[q0:q1].contiguous(), K[k0:k1].contiguous(), V[k0:k1].contiguous(),
+                      torch.tensor([0, q1 - q0], dtype=torch.int32), torch.tensor([0, k1 - k0], dtype=torch.int32),
+                      p0[b:b + 1].clone())
+        assert _same_bits(o1, out[q0:q1]), b
+        assert torch.equal(l1, lse[q0:q1]), b
+
+
+def test_attention_batched_decode_matches_prefill(c8):
+    # one decode call over several sequences (one row each, at different positions) against
+    # the prefill of each sequence
+    Hq, Hkv = 4, 1
+    q_lens = [150, 33, 260]
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, [0, 0, 0], Hq, Hkv, D, seed=25)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    last = [int(qs[b + 1]) - 1 for b in range(3)]
+    Qd = Q[last].contiguous()
+    dq = torch.tensor([0, 1, 2, 3], dtype=torch.int32)
+    dpos = torch.tensor([q_lens[b] - 1 for b in range(3)], dtype=torch.int32)
+    o1, l1 = _run(c8, Qd, K, V, dq, ks, dpos)
+    assert _same_bits(o1, out[last])
+    assert torch.equal(l1, lse[last])
+
+
+def test_attention_without_lse_and_empty(c8):
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs([40, 9], [3, 0], 2, 2, D, seed=26)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    out2, none = _run(c8, Q, K, V, qs, ks, p0, want_lse=False)
+    assert none is None and _same_bits(out, out2)
+    # no sequences / no rows: no-ops
+    e, _ = _run(c8, Q[:0], K, V, torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
+                torch.zeros(0, dtype=torch.int32))
+    assert e.numel() == 0
+    assert B.load().iso_last_device_status(None) == B.ISO_OK
+
+
+def test_attention_argument_errors(c8):
+    lib = B.load()
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs([4], [0], 2, 1, D, seed=27)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    qd, kd, pd = qs.to(DEV), ks.to(DEV), p0.to(DEV)
+    out = torch.empty(4, 2, D, dtype=torch.bfloat16, device=DEV)
+    P = B._ptr
+    s = B._stream()
+
+    def call(Qp=P(Qd), d=D, Hq=2, Hkv=1, outp=P(out)):
+        return lib.iso_attention(c8.handle, Qp, P(Kd), P(Vd), P(qd), P(kd), P(pd), 1, 4, 4, Hq, Hkv, d, 4, SCALE, outp,
+                                 None, s)
+
+    assert call(d=64) == B.ISO_ERR_UNSUPPORTED
+    assert call(Hq=3, Hkv=2) == B.ISO_ERR_SHAPE
+    assert call(Qp=B._vp(Qd.data_ptr() + 2)) == B.ISO_ERR_ALIGNMENT
+    assert call(outp=None) == B.ISO_ERR_INVALID_ARG
+    assert call() == B.ISO_OK
+    # a sequence table whose rows need keys past the sequence: flagged on the device, rows
+    # of that sequence left alone, nothing launched for them
+    bad_pos = torch.tensor([1], dtype=torch.int32, device=DEV)
+    out.fill_(0)
+    st = lib.iso_attention(c8.handle, P(Qd), P(Kd), P(Vd), P(qd), P(kd), P(bad_pos), 1, 4, 4, 2, 1, D, 4, SCALE,
+                           P(out), None, s)
+    assert st == B.ISO_OK
+    assert lib.iso_last_device_status(s) == B.ISO_ERR_SHAPE
+    assert int(out.view(torch.int16).abs().sum()) == 0
+    assert lib.iso_last_device_status(s) == B.ISO_OK
+
+
+@pytest.mark.slow
+def test_attention_full_size_sampled(c8):
+    """The bench's workload (packed prefill, 4096 query rows in 4 sequences of 1024, 32 query
+    heads over 8 KV heads) in the bench's launch; sampled rows against the oracle, each row
+    computed alone there (its KV prefix only)."""
+    Hq, Hkv = 32, 8
+    q_lens = [1024] * 4
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, [0] * 4, Hq, Hkv, D, seed=28)
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    Kb, Vb, Qb = _bits(K), _bits(V), _bits(Q)
+    vmax = float(V.float().abs().max())
+    g = torch.Generator().manual_seed(5)
+    for row in torch.randint(0, 4096, (12,), generator=g).tolist() + [0, 1023, 1024, 4095]:
+        b = row // 1024
+        p = row - b * 1024
+        k0 = int(ks[b])
+        ref = oracle.attention(Qb[row:row + 1], Kb[k0:k0 + p + 1], Vb[k0:k0 + p + 1], np.array([0, 1], np.int32),
+                               np.array([0, p + 1], np.int32), np.array([p], np.int32), SCALE)
+        got = out[row].float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref["out_exact"][0]) <= 2.0 ** -8 * (vmax + np.abs(ref["out_exact"][0]))), row
+        assert np.abs(lse[row].cpu().numpy() - ref["lse"][0]).max() <= 1e-4, row
