@@ -9,18 +9,21 @@
 //   out = softmax(scale * q . k) V  (bf16),  lse = m + log l  (fp32).
 //
 // The merge is the online softmax over fixed 128-key chunks in ascending order, one thread per
-// row.  For chunk c:
-//   s_j  = rn(S_j * scale) for visible keys (position <= p), -inf otherwise; S = q . k from a
-//          chain of 8 tcgen05 MMAs (K = 16 each, ascending dims)
-//   m'   = max(m, max_j s_j);  P_j = expf(s_j - m');  l_c = sum_j P_j  (fp32, ascending j)
-//   a    = expf(m - m') (chunk 0: none);  l = rn(rn(l * a) + l_c);  O = rn(O * a) when a != 1
+// row, in the base-2 domain (c2 = rn(scale * log2 e)).  For chunk c, with S = q . k from a
+// chain of 8 tcgen05 MMAs (K = 16 each, ascending dims) and S_j = -inf for keys past p:
+//   t    = rn(max_j S_j * c2)                           (max is exact in any order)
+//   m'   = max(m, t) if chunk 0 or t > m + 8, else m    (lazy: P stays below 2^8)
+//   P_j  = exp2f(fma(S_j, c2, -m'));  l_c = (sum of four interleaved partial sums, fixed order)
+//   a    = exp2f(m - m') (1 when m' = m);  l = rn(rn(l * a) + l_c);  O = rn(O * a) when a != 1
 //   O   += bf16(P) V   (8 tcgen05 MMAs, K = 16 keys each, ascending keys)
-// and at the end out = bf16_rn(O / l), lse = rn(m + logf(l)).  Every step depends only on the
-// row, its position and the chunk grid, never on the other rows of its tile or the launch, so
-// a decode call (one row) reproduces the row of a prefill call exactly.  A chunk wholly past a
-// row's position changes nothing in that row: a = 1, P = 0, O + 0 = O.
+// and at the end out = bf16_rn(O * rcp(l)), lse = rn(rn(m ln 2) + logf(l)).  Every step
+// depends only on the row, its position and the chunk grid, never on the other rows of its
+// tile or the launch, so a decode call (one row) reproduces the row of a prefill call exactly.
+// A chunk wholly past a row's position changes nothing in that row: t = -inf, a = 1, P = 0,
+// O + 0 = O.
 //
-// Structure: one CTA per (sequence, query head, tile of up to 128 query rows); 192 threads.
+// Structure: one CTA per (query head, sequence, tile of up to 128 query rows), the tiles with
+// the most chunks first; 192 threads.
 //   warp 0     TMA producer: Q once, then K and V chunks into a 2-stage ring
 //   warp 1     MMA issuer (one elected lane) and TMEM owner: S_{c+1} = Q K_{c+1}^T is issued
 //              before waiting for P_c, so it overlaps the softmax of chunk c
@@ -50,7 +53,7 @@ struct AttnParams {
   const int32_t* k_start;  // [B+1]
   const int32_t* pos0;     // [B]
   int B, Hq, Hkv;
-  float scale;
+  float scale_log2e;  // scale * log2(e), rounded to fp32
   __nv_bfloat16* out;  // [Tq x Hq x d]
   float* lse;          // [Tq x Hq]
   unsigned int* status;
@@ -64,19 +67,22 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(AT_ROWS, AT_D, false, true);
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+  const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<const uint32_t*>(&t);
 }
+constexpr float kLazy = 8.0f;  // base-2 headroom before the running maximum moves
+constexpr float kLn2 = 0.693147180559945309f;
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     iso_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // grid (Hq, B, tiles): the tiles furthest into their sequences (the most chunks) start first
+  const int h = blockIdx.x, b = blockIdx.y, tile = gridDim.z - 1 - blockIdx.z;
   const int q0 = p.q_start[b], nq = p.q_start[b + 1] - q0;
   // shape checks, uniform over the CTA and taken before any barrier or TMEM use: the grid
   // must cover every query row, and the last row's keys must lie inside the sequence
-  if (threadIdx.x == 0 && h == 0 && tile == gridDim.x - 1 &&
-      (nq > static_cast<int>(gridDim.x) * AT_ROWS || nq < 0 || p.pos0[b] < 0 ||
+  if (threadIdx.x == 0 && h == 0 && tile == static_cast<int>(gridDim.z) - 1 &&
+      (nq > static_cast<int>(gridDim.z) * AT_ROWS || nq < 0 || p.pos0[b] < 0 ||
        p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]))
     atomicOr(p.status, kDevBadShape);
   if (nq <= 0 || p.pos0[b] < 0 || p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]) return;
@@ -238,10 +244,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else {
     // ----------------------------------------------------- softmax / correction
+    // Scores are handled in the base-2 domain: t_j = S_j * scale * log2(e) (one FMA with the
+    // running maximum), P_j = 2^(t_j - m), and lse = m ln 2 + ln l at the end.  The running
+    // maximum m moves only when a chunk's maximum exceeds it by more than kLazy (2^kLazy
+    // bounds P and the sums stay far from overflow); then O and l are rescaled by 2^(m_old - m).
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int pos = pos_first + r;  // this row's position (rows past rows_valid compute unused values)
+    const int warp_pos_min = pos_first + quarter * 32;
+    const float c2 = p.scale_log2e;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int c = 0; c < n_chunks; ++c) {
@@ -258,24 +270,34 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
       for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld_tie(v + q * 32);
       const int kpos0 = c * AT_KEYS;
-      float mc = -INFINITY;
+      if (kpos0 + AT_KEYS - 1 > warp_pos_min) {  // a key of this chunk is past some row of the warp
 #pragma unroll
-      for (int j = 0; j < AT_KEYS; ++j) {
-        const float sj = (kpos0 + j <= pos) ? __fmul_rn(u2f(v[j]), p.scale) : -INFINITY;
-        v[j] = f2u(sj);
-        mc = fmaxf(mc, sj);
+        for (int j = 0; j < AT_KEYS; ++j)
+          if (kpos0 + j > pos) v[j] = f2u(-INFINITY);
       }
-      const float mn = fmaxf(m, mc);
-      float lc = 0.f;
+      // chunk maximum of the raw scores (max is exact, so the tree's shape cannot matter)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = u2f(v[i]);
+#pragma unroll
+      for (int j = 8; j < AT_KEYS; ++j) mx[j & 7] = fmaxf(mx[j & 7], u2f(v[j]));
+      const float mc = __fmul_rn(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
+                                 c2);
+      const float m_new = (m == -INFINITY || mc > m + kLazy) ? fmaxf(m, mc) : m;
+      const float alpha = (m == -INFINITY) ? 1.f : exp2f(__fsub_rn(m, m_new));  // 1 when m stays
+      m = m_new;
+      const float neg_m = -m;
+      // P_j = 2^(t_j - m); the chunk sum in four interleaved partial sums, combined in a fixed
+      // order
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < AT_KEYS; ++j) {
-        const float e = (u2f(v[j]) == -INFINITY) ? 0.f : expf(__fsub_rn(u2f(v[j]), mn));
+        const float e = exp2f(__fmaf_rn(u2f(v[j]), c2, neg_m));
         v[j] = f2u(e);
-        lc = __fadd_rn(lc, e);
+        ls[j & 3] = __fadd_rn(ls[j & 3], e);
       }
-      const float alpha = (m == -INFINITY) ? 1.f : expf(__fsub_rn(m, mn));
-      l = __fadd_rn(__fmul_rn(l, alpha), lc);
-      m = mn;
+      l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])));
       if (c > 0) {
         // PV of chunk c-1 done: O is current and the P buffer is free
         ok = __all_sync(0xffffffffu, mbar_wait(o_done, (c - 1) & 1, p.timeout_ns, abort_flag, p.status));
@@ -329,16 +351,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (r < rows_valid) {
         const int64_t row = q0 + tile * AT_ROWS + r;
         __nv_bfloat16* dst = p.out + (row * p.Hq + h) * AT_D;
+        const float inv_l = __frcp_rn(l);
 #pragma unroll
         for (int q = 0; q < AT_D / 8; ++q) {
           uint4 w;
-          w.x = pack_bf16x2(__fdiv_rn(u2f(o[q * 8 + 0]), l), __fdiv_rn(u2f(o[q * 8 + 1]), l));
-          w.y = pack_bf16x2(__fdiv_rn(u2f(o[q * 8 + 2]), l), __fdiv_rn(u2f(o[q * 8 + 3]), l));
-          w.z = pack_bf16x2(__fdiv_rn(u2f(o[q * 8 + 4]), l), __fdiv_rn(u2f(o[q * 8 + 5]), l));
-          w.w = pack_bf16x2(__fdiv_rn(u2f(o[q * 8 + 6]), l), __fdiv_rn(u2f(o[q * 8 + 7]), l));
+          w.x = pack_bf16x2(__fmul_rn(u2f(o[q * 8 + 0]), inv_l), __fmul_rn(u2f(o[q * 8 + 1]), inv_l));
+          w.y = pack_bf16x2(__fmul_rn(u2f(o[q * 8 + 2]), inv_l), __fmul_rn(u2f(o[q * 8 + 3]), inv_l));
+          w.z = pack_bf16x2(__fmul_rn(u2f(o[q * 8 + 4]), inv_l), __fmul_rn(u2f(o[q * 8 + 5]), inv_l));
+          w.w = pack_bf16x2(__fmul_rn(u2f(o[q * 8 + 6]), inv_l), __fmul_rn(u2f(o[q * 8 + 7]), inv_l));
           *reinterpret_cast<uint4*>(dst + q * 8) = w;
         }
-        if (p.lse) p.lse[row * p.Hq + h] = __fadd_rn(m, logf(l));
+        if (p.lse) p.lse[row * p.Hq + h] = __fadd_rn(__fmul_rn(m, kLn2), logf(l));
       }
     }
   }
@@ -369,7 +392,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   if (B == 0 || Tq == 0 || max_q_rows == 0) return ISO_OK;
   if (!Q || !K || !V || !q_start || !k_start || !pos0 || !out) return ISO_ERR_INVALID_ARG;
   if (Tk == 0) return ISO_ERR_SHAPE;  // a query row sees at least one key
-  if (Hq > 65535 || B > 65535) return ISO_ERR_UNSUPPORTED;
+  if (B > 65535 || (max_q_rows + AT_ROWS - 1) / AT_ROWS > 65535) return ISO_ERR_UNSUPPORTED;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
   if (mis & 15u) return ISO_ERR_ALIGNMENT;
@@ -388,7 +411,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.scale = scale;
+  p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = device_status_ptr();
@@ -402,7 +425,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
       return ISO_ERR_CUDA;
     attr_dev = dev;
   }
-  const dim3 grid((max_q_rows + AT_ROWS - 1) / AT_ROWS, Hq, B);
+  const dim3 grid(Hq, B, (max_q_rows + AT_ROWS - 1) / AT_ROWS);
   iso_attention_kernel<<<grid, AT_THREADS, AT_SMEM, static_cast<cudaStream_t>(stream)>>>(tQ, tK, tV, p);
   return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
