@@ -22,15 +22,20 @@
 // A chunk wholly past a row's position changes nothing in that row: t = -inf, a = 1, P = 0,
 // O + 0 = O.
 //
-// Structure: one CTA per (query head, sequence, tile of up to 128 query rows), the tiles with
-// the most chunks first; 192 threads.
-//   warp 0     TMA producer: Q once, then K and V chunks into a 2-stage ring
-//   warp 1     MMA issuer (one elected lane) and TMEM owner: S_{c+1} = Q K_{c+1}^T is issued
-//              before waiting for P_c, so it overlaps the softmax of chunk c
-//   warps 2-5  softmax / correction / output: one thread per query row (TMEM lane)
-// TMEM: S in two 128-column buffers, O in a third.  Shared memory: Q 32 KB, K and V 2 x 32 KB
-// each, P 32 KB (bf16, written by the softmax threads in the 128-byte-swizzled K-major layout
-// the MMA reads).  Every wait is bounded (abort flag, device status word).
+// Structure: one CTA per (query head, sequence, pair of 128-row query tiles A and B), the
+// pairs with the most chunks first; 320 threads.
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread per query row
+//              (TMEM lane); each also rescales its O rows and writes the output
+//   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 2-stage ring
+//   warp 9     MMA issuer (lane 0) and TMEM owner.  Per chunk j it issues, in this order,
+//              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the softmax of one tile runs, the
+//              tensor core works for the other.
+// TMEM (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B.  The softmax writes P as
+// packed bf16 pairs over the first 64 columns of its own S buffer, and the P V MMA reads A
+// from there.  tcgen05 MMAs execute in issue order, so PV_t(j) has read P_t(j) before
+// S_t(j+1) overwrites it, and the commit after S_t(j+1) also covers PV_t(j): the softmax
+// may rescale O_t as soon as it sees S_t(j+1).  Shared memory: Q 2 x 32 KB, K and V 2 stages
+// x 32 KB each.  Every wait is bounded (abort flag, device status word).
 #include <cuda_bf16.h>
 #include <stdio.h>
 
@@ -44,9 +49,11 @@ namespace {
 constexpr int AT_ROWS = 128;    // query rows per tile (the MMA's M)
 constexpr int AT_KEYS = 128;    // keys per chunk (N of QK^T, K of PV)
 constexpr int AT_D = 128;       // head dimension
-constexpr int AT_THREADS = 192;
+constexpr int AT_THREADS = 320;
 constexpr int AT_TILE_BYTES = AT_ROWS * AT_D * 2;  // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int AT_SMEM = 1024 /*align*/ + 6 * AT_TILE_BYTES + 256 /*barriers*/;
+constexpr int AT_WARP_PRODUCER = 8;
+constexpr int AT_WARP_MMA = 9;
 
 struct AttnParams {
   const int32_t* q_start;  // [B+1]
@@ -60,7 +67,8 @@ struct AttnParams {
   uint64_t timeout_ns;
 };
 
-// S = Q K^T: A (Q) and B (K) both K-major.  O += P V: A (P) K-major, B (V) MN-major.
+// S = Q K^T: A (Q) and B (K) both K-major in shared memory.  O += P V: A (P) K-major in
+// tensor memory, B (V) MN-major in shared memory.
 constexpr uint32_t kIdescS = idesc_bf16_f32(AT_ROWS, AT_KEYS, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(AT_ROWS, AT_D, false, true);
 
@@ -73,40 +81,63 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 constexpr float kLazy = 8.0f;  // base-2 headroom before the running maximum moves
 constexpr float kLn2 = 0.693147180559945309f;
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A: 128 lanes (rows) x K, two bf16 per
+// 32-bit column in K order.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Bounded wait on the phase of `bar` with the given parity, polled by every lane of the
+// warp; the outcome is made warp-uniform so the warp reaches each later .sync.aligned
+// tcgen05 op converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const AttnParams& p,
+                                          volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status));
+}
+
 __global__ void __launch_bounds__(AT_THREADS, 1)
     iso_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  // grid (Hq, B, tiles): the tiles furthest into their sequences (the most chunks) start first
-  const int h = blockIdx.x, b = blockIdx.y, tile = gridDim.z - 1 - blockIdx.z;
+  // grid (Hq, B, tile pairs): the pairs furthest into their sequences (the most chunks) start first
+  const int h = blockIdx.x, b = blockIdx.y, pair = gridDim.z - 1 - blockIdx.z;
   const int q0 = p.q_start[b], nq = p.q_start[b + 1] - q0;
   // shape checks, uniform over the CTA and taken before any barrier or TMEM use: the grid
   // must cover every query row, and the last row's keys must lie inside the sequence
-  if (threadIdx.x == 0 && h == 0 && tile == static_cast<int>(gridDim.z) - 1 &&
-      (nq > static_cast<int>(gridDim.z) * AT_ROWS || nq < 0 || p.pos0[b] < 0 ||
+  if (threadIdx.x == 0 && h == 0 && pair == static_cast<int>(gridDim.z) - 1 &&
+      (nq > static_cast<int>(gridDim.z) * 2 * AT_ROWS || nq < 0 || p.pos0[b] < 0 ||
        p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]))
     atomicOr(p.status, kDevBadShape);
   if (nq <= 0 || p.pos0[b] < 0 || p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]) return;
-  if (tile * AT_ROWS >= nq) return;  // empty unit
-  const int rows_valid = min(AT_ROWS, nq - tile * AT_ROWS);
-  const int pos_first = p.pos0[b] + tile * AT_ROWS;            // position of the tile's row 0
-  const int n_chunks = (pos_first + rows_valid - 1) / AT_KEYS + 1;  // chunks the last row sees
+  const int tileA = 2 * pair;
+  if (tileA * AT_ROWS >= nq) return;  // empty unit
+  // per tile (A, B): valid rows, position of row 0, chunks its last row sees
+  const int rows_a = min(AT_ROWS, nq - tileA * AT_ROWS);
+  const int rows_b = max(0, min(AT_ROWS, nq - (tileA + 1) * AT_ROWS));
+  const int pos_a = p.pos0[b] + tileA * AT_ROWS;
+  const int chunks_a = (pos_a + rows_a - 1) / AT_KEYS + 1;
+  const int chunks_b = rows_b > 0 ? (pos_a + AT_ROWS + rows_b - 1) / AT_KEYS + 1 : 0;
+  const int n_all = max(chunks_a, chunks_b);
   const int g = h / (p.Hq / p.Hkv);
   const int kbase = p.k_start[b];
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + AT_TILE_BYTES;          // 2 stages
-  uint8_t* sV = smem + 3 * AT_TILE_BYTES;      // 2 stages
-  uint8_t* sP = smem + 5 * AT_TILE_BYTES;
+  uint8_t* sQ = smem;                       // 2 tiles
+  uint8_t* sK = smem + 2 * AT_TILE_BYTES;   // 2 stages
+  uint8_t* sV = smem + 4 * AT_TILE_BYTES;   // 2 stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * AT_TILE_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* o_done = bars + 8;
-  uint64_t* drain = bars + 9;
+  uint64_t* kv_full = bars + 1;   // [2 stages]
+  uint64_t* kv_empty = bars + 3;  // [2 stages]
+  uint64_t* s_full = bars + 5;    // [2 tiles]
+  uint64_t* p_full = bars + 7;    // [2 tiles]
+  uint64_t* mma_done = bars + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -121,15 +152,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], AT_ROWS);
     }
-    mbar_init(p_full, AT_ROWS);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == AT_WARP_MMA) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -137,31 +167,29 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S buffer s at columns [128 s, 128 s + 128), O at [256, 384)
-  const uint32_t tO = tmem + 256;
+  // S_t at columns [128 t, 128 t + 128) (P_t over its first 64), O_t at [256 + 128 t, ...)
 
-  if (warp == 0) {
+  if (warp == AT_WARP_PRODUCER) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      bool ok = true;
       int issued = 0;
-      mbar_arrive_expect_tx(q_full, AT_TILE_BYTES);
-      for (int kb = 0; kb < 2; ++kb)
-        tma_load_2d(sQ + kb * (AT_TILE_BYTES / 2), &tmQ, q_full, h * AT_D + kb * 64, q0 + tile * AT_ROWS);
-      for (int c = 0; c < n_chunks && ok; ++c) {
+      const int n_q_tiles = chunks_b > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, n_q_tiles * AT_TILE_BYTES);
+      for (int t = 0; t < n_q_tiles; ++t)
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_2d(sQ + t * AT_TILE_BYTES + kb * (AT_TILE_BYTES / 2), &tmQ, q_full, h * AT_D + kb * 64,
+                      q0 + (tileA + t) * AT_ROWS);
+      for (int c = 0; c < n_all; ++c) {
         const int s = c & 1;
-        if (c >= 2 && !mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, p.timeout_ns, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+        if (c >= 2 && !mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, p.timeout_ns, abort_flag, p.status)) break;
         const int krow = kbase + c * AT_KEYS;
         mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE_BYTES);
         uint8_t* k_dst = sK + s * AT_TILE_BYTES;
         uint8_t* v_dst = sV + s * AT_TILE_BYTES;
-        // K: two 64-dim boxes of 128 keys (K-major B of QK^T)
+        // K: two 64-dim boxes of 128 keys (K-major B of Q K^T)
         for (int kb = 0; kb < 2; ++kb)
           tma_load_2d(k_dst + kb * (AT_TILE_BYTES / 2), &tmK, &kv_full[s], g * AT_D + kb * 64, krow);
-        // V: per 64-key block, two 64-dim boxes (MN-major B of PV)
+        // V: per 64-key block, two 64-dim boxes (MN-major B of P V)
         for (int kb = 0; kb < 2; ++kb)
           for (int half = 0; half < 2; ++half)
             tma_load_2d(v_dst + kb * (AT_TILE_BYTES / 2) + half * (AT_TILE_BYTES / 4), &tmV, &kv_full[s],
@@ -182,60 +210,72 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         atomicOr(p.status, kDevTimeout);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == AT_WARP_MMA) {
     // --------------------------------------------------------------------- MMA
     const bool leader = (lane == 0);
-    // every lane polls; the outcome is made warp-uniform before any .sync.aligned op
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.timeout_ns, abort_flag, p.status));
-    const uint32_t q_lo = smem_u32(sQ) >> 4, p_lo = smem_u32(sP) >> 4;
-    const uint64_t kdesc0 = sdesc_sw128(0, 16, 1024);   // K-major operand template
-    const uint64_t vdesc0 = sdesc_sw128(0, 8192, 1024); // MN-major operand template
-    auto issue_s = [&](int c) -> bool {
-      const int s = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (c >> 1) & 1, p.timeout_ns, abort_flag, p.status)))
-        return false;
-      tc_fence_after();
+    const uint64_t kdesc0 = sdesc_sw128(0, 16, 1024);    // K-major operand template
+    const uint64_t vdesc0 = sdesc_sw128(0, 8192, 1024);  // MN-major operand template
+    // S_t(c) = Q_t K_c^T into S_t's columns; K from stage c & 1 (already waited for)
+    auto issue_s = [&](int t, int c) {
       if (leader) {
-        const uint32_t k_lo = smem_u32(sK + s * AT_TILE_BYTES) >> 4;
+        const uint32_t q_lo = smem_u32(sQ + t * AT_TILE_BYTES) >> 4;
+        const uint32_t k_lo = smem_u32(sK + (c & 1) * AT_TILE_BYTES) >> 4;
+#pragma unroll
         for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) {
             const uint64_t ad = kdesc0 + q_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 2;
             const uint64_t bd = kdesc0 + k_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 2;
-            umma_bf16((tmem + s * 128), ad, bd, kIdescS, (kb | k16) != 0 ? 1u : 0u);
+            umma_bf16(tmem + t * 128, ad, bd, kIdescS, (kb | k16) != 0 ? 1u : 0u);
           }
-        umma_commit(&s_full[s]);
+        umma_commit(&s_full[t]);
       }
       __syncwarp();
-      return true;
     };
-    if (ok) ok = issue_s(0);
-    for (int c = 0; c < n_chunks && ok; ++c) {
-      if (c + 1 < n_chunks && !issue_s(c + 1)) {
-        ok = false;
-        break;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(p_full, c & 1, p.timeout_ns, abort_flag, p.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    // O_t += P_t(c) V_c; P_t from the first 64 columns of S_t, V from stage c & 1
+    auto issue_pv = [&](int t, int c) {
       if (leader) {
         const uint32_t v_lo = smem_u32(sV + (c & 1) * AT_TILE_BYTES) >> 4;
+#pragma unroll
         for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t ad = kdesc0 + p_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 2;
             const uint64_t bd = vdesc0 + v_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 128;
-            umma_bf16(tO, ad, bd, kIdescPV, (c | kb | k16) != 0 ? 1u : 0u);
+            umma_bf16_tmem_a(tmem + 256 + t * 128, tmem + t * 128 + (kb * 4 + k16) * 8, bd, kIdescPV,
+                             (c | kb | k16) != 0 ? 1u : 0u);
           }
-        umma_commit(&kv_empty[c & 1]);
-        umma_commit(o_done);
       }
       __syncwarp();
+    };
+    bool ok = warp_wait(q_full, 0, p, abort_flag) && warp_wait(&kv_full[0], 0, p, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      if (chunks_b > 0) issue_s(1, 0);
     }
-    if (leader) umma_commit(drain);
+    for (int c = 0; c < n_all && ok; ++c) {
+      for (int t = 0; t < 2 && ok; ++t) {
+        const int nct = t ? chunks_b : chunks_a;
+        if (c >= nct) continue;
+        ok = warp_wait(&p_full[t], c & 1, p, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(t, c);
+        if (c + 1 < nct) {
+          ok = warp_wait(&kv_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t, c + 1);
+        }
+      }
+      if (leader) umma_commit(&kv_empty[c & 1]);  // every MMA reading stage c & 1 is issued
+      __syncwarp();
+    }
+    if (leader) umma_commit(mma_done);
     __syncwarp();
+    // drain: the CTA exits only after its MMAs completed
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(smem_u32(drain), 0)) {
+    while (!mbar_try_wait(smem_u32(mma_done), 0)) {
       if (globaltimer_ns() - t0 > p.timeout_ns) {
         *abort_flag = 1;
         atomicOr(p.status, kDevTimeout);
@@ -248,24 +288,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // running maximum), P_j = 2^(t_j - m), and lse = m ln 2 + ln l at the end.  The running
     // maximum m moves only when a chunk's maximum exceeds it by more than kLazy (2^kLazy
     // bounds P and the sums stay far from overflow); then O and l are rescaled by 2^(m_old - m).
+    const int t = warp >> 2;       // 0: tile A, 1: tile B
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int pos = pos_first + r;  // this row's position (rows past rows_valid compute unused values)
-    const int warp_pos_min = pos_first + quarter * 32;
+    const uint32_t tS = tmem + t * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + t * 128 + lane_off;
+    const int nc = t ? chunks_b : chunks_a;
+    const int rows_valid = t ? rows_b : rows_a;
+    const int pos = pos_a + t * AT_ROWS + r;  // this row's position (rows past rows_valid compute unused values)
+    const int warp_pos_min = pos_a + t * AT_ROWS + quarter * 32;
     const float c2 = p.scale_log2e;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int s = c & 1;
-      // each lane polls; the outcome is made warp-uniform, so the warp reaches every
-      // tcgen05.ld / st (.sync.aligned) converged
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (c >> 1) & 1, p.timeout_ns, abort_flag, p.status));
+    bool ok = nc > 0;
+    for (int c = 0; c < nc && ok; ++c) {
+      // S_t(c) complete; for c > 0 so is P V of chunk c - 1 (issued before it)
+      ok = warp_wait(&s_full[t], c & 1, p, abort_flag);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[AT_KEYS];
 #pragma unroll
-      for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld32p((tmem + s * 128) + lane_off + q * 32, v + q * 32);
+      for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld32p(tS + q * 32, v + q * 32);
       tmem_ld_wait_only();
 #pragma unroll
       for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld_tie(v + q * 32);
@@ -288,68 +331,50 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const float alpha = (m == -INFINITY) ? 1.f : exp2f(__fsub_rn(m, m_new));  // 1 when m stays
       m = m_new;
       const float neg_m = -m;
-      // P_j = 2^(t_j - m); the chunk sum in four interleaved partial sums, combined in a fixed
-      // order
+      // P_j = 2^(t_j - m), packed to bf16 pairs in place; the chunk sum in four interleaved
+      // partial sums, combined in a fixed order
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < AT_KEYS; ++j) {
-        const float e = exp2f(__fmaf_rn(u2f(v[j]), c2, neg_m));
-        v[j] = f2u(e);
-        ls[j & 3] = __fadd_rn(ls[j & 3], e);
+      for (int j = 0; j < AT_KEYS; j += 2) {
+        const float e0 = exp2f(__fmaf_rn(u2f(v[j]), c2, neg_m));
+        const float e1 = exp2f(__fmaf_rn(u2f(v[j + 1]), c2, neg_m));
+        ls[j & 3] = __fadd_rn(ls[j & 3], e0);
+        ls[(j + 1) & 3] = __fadd_rn(ls[(j + 1) & 3], e1);
+        v[j >> 1] = pack_bf16x2(e0, e1);
       }
       l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])));
-      if (c > 0) {
-        // PV of chunk c-1 done: O is current and the P buffer is free
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (c - 1) & 1, p.timeout_ns, abort_flag, p.status));
-        if (!ok) break;
-        tc_fence_after();
-        // the rescale is taken by the whole warp when any of its rows needs it (x * 1 = x
-        // exactly, so a row whose maximum did not move keeps its bits)
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // the rescale is taken by the whole warp when any of its rows needs it (x * 1 = x
+      // exactly, so a row whose maximum did not move keeps its bits)
+      if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int q = 0; q < AT_D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32p(tO + lane_off + q * 32, o);
-            tmem_ld_wait_only();
-            tmem_ld_tie(o);
+        for (int q = 0; q < AT_D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32p(tO + q * 32, o);
+          tmem_ld_wait_only();
+          tmem_ld_tie(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(__fmul_rn(u2f(o[i]), alpha));
-            tmem_st32p(tO + lane_off + q * 32, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) o[i] = f2u(__fmul_rn(u2f(o[i]), alpha));
+          tmem_st32p(tO + q * 32, o);
         }
       }
-      // P as bf16 into the K-major, 128-byte-swizzled A tile of the PV MMA: key block kb
-      // (64 keys) at kb * 16 KB, row r at (r / 8) * 1024 + (r % 8) * 128, 16-byte chunk q
-      // of the row at slot q ^ (r % 8)
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int j = kb * 64 + q * 8;
-          uint4 w;
-          w.x = pack_bf16x2(u2f(v[j + 0]), u2f(v[j + 1]));
-          w.y = pack_bf16x2(u2f(v[j + 2]), u2f(v[j + 3]));
-          w.z = pack_bf16x2(u2f(v[j + 4]), u2f(v[j + 5]));
-          w.w = pack_bf16x2(u2f(v[j + 6]), u2f(v[j + 7]));
-          *reinterpret_cast<uint4*>(sP + kb * (AT_TILE_BYTES / 2) + (r >> 3) * 1024 + (r & 7) * 128 +
-                                    ((q ^ (r & 7)) << 4)) = w;
-        }
-      fence_proxy_async_smem();
+      // P over the first 64 columns of S_t: column k holds keys 2k (low half) and 2k + 1
+      tmem_st32p(tS, v);
+      tmem_st32p(tS + 32, v + 32);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[t]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_chunks - 1) & 1, p.timeout_ns, abort_flag, p.status));
+    if (ok) ok = warp_wait(mma_done, 0, p, abort_flag);
     if (ok) {
       tc_fence_after();
       uint32_t o[AT_D];
 #pragma unroll
-      for (int q = 0; q < AT_D / 32; ++q) tmem_ld32p(tO + lane_off + q * 32, o + q * 32);
+      for (int q = 0; q < AT_D / 32; ++q) tmem_ld32p(tO + q * 32, o + q * 32);
       tmem_ld_wait_only();
 #pragma unroll
       for (int q = 0; q < AT_D / 32; ++q) tmem_ld_tie(o + q * 32);
       if (r < rows_valid) {
-        const int64_t row = q0 + tile * AT_ROWS + r;
+        const int64_t row = q0 + (tileA + t) * AT_ROWS + r;
         __nv_bfloat16* dst = p.out + (row * p.Hq + h) * AT_D;
         const float inv_l = __frcp_rn(l);
 #pragma unroll
@@ -369,7 +394,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == AT_WARP_MMA) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
@@ -392,7 +417,8 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   if (B == 0 || Tq == 0 || max_q_rows == 0) return ISO_OK;
   if (!Q || !K || !V || !q_start || !k_start || !pos0 || !out) return ISO_ERR_INVALID_ARG;
   if (Tk == 0) return ISO_ERR_SHAPE;  // a query row sees at least one key
-  if (B > 65535 || (max_q_rows + AT_ROWS - 1) / AT_ROWS > 65535) return ISO_ERR_UNSUPPORTED;
+  const int pairs = ((max_q_rows + AT_ROWS - 1) / AT_ROWS + 1) / 2;
+  if (B > 65535 || pairs > 65535) return ISO_ERR_UNSUPPORTED;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
   if (mis & 15u) return ISO_ERR_ALIGNMENT;
@@ -425,7 +451,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
       return ISO_ERR_CUDA;
     attr_dev = dev;
   }
-  const dim3 grid(Hq, B, (max_q_rows + AT_ROWS - 1) / AT_ROWS);
+  const dim3 grid(Hq, B, pairs);
   iso_attention_kernel<<<grid, AT_THREADS, AT_SMEM, static_cast<cudaStream_t>(stream)>>>(tQ, tK, tV, p);
   return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
