@@ -410,6 +410,8 @@ def secondary(c, dev, stream, peaks, rank):
     out["diagnostics"] = dict(workload=f"64 packed sequences, {n} tokens", ms=tt, tokens_per_s=n / (tt * 1e-3),
                               hbm_gbs=byt / (tt * 1e-3) / 1e9, bound="fp64")
 
+    out["attention"] = attention_measure(c, dev, stream, peaks, flush)
+
     # MoE expert layer: T=8192, H=2048, E=128, F=768, k=8
     T, H, E, F, k = 8192, 2048, 128, 768, 8
     xm, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=3, device=dev)
@@ -421,6 +423,56 @@ def secondary(c, dev, stream, peaks, rank):
     out["moe"] = dict(workload="T=8192, H=2048, E=128, F=768, k=8", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
                       roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3))
     return out
+
+
+ATT_HQ, ATT_HKV, ATT_D = 32, 8, 128  # 8B-class decoder: 32 query heads over 8 KV heads
+
+
+def attention_workload(dev, small=False):
+    """Causal attention over the packed rollout batch (64 sequences, lengths ~ U[1, 8192],
+    seed 4), or 8 sequences of 2048 tokens (small)."""
+    from parallelism_invariant_logprob_gb300 import inputs
+    lens = [2048] * 8 if small else inputs.sequence_lengths(64, 8192, seed=4)
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(lens, [0] * len(lens), ATT_HQ, ATT_HKV, ATT_D, seed=6, device=dev)
+    return lens, Q, K, V, qs, ks, p0
+
+
+def attention_flops(lens):
+    # 2 d flops for q.k and 2 d for p.v per (row, visible key) pair, per query head
+    return 4.0 * ATT_D * ATT_HQ * sum(L * (L + 1) // 2 for L in lens)
+
+
+def attention_measure(c, dev, stream, peaks, flush):
+    """Packed prefill over the rollout batch, and one decode step per sequence (its last
+    position, reading its whole KV cache)."""
+    import math
+    import torch
+    from parallelism_invariant_logprob_gb300 import binding as B
+    lens, Q, K, V, qs, ks, p0 = attention_workload(dev)
+    scale = 1.0 / math.sqrt(ATT_D)
+    o = torch.empty_like(Q)
+    lse = torch.empty(Q.shape[0], ATT_HQ, dtype=torch.float32, device=dev)
+    mq = max(lens)
+    tt = time_call(lambda: B.attention(c, Q, K, V, qs, ks, p0, scale, max_q_rows=mq, out=o, lse=lse, stream=stream),
+                   3, 1, stream)
+    fl = attention_flops(lens)
+    r = dict(workload=f"causal prefill, 64 packed sequences ({sum(lens)} tokens), {ATT_HQ} query / {ATT_HKV} KV "
+                      f"heads, d {ATT_D}", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
+             roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3), bound="tensor")
+    # decode: the last row of each sequence
+    last = (qs[1:] - 1).long()
+    Qd = Q[last].contiguous()
+    dq = torch.arange(len(lens) + 1, dtype=torch.int32, device=dev)
+    dpos = torch.tensor([L - 1 for L in lens], dtype=torch.int32, device=dev)
+    od = torch.empty_like(Qd)
+    ld = torch.empty(len(lens), ATT_HQ, dtype=torch.float32, device=dev)
+    td = time_call(lambda: B.attention(c, Qd, K, V, dq, ks, dpos, scale, max_q_rows=1, out=od, lse=ld, stream=stream),
+                   5, 2, stream, flush)
+    byt = 2.0 * 2 * ATT_HKV * ATT_D * sum(lens) + 2.0 * 2 * len(lens) * ATT_HQ * ATT_D
+    r["decode"] = dict(workload=f"one row per sequence at its last position, {len(lens)} sequences", ms=td,
+                       hbm_gbs=byt / (td * 1e-3) / 1e9, roofline_frac=byt / (peaks["hbm"] * 1e9) / (td * 1e-3),
+                       bound="hbm")
+    return r
 
 
 def profile_target(target: str, calls: int):
@@ -446,6 +498,12 @@ def profile_target(target: str, calls: int):
         om = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
         wsm = torch.empty(B.grouped_gemm_moe_workspace(c, T, E, k, H, F), dtype=torch.uint8, device=dev)
         fn = lambda: B.grouped_gemm_moe(c, x, ids, w, W1, W2, out=om, ws=wsm)
+    elif target in ("attention", "attention_small"):
+        import math
+        lens, Q, K, V, qs, ks, p0 = attention_workload(dev, small=target == "attention_small")
+        o = torch.empty_like(Q)
+        lse = torch.empty(Q.shape[0], ATT_HQ, dtype=torch.float32, device=dev)
+        fn = lambda: B.attention(c, Q, K, V, qs, ks, p0, 1.0 / math.sqrt(ATT_D), max_q_rows=max(lens), out=o, lse=lse)
     elif target == "rmsnorm":
         x, g = inputs.rmsnorm_inputs(262144, 4096, seed=4, device=dev)
         y = torch.empty_like(x)
@@ -466,7 +524,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm"],
+    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small"],
                     help="run one workload --steps times without timing (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_target:

@@ -13,8 +13,8 @@
 // chain of 8 tcgen05 MMAs (K = 16 each, ascending dims) and S_j = -inf for keys past p:
 //   t    = rn(max_j S_j * c2)                           (max is exact in any order)
 //   m'   = max(m, t) if chunk 0 or t > m + 8, else m    (lazy: P stays below 2^8)
-//   P_j  = exp2f(fma(S_j, c2, -m'));  l_c = (sum of four interleaved partial sums, fixed order)
-//   a    = exp2f(m - m') (1 when m' = m);  l = rn(rn(l * a) + l_c);  O = rn(O * a) when a != 1
+//   P_j  = ex2(fma(S_j, c2, -m'));  l_c = (sum of four interleaved partial sums, fixed order)
+//   a    = ex2(m - m') (1 when m' = m);  l = rn(rn(l * a) + l_c);  O = rn(O * a) when a != 1
 //   O   += bf16(P) V   (8 tcgen05 MMAs, K = 16 keys each, ascending keys)
 // and at the end out = bf16_rn(O * rcp(l)), lse = rn(rn(m ln 2) + logf(l)).  Every step
 // depends only on the row, its position and the chunk grid, never on the other rows of its
@@ -23,11 +23,11 @@
 // O + 0 = O.
 //
 // Structure: one CTA per (query head, sequence, pair of 128-row query tiles A and B), the
-// pairs with the most chunks first; 320 threads.
+// pairs with the most chunks first; 384 threads (3 warpgroups, registers rebalanced at entry).
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread per query row
 //              (TMEM lane); each also rescales its O rows and writes the output
 //   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 2-stage ring
-//   warp 9     MMA issuer (lane 0) and TMEM owner.  Per chunk j it issues, in this order,
+//   warp 9     MMA issuer (lane 0) and TMEM owner (warps 10, 11 only fill the warpgroup).  Per chunk j it issues, in this order,
 //              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the softmax of one tile runs, the
 //              tensor core works for the other.
 // TMEM (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B.  The softmax writes P as
@@ -49,7 +49,13 @@ namespace {
 constexpr int AT_ROWS = 128;    // query rows per tile (the MMA's M)
 constexpr int AT_KEYS = 128;    // keys per chunk (N of QK^T, K of PV)
 constexpr int AT_D = 128;       // head dimension
-constexpr int AT_THREADS = 320;
+constexpr int AT_THREADS = 384;  // 3 warpgroups
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64,512), the two softmax
+// warpgroups take 216 and the producer / MMA warpgroup keeps 72: 2 x 128 x 216 + 128 x 72 =
+// 64,512, exactly the launch's total, so the increase always finds its registers.
+constexpr int AT_REGS_SOFTMAX = 216;
+constexpr int AT_REGS_CONTROL = 72;
+static_assert(2 * 128 * AT_REGS_SOFTMAX + 128 * AT_REGS_CONTROL <= AT_THREADS * 168, "register split");
 constexpr int AT_TILE_BYTES = AT_ROWS * AT_D * 2;  // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int AT_SMEM = 1024 /*align*/ + 6 * AT_TILE_BYTES + 256 /*barriers*/;
 constexpr int AT_WARP_PRODUCER = 8;
@@ -78,6 +84,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
   return *reinterpret_cast<const uint32_t*>(&t);
 }
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (one MUFU op; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// three-input maximum (PTX max.f32 with three sources)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 constexpr float kLazy = 8.0f;  // base-2 headroom before the running maximum moves
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -91,6 +109,15 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
 // Bounded wait on the phase of `bar` with the given parity, polled by every lane of the
@@ -169,6 +196,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   // S_t at columns [128 t, 128 t + 128) (P_t over its first 64), O_t at [256 + 128 t, ...)
 
+  if (warp >= 8) {
+    // the control warpgroup (producer, MMA, two idle warps) hands registers to the softmax
+    regs_dec<AT_REGS_CONTROL>();
+  }
   if (warp == AT_WARP_PRODUCER) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
@@ -282,8 +313,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         break;
       }
     }
-  } else {
+  } else if (warp < 8) {
     // ----------------------------------------------------- softmax / correction
+    regs_inc<AT_REGS_SOFTMAX>();
     // Scores are handled in the base-2 domain: t_j = S_j * scale * log2(e) (one FMA with the
     // running maximum), P_j = 2^(t_j - m), and lse = m ln 2 + ln l at the end.  The running
     // maximum m moves only when a chunk's maximum exceeds it by more than kLazy (2^kLazy
@@ -321,14 +353,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // chunk maximum of the raw scores (max is exact, so the tree's shape cannot matter)
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = u2f(v[i]);
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(u2f(v[i]), u2f(v[i + 8]));
 #pragma unroll
-      for (int j = 8; j < AT_KEYS; ++j) mx[j & 7] = fmaxf(mx[j & 7], u2f(v[j]));
-      const float mc = __fmul_rn(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
-                                 c2);
+      for (int j = 16; j < AT_KEYS; j += 16)  // keys j .. j + 15, j + 15 <= 127
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], u2f(v[j + i]), u2f(v[j + 8 + i]));
+      const float mc = __fmul_rn(max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])), c2);
       const float m_new = (m == -INFINITY || mc > m + kLazy) ? fmaxf(m, mc) : m;
-      const float alpha = (m == -INFINITY) ? 1.f : exp2f(__fsub_rn(m, m_new));  // 1 when m stays
+      const float alpha = (m == -INFINITY) ? 1.f : ex2(__fsub_rn(m, m_new));  // 1 when m stays
       m = m_new;
       const float neg_m = -m;
       // P_j = 2^(t_j - m), packed to bf16 pairs in place; the chunk sum in four interleaved
@@ -336,8 +368,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < AT_KEYS; j += 2) {
-        const float e0 = exp2f(__fmaf_rn(u2f(v[j]), c2, neg_m));
-        const float e1 = exp2f(__fmaf_rn(u2f(v[j + 1]), c2, neg_m));
+        const float e0 = ex2(__fmaf_rn(u2f(v[j]), c2, neg_m));
+        const float e1 = ex2(__fmaf_rn(u2f(v[j + 1]), c2, neg_m));
         ls[j & 3] = __fadd_rn(ls[j & 3], e0);
         ls[(j + 1) & 3] = __fadd_rn(ls[(j + 1) & 3], e1);
         v[j >> 1] = pack_bf16x2(e0, e1);

@@ -89,7 +89,7 @@ def random_partition(E: int, P: int, seed: int) -> torch.Tensor:
     return torch.randint(0, P, (E,), generator=g, dtype=torch.int32)
 
 
-def attention_inputs(q_lens, pos0, Hq: int, Hkv: int, d: int, seed: int, extra_keys=None):
+def attention_inputs(q_lens, pos0, Hq: int, Hkv: int, d: int, seed: int, extra_keys=None, device="cpu"):
     """Packed causal-attention inputs (CPU tensors).  Sequence b has q_lens[b] query rows at
     positions pos0[b], pos0[b]+1, ... and pos0[b] + q_lens[b] + extra_keys[b] keys (the KV
     cache of earlier positions, then the keys of its query rows, then keys no row sees).
@@ -102,7 +102,8 @@ def attention_inputs(q_lens, pos0, Hq: int, Hkv: int, d: int, seed: int, extra_k
     q_start[1:] = torch.tensor([int(v) for v in q_lens], dtype=torch.int64).cumsum(0).to(torch.int32)
     k_start[1:] = torch.tensor(k_lens, dtype=torch.int64).cumsum(0).to(torch.int32)
     Tq, Tk = int(q_start[-1]), int(k_start[-1])
-    Q = normal_bf16((Tq, Hq, d), 1.0, seed * 3 + 0)
-    K = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 1)
-    V = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 2)
-    return Q, K, V, q_start, k_start, torch.tensor([int(v) for v in pos0], dtype=torch.int32)
+    Q = normal_bf16((Tq, Hq, d), 1.0, seed * 3 + 0, device)
+    K = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 1, device)
+    V = normal_bf16((Tk, Hkv, d), 1.0, seed * 3 + 2, device)
+    p0 = torch.tensor([int(v) for v in pos0], dtype=torch.int32)
+    return Q, K, V, q_start.to(device), k_start.to(device), p0.to(device)
