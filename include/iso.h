@@ -138,6 +138,11 @@ iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, co
  * iso_tree_combine: applies the top log2(R) levels of the same tree to
  * S[r] = S + r * rank_stride (fp32 [M x lds] each) and writes C = bf16_rn(root).
  * The pair reproduces iso_gemm bit for bit for every R.
+ * Sequence parallelism (the reduce-scatter form): a rank that keeps output rows
+ * [r0, r1) passes S + r0 * lds and M = r1 - r0 (the rows of every rank's
+ * partial, exchanged without arithmetic); its rows equal rows [r0, r1) of
+ * iso_gemm bit for bit [IsoExec blog, "Parallelism-invariant kernels": SP
+ * reuses the non-SP reduction tree, each rank keeping its output slice].
  * [IsoExec blog, "Parallelism-invariant kernels": NCCL only transports the
  *  partial results]; [RL-Kernel blog, §6 table row 06: the same fixed
  *  balanced tree for TP1/2/4/8] */
@@ -314,6 +319,30 @@ iso_status iso_mismatch_diagnostics(const iso_contract* c, const float* logp_tra
                                     float* delta, float* tis_weight, double* seq_k1, double* seq_k3,
                                     uint8_t* accept_k1, uint8_t* accept_k3, float* seq_max_abs_delta,
                                     double* seq_sum_abs_delta, int32_t* seq_mismatches, iso_stream stream);
+
+/* ------------------------------------------- RMSNorm fused into the A prologue
+ * [IsoExec blog, "Parallelism-invariant kernels"; RL-Kernel blog, §6 table row
+ *  02 (RMSNorm) and §7: fusions must keep the separate stages' numerics]
+ * iso_rmsnorm_gemm: C = iso_gemm(iso_rmsnorm(x, gamma, eps), B) bit for bit,
+ * without writing the normalised activations: a row pass computes
+ * r_t = 1 / sqrt(mean x^2 + eps) with iso_rmsnorm's reduction into ws, then the
+ * GEMM's producer warps build each A tile in shared memory as
+ * bf16_rn((x * r_t) * gamma_i), iso_rmsnorm's per-element arithmetic.  x: [M x K]
+ * bf16 (ld = K), gamma: [K] bf16, B / C as for iso_gemm; ws (DEVICE, 16-byte
+ * aligned): iso_rmsnorm_gemm_workspace(c, M) bytes (ISO_ERR_WORKSPACE).
+ * iso_rmsnorm_selected_logprob: iso_selected_logprob(iso_rmsnorm(x, gamma, eps),
+ * W, ids) bit for bit; ws: iso_rmsnorm_selected_logprob_workspace(c, T, V) bytes
+ * (the per-row factors first, then the logprob workspace; with less room than
+ * that but at least the factors plus iso_selected_logprob_min_workspace the
+ * chunk-unit schedule runs, same bits).  Other errors as the unfused calls. */
+size_t iso_rmsnorm_gemm_workspace(const iso_contract* c, int M);
+iso_status iso_rmsnorm_gemm(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps,
+                            const iso_bf16* B, int64_t ldb, iso_bf16* C, int64_t ldc, int M, int N, int K, void* ws,
+                            size_t ws_bytes, iso_stream stream);
+size_t iso_rmsnorm_selected_logprob_workspace(const iso_contract* c, int T, int V);
+iso_status iso_rmsnorm_selected_logprob(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps,
+                                        const iso_bf16* W, const int32_t* ids, float* out, int T, int H, int V,
+                                        void* ws, size_t ws_bytes, iso_stream stream);
 
 /* ------------------------------------------------------------ attention
  * [RL-Kernel blog, §4 "Focus: The Shared Dependency of Attention and Linear

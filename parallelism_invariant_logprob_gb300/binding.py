@@ -77,6 +77,11 @@ _SIGNATURES = {
                                     _vp, _sz, _vp]),
     "iso_selftest_bounded_wait": (_int, [_u64, _vp]),
     "iso_selected_logprob_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
+    "iso_rmsnorm_gemm_workspace": (_sz, [_vp, _int]),
+    "iso_rmsnorm_gemm": (_int, [_vp, _vp, _vp, ctypes.c_float, _vp, _i64, _vp, _i64, _int, _int, _int, _vp, _sz, _vp]),
+    "iso_rmsnorm_selected_logprob_workspace": (_sz, [_vp, _int, _int]),
+    "iso_rmsnorm_selected_logprob": (_int, [_vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _int, _int, _int, _vp, _sz,
+                                            _vp]),
     "iso_attention": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _int,
                              ctypes.c_float, _vp, _vp, _vp]),
 }
@@ -316,6 +321,38 @@ def attention(c: Contract, Q, K, V, q_start, k_start, pos0, scale: float, max_q_
                              _stream(stream))
     c.lib.check(st, "iso_attention")
     return out, lse
+
+
+def rmsnorm_gemm(c: Contract, x, gamma, eps: float, B, out=None, ws=None, stream=None):
+    """iso_gemm(iso_rmsnorm(x, gamma, eps), B) with the normalisation fused into the A prologue."""
+    import torch
+    M, K = x.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(int(c.lib.iso_rmsnorm_gemm_workspace(c.handle, M)), 16), dtype=torch.uint8,
+                         device=x.device)
+    st = c.lib.iso_rmsnorm_gemm(c.handle, _ptr(x), _ptr(gamma), float(eps), _ptr(B), B.stride(0), _ptr(out),
+                                out.stride(0), M, N, K, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    c.lib.check(st, "iso_rmsnorm_gemm")
+    return out
+
+
+def rmsnorm_selected_logprob(c: Contract, x, gamma, eps: float, W, ids, out=None, ws=None, stream=None):
+    """iso_selected_logprob(iso_rmsnorm(x, gamma, eps), W, ids) with the normalisation fused."""
+    import torch
+    T, H = x.shape
+    V = W.shape[1]
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(int(c.lib.iso_rmsnorm_selected_logprob_workspace(c.handle, T, V)), 16),
+                         dtype=torch.uint8, device=x.device)
+    st = c.lib.iso_rmsnorm_selected_logprob(c.handle, _ptr(x), _ptr(gamma), float(eps), _ptr(W), _ptr(ids), _ptr(out),
+                                            T, H, V, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    c.lib.check(st, "iso_rmsnorm_selected_logprob")
+    return out
 
 
 def selected_logprob_min_workspace(c: Contract, T: int, V: int) -> int:

@@ -225,6 +225,31 @@ iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t 
   return launch_gemm(epi, tA, tB, p, p.num_units, s);
 }
 
+// The leaf-tree GEMM of y = rmsnorm(x) and B with the normalisation in the A prologue: the
+// producer warps build each A stage from x, rinv and gamma (one CTA per unit, 128-row A boxes).
+iso_status run_gemm_rmsnorm(const void* x, const float* rinv, const void* gamma, const void* B, int64_t ldb, void* C,
+                            int64_t ldc, int M, int N, int K, int L, cudaStream_t s) {
+  GemmParams p = base_params(M, N, K, L);
+  set_a_rows(p, 128);
+  p.a_transform = 1;
+  p.a_src = x;
+  p.lda_src = K;
+  p.a_rinv = rinv;
+  p.a_gamma = gamma;
+  CUtensorMap tA, tB;
+  iso_status st = make_tmap_bf16(&tA, x, M, K, K, BK, 128);  // unused by the kernel in this mode
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
+  if (st != ISO_OK) return st;
+  p.unit_mode = UNIT_GEMM;
+  p.num_units = p.m_blocks * p.n_blocks;
+  p.group_m = raster_group(p, K);
+  p.out = C;
+  p.ldo = ldc;
+  trace("rmsnorm_gemm", M, N, K, L);
+  return launch_gemm(EPI_BF16, tA, tB, p, p.num_units, s);
+}
+
 }  // namespace
 
 }  // namespace iso
@@ -379,15 +404,25 @@ size_t iso_selected_logprob_min_workspace(const iso_contract* c, int T, int V) {
 // chunk_stats and z at each row's id (when the id falls in these columns) into zsel.  With
 // tile_stats (room for [tiles x T]) every 128-column tile is its own unit and a fold kernel forms
 // the chunk entries; otherwise one CTA folds a whole chunk.  Same fold, same bits.
+// With rinv (the fused RMSNorm prologue) h holds the raw states x and the A stages are built
+// as bf16((x * rinv[t]) * gamma[i]) by the producer warps (one CTA per unit, 128-row boxes).
 static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, int64_t ldw,
                                     const int32_t* ids, int T, int H, int Vl, int sel_base, float2* chunk_stats,
-                                    float* zsel, float2* tile_stats, cudaStream_t s) {
+                                    float* zsel, float2* tile_stats, cudaStream_t s, const float* rinv = nullptr,
+                                    const iso_bf16* gamma = nullptr) {
   const int L = iso_contract_leaf_count(c);
   GemmParams p = base_params(T, Vl, H, L);
-  if (p.m_blocks == 1)
+  if (rinv != nullptr) {
+    p.a_transform = 1;
+    p.a_src = h;
+    p.lda_src = H;
+    p.a_rinv = rinv;
+    p.a_gamma = gamma;
+  } else if (p.m_blocks == 1) {
     set_a_rows(p, a_rows_for(T));
-  else if (use_pair(T, H, L))
+  } else if (use_pair(T, H, L)) {
     set_pair(p, T);
+  }
   CUtensorMap tA, tB;
   iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
   if (st != ISO_OK) return st;
@@ -412,8 +447,11 @@ static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, co
              : ISO_ERR_CUDA;
 }
 
-iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
-                                float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream) {
+// iso_selected_logprob and its fused-RMSNorm form (gamma != NULL: h holds the raw states and
+// the workspace starts with the per-row factors).
+static iso_status selected_logprob_impl(const iso_contract* c, const iso_bf16* h, const iso_bf16* gamma, float eps,
+                                        const iso_bf16* W, const int32_t* ids, float* out, int T, int H, int V,
+                                        void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!c || T < 0 || H <= 0 || V <= 0) return ISO_ERR_INVALID_ARG;
   if (T == 0) return ISO_OK;
   if (!h || !W || !ids || !out || !ws) return ISO_ERR_INVALID_ARG;
@@ -422,22 +460,69 @@ iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const 
   if (V % 8 != 0 || lp_num_chunks(V) > 256) return ISO_ERR_SHAPE;
   if (H % 8 != 0) return ISO_ERR_ALIGNMENT;
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(out)) return ISO_ERR_ALIGNMENT;
-  if (ws_bytes < lp_chunk_ws_bytes(T, V)) return ISO_ERR_WORKSPACE;
+  if (gamma != nullptr) {
+    if (!aligned16(gamma)) return ISO_ERR_ALIGNMENT;
+    if (!(eps >= 0.0f)) return ISO_ERR_INVALID_ARG;
+  }
+  const size_t pre = gamma != nullptr ? al256(static_cast<size_t>(T) * sizeof(float)) : 0;
+  if (ws_bytes < pre + lp_chunk_ws_bytes(T, V)) return ISO_ERR_WORKSPACE;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
-  const bool tiles = ws_bytes >= lp_full_ws_bytes(T, V);
   char* wsb = static_cast<char*>(ws);
+  float* rinv = gamma != nullptr ? reinterpret_cast<float*>(wsb) : nullptr;
+  wsb += pre;
+  ws_bytes -= pre;
+  const bool tiles = ws_bytes >= lp_full_ws_bytes(T, V);
   float2* tile_stats = tiles ? reinterpret_cast<float2*>(wsb) : nullptr;
   char* rest = wsb + (tiles ? lp_tile_stats_bytes(T, V) : 0);
   float2* chunk_stats = reinterpret_cast<float2*>(rest);
   float* zsel = reinterpret_cast<float*>(rest + al256(static_cast<size_t>(T) * lp_num_chunks(V) * sizeof(float2)));
-  iso_status st = run_logprob_stats(c, h, W, V, ids, T, H, V, 0, chunk_stats, zsel, tile_stats, S(stream));
+  if (rinv != nullptr && launch_rms_rows(h, eps, rinv, T, H, H, s) != cudaSuccess) return ISO_ERR_CUDA;
+  iso_status st = run_logprob_stats(c, h, W, V, ids, T, H, V, 0, chunk_stats, zsel, tile_stats, s, rinv, gamma);
   if (st != ISO_OK) return st;
   ShardBounds one;
   one.n = 1;
   one.chunk0[0] = 0;
-  return launch_lse_combine(chunk_stats, zsel, ids, out, T, lp_num_chunks(V), V, one, S(stream)) == cudaSuccess
+  return launch_lse_combine(chunk_stats, zsel, ids, out, T, lp_num_chunks(V), V, one, s) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;
+}
+
+iso_status iso_selected_logprob(const iso_contract* c, const iso_bf16* h, const iso_bf16* W, const int32_t* ids,
+                                float* out, int T, int H, int V, void* ws, size_t ws_bytes, iso_stream stream) {
+  return selected_logprob_impl(c, h, nullptr, 0.f, W, ids, out, T, H, V, ws, ws_bytes, S(stream));
+}
+
+size_t iso_rmsnorm_selected_logprob_workspace(const iso_contract* c, int T, int V) {
+  if (!c || T < 0 || V <= 0) return 0;
+  return al256(static_cast<size_t>(T) * sizeof(float)) + lp_full_ws_bytes(T, V);
+}
+
+iso_status iso_rmsnorm_selected_logprob(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps,
+                                        const iso_bf16* W, const int32_t* ids, float* out, int T, int H, int V,
+                                        void* ws, size_t ws_bytes, iso_stream stream) {
+  if (!gamma && T > 0) return ISO_ERR_INVALID_ARG;
+  return selected_logprob_impl(c, x, gamma, eps, W, ids, out, T, H, V, ws, ws_bytes, S(stream));
+}
+
+size_t iso_rmsnorm_gemm_workspace(const iso_contract* c, int M) {
+  if (!c || M < 0) return 0;
+  return al256(static_cast<size_t>(M) * sizeof(float));
+}
+
+iso_status iso_rmsnorm_gemm(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps,
+                            const iso_bf16* B, int64_t ldb, iso_bf16* C, int64_t ldc, int M, int N, int K, void* ws,
+                            size_t ws_bytes, iso_stream stream) {
+  if (!c) return ISO_ERR_INVALID_ARG;
+  const int L = iso_contract_leaf_count(c);
+  iso_status st = check_gemm_args(x, K, B, ldb, C, ldc, 8, M, N, K, L);
+  if (st != ISO_OK || M == 0) return st;
+  if (!gamma || !ws || !(eps >= 0.0f)) return ISO_ERR_INVALID_ARG;
+  if (!aligned16(gamma) || !aligned16(ws)) return ISO_ERR_ALIGNMENT;
+  if (ws_bytes < static_cast<size_t>(M) * sizeof(float)) return ISO_ERR_WORKSPACE;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  float* rinv = static_cast<float*>(ws);
+  if (launch_rms_rows(x, eps, rinv, M, K, K, S(stream)) != cudaSuccess) return ISO_ERR_CUDA;
+  return run_gemm_rmsnorm(x, rinv, gamma, B, ldb, C, ldc, M, N, K, L, S(stream));
 }
 
 size_t iso_selected_logprob_partial_workspace(const iso_contract* c, int T, int V_r) {

@@ -541,6 +541,43 @@ cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, 
   return cudaGetLastError();
 }
 
+// Per-row 1 / sqrt(mean x^2 + eps) of the fused RMSNorm prologue: one warp per row with the
+// reduction of rmsnorm_kernel (lane l accumulates x^2 over the 8-element vectors l, l + 32, ...
+// in ascending order, low then high half of each pair; xor shuffle tree 16, 8, 4, 2, 1; IEEE
+// division and square root), so the factor has the bits iso_rmsnorm uses.
+__global__ void __launch_bounds__(256) rms_rows_kernel(const __nv_bfloat16* __restrict__ x, float eps,
+                                                       float* __restrict__ rinv, int T, int H, int64_t ldx) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = H / 8;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); row < T;
+       row += static_cast<int64_t>(gridDim.x) * 8) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * ldx);
+    float acc = 0.f;
+    for (int vi = lane; vi < nvec; vi += 32) {
+      const uint4 v = xr[vi];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = bf16_lo(w[q]), b = bf16_hi(w[q]);
+        acc = __fadd_rn(acc, __fmul_rn(a, a));
+        acc = __fadd_rn(acc, __fmul_rn(b, b));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    const float ms = __fdiv_rn(acc, static_cast<float>(H));
+    if (lane == 0) rinv[row] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  }
+}
+
+cudaError_t launch_rms_rows(const void* x, float eps, float* rinv, int T, int H, int64_t ldx, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  int blocks = (T + 7) / 8;
+  if (blocks > sm_count() * 16) blocks = sm_count() * 16;
+  rms_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), eps, rinv, T, H, ldx);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, const float* zsel, const int32_t* ids,
                                 float* out, int T, int C, int V, int ntiles, int chunk_tiles, cudaStream_t s) {
   if (tile_stats != nullptr) {

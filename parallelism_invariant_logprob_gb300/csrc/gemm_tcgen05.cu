@@ -209,6 +209,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+// Fused RMSNorm prologue: the 128-row x 64-column A tile (rows [row0, row0 + 128), columns
+// [k0, k0 + 64)) of y = bf16_rn((x * rinv[row]) * gamma[k]), the per-element arithmetic of
+// iso_rmsnorm, built by the 32 lanes of a producer warp directly in the 128-byte-swizzled
+// K-major layout the MMA reads (the layout TMA writes): row r, 16-byte chunk q of its 128-byte
+// line at (r / 8) * 1024 + (r % 8) * 128 + ((q ^ (r % 8)) * 16).  A warp instruction covers
+// 4 rows x 8 chunks (four whole 128-byte lines of x).  Rows past M and columns past K are 0.
+__device__ __forceinline__ void rmsnorm_a_tile(uint8_t* sA, const GemmParams& p, int row0, int k0, int lane) {
+  const int q = lane & 7;  // this lane's 16-byte chunk of every row it writes
+  const int k = k0 + q * 8;
+  const bool k_in = k < p.K;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.a_src);
+  uint4 g = make_uint4(0u, 0u, 0u, 0u);
+  if (k_in) g = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.a_gamma) + k));
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  constexpr int kIters = BM * (BK / 8) / 32;  // 32 chunks per lane
+  uint4 v[kIters];
+  float rr[kIters];
+#pragma unroll
+  for (int i = 0; i < kIters; ++i) {
+    const int row = row0 + i * 4 + (lane >> 3);
+    const bool in = k_in && row < p.M;
+    v[i] = in ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(row) * p.lda_src + k))
+              : make_uint4(0u, 0u, 0u, 0u);
+    rr[i] = row < p.M ? __ldg(p.a_rinv + row) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kIters; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __fmul_rn(__fmul_rn(__uint_as_float(w[j] << 16), rr[i]), __uint_as_float(gw[j] << 16));
+      const float hi = __fmul_rn(__fmul_rn(__uint_as_float(w[j] & 0xffff0000u), rr[i]), __uint_as_float(gw[j] & 0xffff0000u));
+      o[j] = pack_bf16x2(lo, hi);
+    }
+    *reinterpret_cast<uint4*>(sA + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // One epilogue warp writes the bf16 tile rows of its 32 TMEM lanes.  Lane r holds
 // row r as CH chunks of 8 bf16 (16 bytes) and its destination row `orow` (-1: row not
 // stored).  The rows go through the warp's staging area (32 rows x CH*16 bytes, chunk c of
@@ -283,6 +324,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int BSTAGE = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // B bytes per stage in this CTA
   constexpr int CL = PAIR ? 2 : 1;
+  // the fused RMSNorm prologue exists for single-CTA dense and logprob launches only
+  constexpr bool kFusedA = !PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB);
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
@@ -310,7 +353,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < nstages; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], p.a_transform ? 2 : 1);  // + the producer warp's A-tile arrival
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < NUM_TMEM_BUFS; ++b) {
@@ -381,12 +424,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(2 * (p.a_bytes + BSTAGE)));
                   tma_load_2d_pair(sA, &tmA, fb, U.a_col0 + kx, U.a_row0);
                   tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);
+                } else if (kFusedA && p.a_transform) {
+                  // B by TMA; A is built below by the whole warp (the barrier's second arrival)
+                  mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(BSTAGE));
+                  tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+                  tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
                 } else {
                   mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + BSTAGE));
                   tma_load_2d(sA, &tmA, &full_bar[stage], U.a_col0 + kx, U.a_row0);
                   tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
                   tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
                 }
+              }
+              if (kFusedA && p.a_transform) {
+                rmsnorm_a_tile(sA, p, U.a_row0, U.a_col0 + kx, lane);
+                fence_proxy_async_smem();  // the generic-proxy stores become visible to the MMA
+                __syncwarp();
+                if (leader) mbar_arrive(&full_bar[stage]);
               }
               __syncwarp();
               ++issued;

@@ -38,5 +38,7 @@ cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int3
 cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,
                                cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(uint64_t timeout_ns, cudaStream_t s);
+// rinv[t] = 1 / sqrt(mean_i x[t, i]^2 + eps) with iso_rmsnorm's reduction (x: [T x H], leading dim ldx).
+cudaError_t launch_rms_rows(const void* x, float eps, float* rinv, int T, int H, int64_t ldx, cudaStream_t s);
 
 }  // namespace iso

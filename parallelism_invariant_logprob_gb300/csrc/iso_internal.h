@@ -87,6 +87,14 @@ struct GemmParams {
   // full problem (K here is the group's length) and writes its fp32 subtree root to
   // out + r * out_group_stride
   int64_t out_group_stride;
+  // fused RMSNorm prologue (a_transform = 1): the A operand is y = bf16((x * rinv[row]) * gamma[k])
+  // [RL-Kernel blog, §6 table row 02; the same arithmetic as iso_rmsnorm], built in shared memory
+  // by the producer warps from x [M x K] (leading dimension lda_src) instead of loaded by TMA
+  int a_transform;
+  const void* a_src;      // x, bf16
+  int64_t lda_src;
+  const float* a_rinv;    // [M] per-row 1 / sqrt(mean x^2 + eps)
+  const void* a_gamma;    // [K] bf16
   // error reporting
   unsigned int* status;
   uint64_t timeout_ns;

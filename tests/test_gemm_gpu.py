@@ -154,6 +154,28 @@ def test_config2_shapes_sampled_rows_and_ranks(c8, K, N):
         assert same_bits(B.tree_combine(c8, S), full), R
 
 
+@pytest.mark.parametrize("R", [2, 4, 8])
+def test_sp_reduce_scatter_slices_equal_rows_of_iso_gemm(c8, R):
+    """Sequence parallelism [IsoExec blog, "Parallelism-invariant kernels": the row-parallel
+    reduction becomes a reduce-scatter over the same tree; each rank keeps its output slice].
+    Rank q's slice is the top tree levels over rows [q M / R, (q+1) M / R) of every rank's
+    partial (iso_tree_combine on the row-offset view; the exchange only moves rows): the bits
+    equal those rows of iso_gemm, for ragged slices (M = 1000 is not a multiple of 8)."""
+    M, K, N = 1000, 4096, 520
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=77)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c8, Ad, Bd)
+    Kl = K // R
+    S = torch.stack([B.gemm_leaf_partial(c8, r, R, Ad[:, r * Kl:(r + 1) * Kl].contiguous(), Bd[r * Kl:(r + 1) * Kl])
+                     for r in range(R)])
+    for q in range(R):
+        r0, r1 = (q * M) // R, ((q + 1) * M) // R
+        # in place on the rank-strided view, and after the exchange packs the slices contiguously
+        Cq = B.tree_combine(c8, S[:, r0:r1])
+        assert same_bits(Cq, full[r0:r1]), (R, q)
+        assert same_bits(B.tree_combine(c8, S[:, r0:r1].contiguous()), full[r0:r1]), (R, q)
+
+
 @pytest.mark.parametrize("M", [129, 200, 257, 384])
 def test_cta_pair_units_ragged_exact(c8, M):
     """Leaves of 1024 k (K = 8192, 8 leaves) run on CTA pairs: a unit is 256 rows, the
