@@ -348,7 +348,20 @@ def secondary(c, dev, stream, peaks, rank):
         byt = 2.0 * LP_H * LP_V + 2.0 * T * LP_H + 8.0 * T
         out["logprob"][f"T{T}"] = dict(ms=tt, tokens_per_s=T / (tt * 1e-3), hbm_gbs=byt / (tt * 1e-3) / 1e9,
                                        roofline_frac=byt / (peaks["hbm"] * 1e9) / (tt * 1e-3), bound="hbm")
-    del h, W, ids, ws
+    # RMSNorm + logprob at T = 4096: the separate stages against the fused A prologue (same bits)
+    xr, gr = inputs.rmsnorm_inputs(LP_T, LP_H, seed=12, device=dev)
+    hn = torch.empty_like(xr)
+    ws_f = torch.empty(B.rmsnorm_selected_logprob_workspace(c, LP_T, LP_V), dtype=torch.uint8, device=dev)
+
+    def separate():
+        B.rmsnorm(c, xr, gr, 1e-6, out=hn, stream=stream)
+        B.selected_logprob(c, hn, W, ids, out=lp_out, ws=ws, stream=stream)
+    t_sep = time_call(separate, 5, 2, stream, flush)
+    t_fused = time_call(lambda: B.rmsnorm_selected_logprob(c, xr, gr, 1e-6, W, ids, out=lp_out, ws=ws_f, stream=stream),
+                        5, 2, stream, flush)
+    out["logprob"]["rmsnorm_fused"] = dict(workload="iso_rmsnorm + iso_selected_logprob vs iso_rmsnorm_selected_logprob, "
+                                                    "T=4096, H=4096, V=151936", ms_separate=t_sep, ms_fused=t_fused)
+    del h, W, ids, ws, xr, hn, ws_f
 
     # GEMM at small M (weight-streaming, HBM-bound) and the cuBLAS non-invariant reference
     gm = {}

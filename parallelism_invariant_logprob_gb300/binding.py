@@ -323,6 +323,14 @@ def attention(c: Contract, Q, K, V, q_start, k_start, pos0, scale: float, max_q_
     return out, lse
 
 
+def rmsnorm_gemm_workspace(c: Contract, M: int) -> int:
+    return int(c.lib.iso_rmsnorm_gemm_workspace(c.handle, M))
+
+
+def rmsnorm_selected_logprob_workspace(c: Contract, T: int, V: int) -> int:
+    return int(c.lib.iso_rmsnorm_selected_logprob_workspace(c.handle, T, V))
+
+
 def rmsnorm_gemm(c: Contract, x, gamma, eps: float, B, out=None, ws=None, stream=None):
     """iso_gemm(iso_rmsnorm(x, gamma, eps), B) with the normalisation fused into the A prologue."""
     import torch

@@ -188,6 +188,16 @@ __device__ __forceinline__ bool wait_ticket(volatile uint32_t* ticket, uint32_t 
 // Per-buffer phase bits (one bit per TMEM buffer) kept in a register.
 __device__ __forceinline__ uint32_t bit_of(uint32_t bits, int b) { return (bits >> b) & 1u; }
 
+// Register reallocation between warpgroups (every warp of a warpgroup executes the same one).
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // One lane of a converged warp (elected once per warp and reused, so the thread that issues a
 // warp's MMAs is also the one whose tcgen05.commit tracks them).
 __device__ __forceinline__ bool elect_one() {
@@ -209,41 +219,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// Fused RMSNorm prologue: the 128-row x 64-column A tile (rows [row0, row0 + 128), columns
-// [k0, k0 + 64)) of y = bf16_rn((x * rinv[row]) * gamma[k]), the per-element arithmetic of
-// iso_rmsnorm, built by the 32 lanes of a producer warp directly in the 128-byte-swizzled
-// K-major layout the MMA reads (the layout TMA writes): row r, 16-byte chunk q of its 128-byte
-// line at (r / 8) * 1024 + (r % 8) * 128 + ((q ^ (r % 8)) * 16).  A warp instruction covers
-// 4 rows x 8 chunks (four whole 128-byte lines of x).  Rows past M and columns past K are 0.
-__device__ __forceinline__ void rmsnorm_a_tile(uint8_t* sA, const GemmParams& p, int row0, int k0, int lane) {
-  const int q = lane & 7;  // this lane's 16-byte chunk of every row it writes
+// Fused RMSNorm prologue, in place, rows [32 w, 32 w + 32) of the tile (transform warp w): the
+// stage's A tile holds raw x (rows [row0, row0 + 128),
+// columns [k0, k0 + 64)) as TMA wrote it (128-byte-swizzled K-major: row r, 16-byte chunk q of
+// its 128-byte line at (r / 8) * 1024 + (r % 8) * 128 + ((q ^ (r % 8)) * 16); rows past M and
+// columns past K zero-filled); the 32 lanes overwrite each element with
+// y = bf16_rn((x * rinv[row]) * gamma[k]), the per-element arithmetic of iso_rmsnorm.  Lane l
+// handles chunk q = l % 8 of rows 32 w + 4 i + l / 8, so its gamma chunk is the same for every row.
+__device__ __forceinline__ void rmsnorm_a_rows_inplace(uint8_t* sA, const GemmParams& p, int row0, int k0, int w,
+                                                       int lane) {
+  const int q = lane & 7;
   const int k = k0 + q * 8;
-  const bool k_in = k < p.K;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.a_src);
   uint4 g = make_uint4(0u, 0u, 0u, 0u);
-  if (k_in) g = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.a_gamma) + k));
+  if (k < p.K) g = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.a_gamma) + k));
   const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-  constexpr int kIters = BM * (BK / 8) / 32;  // 32 chunks per lane
-  uint4 v[kIters];
+  constexpr int kIters = (BM / 4) * (BK / 8) / 32;  // 8 chunks per lane: rows [32 w, 32 w + 32)
   float rr[kIters];
 #pragma unroll
   for (int i = 0; i < kIters; ++i) {
-    const int row = row0 + i * 4 + (lane >> 3);
-    const bool in = k_in && row < p.M;
-    v[i] = in ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(row) * p.lda_src + k))
-              : make_uint4(0u, 0u, 0u, 0u);
+    const int row = row0 + w * 32 + i * 4 + (lane >> 3);
     rr[i] = row < p.M ? __ldg(p.a_rinv + row) : 0.f;
+  }
+  // every load first, then every store: no load waits behind a store it might alias
+  uint4 v[kIters];
+#pragma unroll
+  for (int i = 0; i < kIters; ++i) {
+    const int r = w * 32 + i * 4 + (lane >> 3);
+    v[i] = *reinterpret_cast<const uint4*>(sA + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4));
   }
 #pragma unroll
   for (int i = 0; i < kIters; ++i) {
-    const int r = i * 4 + (lane >> 3);
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    const int r = w * 32 + i * 4 + (lane >> 3);
+    const uint32_t xw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float lo = __fmul_rn(__fmul_rn(__uint_as_float(w[j] << 16), rr[i]), __uint_as_float(gw[j] << 16));
-      const float hi = __fmul_rn(__fmul_rn(__uint_as_float(w[j] & 0xffff0000u), rr[i]), __uint_as_float(gw[j] & 0xffff0000u));
-      o[j] = pack_bf16x2(lo, hi);
+      const float lo = __fmul_rn(__fmul_rn(__uint_as_float(xw[j] << 16), rr[i]), __uint_as_float(gw[j] << 16));
+      const float hi = __fmul_rn(__fmul_rn(__uint_as_float(xw[j] & 0xffff0000u), rr[i]), __uint_as_float(gw[j] & 0xffff0000u));
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);  // round to nearest even, .x = lo
+      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
     }
     *reinterpret_cast<uint4*>(sA + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4)) =
         make_uint4(o[0], o[1], o[2], o[3]);
@@ -316,16 +330,18 @@ __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int 
 // for SwiGLU), with the loads of both counted on rank 0's stage barrier; the MMA commits
 // arrive on the barriers of both CTAs.  Per CTA a stage is then 24 KB instead of 32 KB, so
 // more stages fit and each SM moves three quarters of the bytes per MMA.
-template <int EPI, bool PAIR>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// FUSED: the fused RMSNorm prologue (single CTA, EPI_BF16 / EPI_LOGPROB): 12 warps, warps 8-11
+// normalise the A stages in place; registers rebalanced by setmaxnreg (epilogue 256, the rest
+// 120: 128 x 256 + 256 x 120 = 63,488 <= the launch's 384 x 168).
+template <int EPI, bool PAIR, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
     iso_leaf_tree_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int BSTAGE = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // B bytes per stage in this CTA
   constexpr int CL = PAIR ? 2 : 1;
-  // the fused RMSNorm prologue exists for single-CTA dense and logprob launches only
-  constexpr bool kFusedA = !PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB);
+  static_assert(!FUSED || (!PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB)), "fused prologue: single CTA, bf16/logprob");
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
@@ -336,7 +352,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* leaf_full = empty_bar + MAX_STAGES;
   uint64_t* buf_free = leaf_full + NUM_TMEM_BUFS;
   uint64_t* drain_bar = buf_free + NUM_TMEM_BUFS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 2);
+  uint64_t* raw_bar = drain_bar + 2;  // [MAX_STAGES] fused RMSNorm prologue: raw x landed in the A stage
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_bar + MAX_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // Sequence number of the next leaf allowed to start.  The two MMA threads start their leaves
   // strictly in leaf order; without that, a thread could wait on a TMEM buffer's buf_free
@@ -353,7 +370,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < nstages; ++s) {
-      mbar_init(&full_bar[s], p.a_transform ? 2 : 1);  // + the producer warp's A-tile arrival
+      mbar_init(&full_bar[s], FUSED ? 1 + 4 : 1);  // + one arrival per transform warp
+      if (FUSED) mbar_init(&raw_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < NUM_TMEM_BUFS; ++b) {
@@ -389,6 +407,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   // k in [l*leaf_len + 64 j, min(+64, (l+1)*leaf_len)).
   const int per = (p.L >= 2) ? 2 : 1;
 
+  if (warp < 4 || warp >= 8) {
+  if constexpr (FUSED) regs_dec<GEMM_REGS_CONTROL_FUSED>();
   if (warp == 0 || warp == 3) {
     const int me = warp == 0 ? 0 : 1;  // stage parity loaded by this warp
     if (me < per) {
@@ -424,8 +444,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(2 * (p.a_bytes + BSTAGE)));
                   tma_load_2d_pair(sA, &tmA, fb, U.a_col0 + kx, U.a_row0);
                   tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);
-                } else if (kFusedA && p.a_transform) {
-                  // B by TMA; A is built below by the whole warp (the barrier's second arrival)
+                } else if (FUSED) {
+                  // raw x on raw_bar (the transform warps normalise it in place, then add their
+                  // four arrivals to full_bar); B on full_bar
+                  mbar_arrive_expect_tx(&raw_bar[stage], static_cast<uint32_t>(p.a_bytes));
+                  tma_load_2d(sA, &tmA, &raw_bar[stage], U.a_col0 + kx, U.a_row0);
                   mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(BSTAGE));
                   tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
                   tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
@@ -435,12 +458,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
                   tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
                 }
-              }
-              if (kFusedA && p.a_transform) {
-                rmsnorm_a_tile(sA, p, U.a_row0, U.a_col0 + kx, lane);
-                fence_proxy_async_smem();  // the generic-proxy stores become visible to the MMA
-                __syncwarp();
-                if (leader) mbar_arrive(&full_bar[stage]);
               }
               __syncwarp();
               ++issued;
@@ -460,7 +477,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t total = issued;
         for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(nstages / per); ++back) {
           const uint32_t gidx = static_cast<uint32_t>(me) + static_cast<uint32_t>(per) * (total - back);
-          const uint32_t a = smem_u32(&full_bar[gidx % static_cast<uint32_t>(nstages)]);
+          // FUSED: the raw x loads land on raw_bar (full_bar may also wait for transform
+          // arrivals that an abort cut short; its B bytes land in the same window)
+          const uint32_t a = smem_u32(FUSED ? &raw_bar[gidx % static_cast<uint32_t>(nstages)]
+                                            : &full_bar[gidx % static_cast<uint32_t>(nstages)]);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(a, (gidx / static_cast<uint32_t>(nstages)) & 1u)) {
             if (globaltimer_ns() - t0 > p.timeout_ns) break;
@@ -589,8 +609,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
     }
+  } else if constexpr (FUSED) {
+    // ---------------------------------------------------- fused prologue (warps 8-11)
+    // Walk the stages in the producers' global order (for each K-block, the leaf of each
+    // parity); for each: wait for its raw x, normalise rows [32 w, 32 w + 32) in place,
+    // publish with one arrival on the stage's full barrier.
+    const int w = warp - 8;
+    uint32_t cidx = 0;  // global stage counter
+    bool ok = true;
+    for (int u = unit0; u < nunits && ok; u += unit_step) {
+      Unit U;
+      decode_unit(p, u, U, CL, rank);
+      for (int t = 0; t < U.n_tiles && ok; ++t) {
+        for (int g = 0; g < p.L / per && ok; ++g) {
+          for (int j = 0; j < p.kb_per_leaf && ok; ++j) {
+            for (int me = 0; me < per; ++me, ++cidx) {
+              const int stage = static_cast<int>(cidx % static_cast<uint32_t>(nstages));
+              const uint32_t round = cidx / static_cast<uint32_t>(nstages);
+              ok = __all_sync(0xffffffffu, mbar_wait(&raw_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status));
+              if (!ok) break;
+              const int kx = (g * per + me) * p.leaf_len + j * BK;
+              rmsnorm_a_rows_inplace(smem + stage * p.a_bytes, p, U.a_row0, U.a_col0 + kx, w, lane);
+              fence_proxy_async_smem();  // the generic-proxy stores become visible to the MMA
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&full_bar[stage]);
+            }
+          }
+        }
+      }
+    }
+  }
   } else {
     // --------------------------------------------------------------- epilogue
+    if constexpr (FUSED) regs_inc<256>();
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -835,14 +886,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 namespace {
 
-template <int EPI, bool PAIR>
+template <int EPI, bool PAIR, bool FUSED = false>
 iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                       cudaStream_t s) {
+  constexpr int kThreads = FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS;
   static int attr_dev = -1;  // device whose function attributes are set
   static int slots = 0;      // CTAs (pairs: clusters) resident at once on that device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
-  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR>;
+  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED>;
   if (attr_dev != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
       return ISO_ERR_CUDA;
@@ -874,7 +926,7 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
   const int units = max_units < slots ? max_units : slots;
   if (units <= 0) return ISO_OK;
   if (!PAIR) {
-    kern<<<units, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+    kern<<<units, kThreads, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
@@ -898,6 +950,12 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                        cudaStream_t s) {
   const bool pair = p.pair != 0;
+  if (p.a_transform) {
+    if (pair) return ISO_ERR_INVALID_ARG;
+    if (epi == EPI_BF16) return launch_one<EPI_BF16, false, true>(tmA, tmB, p, max_units, s);
+    if (epi == EPI_LOGPROB) return launch_one<EPI_LOGPROB, false, true>(tmA, tmB, p, max_units, s);
+    return ISO_ERR_INVALID_ARG;
+  }
   switch (epi) {
     case EPI_BF16:
       return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s)

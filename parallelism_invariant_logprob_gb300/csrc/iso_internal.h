@@ -37,6 +37,8 @@ constexpr int GEMM_BARRIER_BYTES = 512;
 constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
+constexpr int GEMM_THREADS_FUSED = 384;      // + warps 8..11: the fused RMSNorm prologue
+constexpr int GEMM_REGS_CONTROL_FUSED = 120;  // setmaxnreg of warps 0-3 and 8-11 (epilogue: 256)
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
 constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
 constexpr int MOE_MAX_EXPERTS = 256;
