@@ -8,14 +8,15 @@
 // query head h (KV head h / (Hq / Hkv)), over the keys k_start[b] .. k_start[b] + p,
 //   out = softmax(scale * q . k) V  (bf16),  lse = m + log l  (fp32).
 //
-// The merge is the online softmax over fixed 128-key chunks in ascending order, one thread per
-// row, in the base-2 domain (c2 = rn(scale * log2 e)).  For chunk c, with S = q . k from a
-// chain of 8 tcgen05 MMAs (K = 16 each, ascending dims) and S_j = -inf for keys past p:
+// The merge is the online softmax over fixed 80-key chunks (keys [80 c, 80 c + 80) of the
+// sequence) in ascending order, one thread per row, in the base-2 domain
+// (c2 = rn(scale * log2 e)).  For chunk c, with S = q . k from a chain of 8 tcgen05 MMAs
+// (K = 16 each, ascending dims) and S_j = -inf for keys past p:
 //   t    = rn(max_j S_j * c2)                           (max is exact in any order)
 //   m'   = max(m, t) if chunk 0 or t > m + 8, else m    (lazy: P stays below 2^8)
 //   P_j  = ex2(fma(S_j, c2, -m'));  l_c = (sum of four interleaved partial sums, fixed order)
 //   a    = ex2(m - m') (1 when m' = m);  l = rn(rn(l * a) + l_c);  O = rn(O * a) when a != 1
-//   O   += bf16(P) V   (8 tcgen05 MMAs, K = 16 keys each, ascending keys)
+//   O   += bf16(P) V   (5 tcgen05 MMAs, K = 16 keys each, ascending keys)
 // and at the end out = bf16_rn(O * rcp(l)), lse = rn(rn(m ln 2) + logf(l)).  Every step
 // depends only on the row, its position and the chunk grid, never on the other rows of its
 // tile or the launch, so a decode call (one row) reproduces the row of a prefill call exactly.
@@ -23,19 +24,19 @@
 // O + 0 = O.
 //
 // Structure: one CTA per (query head, sequence, pair of 128-row query tiles A and B), the
-// pairs with the most chunks first; 384 threads (3 warpgroups, registers rebalanced at entry).
+// pairs with the most chunks first; 512 threads (4 warpgroups, registers rebalanced at entry).
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread per query row
 //              (TMEM lane); each also rescales its O rows and writes the output
-//   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 2-stage ring
-//   warp 9     MMA issuer (lane 0) and TMEM owner (warps 10, 11 only fill the warpgroup).  Per chunk j it issues, in this order,
-//              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the softmax of one tile runs, the
-//              tensor core works for the other.
-// TMEM (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B.  The softmax writes P as
-// packed bf16 pairs over the first 64 columns of its own S buffer, and the P V MMA reads A
-// from there.  tcgen05 MMAs execute in issue order, so PV_t(j) has read P_t(j) before
-// S_t(j+1) overwrites it, and the commit after S_t(j+1) also covers PV_t(j): the softmax
-// may rescale O_t as soon as it sees S_t(j+1).  Shared memory: Q 2 x 32 KB, K and V 2 stages
-// x 32 KB each.  Every wait is bounded (abort flag, device status word).
+//   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 4-stage ring
+//   warps 9-12 MMA issuers, one lane each: Q K^T of tile A, P V of tile A, Q K^T of tile B,
+//              P V of tile B.  One thread cannot issue tcgen05 MMAs as fast as the tensor core
+//              retires them (one per ~190 cycles at any N on this part), so every chain that
+//              can run on its own has its own thread.  Warp 9 owns TMEM; warps 13-15 idle.
+// TMEM (512 columns): per tile t at 256 t: S (80 fp32 columns), P (40 columns of bf16 pairs, its
+// own region) and O (128 columns at 256 t + 128).  P apart from S lets Q K^T of chunk c + 1 run
+// as soon as the softmax has read S of chunk c, overlapping the softmax and P V of chunk c.
+// Shared memory: Q 2 x 32 KB, K and V 4 stages x 20 KB each.  Every wait is bounded (abort
+// flag, device status word).
 #include <cuda_bf16.h>
 #include <stdio.h>
 
@@ -47,19 +48,27 @@ namespace iso {
 namespace {
 
 constexpr int AT_ROWS = 128;    // query rows per tile (the MMA's M)
-constexpr int AT_KEYS = 128;    // keys per chunk (N of QK^T, K of PV)
+constexpr int AT_KEYS = 80;     // keys per chunk (N of Q K^T, K of P V)
 constexpr int AT_D = 128;       // head dimension
-constexpr int AT_THREADS = 384;  // 3 warpgroups
-// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64,512), the two softmax
-// warpgroups take 216 and the producer / MMA warpgroup keeps 72: 2 x 128 x 216 + 128 x 72 =
-// 64,512, exactly the launch's total, so the increase always finds its registers.
-constexpr int AT_REGS_SOFTMAX = 216;
-constexpr int AT_REGS_CONTROL = 72;
-static_assert(2 * 128 * AT_REGS_SOFTMAX + 128 * AT_REGS_CONTROL <= AT_THREADS * 168, "register split");
-constexpr int AT_TILE_BYTES = AT_ROWS * AT_D * 2;  // 32 KB: one 128 x 128 bf16 operand tile
-constexpr int AT_SMEM = 1024 /*align*/ + 6 * AT_TILE_BYTES + 256 /*barriers*/;
+constexpr int AT_STAGES = 4;    // K / V ring depth (chunk c in stage c % 4)
+constexpr int AT_THREADS = 512;  // 4 warpgroups
+// Register split (setmaxnreg): launched at 128 per thread (512 x 128 = 65,536); the two softmax
+// warpgroups take 200 and the two control warpgroups keep 56: 2 x 128 x 200 + 2 x 128 x 56 =
+// 65,536, exactly the launch's total, so the increase always finds its registers.
+constexpr int AT_REGS_SOFTMAX = 200;
+constexpr int AT_REGS_CONTROL = 56;
+static_assert(2 * 128 * AT_REGS_SOFTMAX + 2 * 128 * AT_REGS_CONTROL <= AT_THREADS * 128, "register split");
+constexpr int AT_Q_BYTES = AT_ROWS * AT_D * 2;      // 32 KB: one Q tile (two {64, 128} boxes)
+constexpr int AT_KV_HALF = AT_KEYS * 64 * 2;        // 10 KB: one {64 dims, 80 keys} box
+constexpr int AT_KV_BYTES = 2 * AT_KV_HALF;         // 20 KB: K or V of one chunk
+constexpr int AT_SMEM = 1024 /*align*/ + 2 * AT_Q_BYTES + 2 * AT_STAGES * AT_KV_BYTES + 256 /*barriers*/;
+static_assert(AT_KV_HALF % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
 constexpr int AT_WARP_PRODUCER = 8;
-constexpr int AT_WARP_MMA = 9;
+constexpr int AT_WARP_MMA0 = 9;  // 9: S_A, 10: PV_A, 11: S_B, 12: PV_B
+// TMEM columns of tile t (add 256 t)
+constexpr int AT_COL_S = 0;
+constexpr int AT_COL_P = 80;
+constexpr int AT_COL_O = 128;
 
 struct AttnParams {
   const int32_t* q_start;  // [B+1]
@@ -73,7 +82,7 @@ struct AttnParams {
   uint64_t timeout_ns;
 };
 
-// S = Q K^T: A (Q) and B (K) both K-major in shared memory.  O += P V: A (P) K-major in
+// S = Q K^T: A (Q) and B (K) both K-major in shared memory, N = 80.  O += P V: A (P) K-major in
 // tensor memory, B (V) MN-major in shared memory.
 constexpr uint32_t kIdescS = idesc_bf16_f32(AT_ROWS, AT_KEYS, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(AT_ROWS, AT_D, false, true);
@@ -110,6 +119,29 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// 32 lanes x 16 consecutive fp32 columns
+__device__ __forceinline__ void tmem_ld16p(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_tie16(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+// 32 lanes x 8 consecutive 32-bit columns
+__device__ __forceinline__ void tmem_st8p(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 
 template <int R>
 __device__ __forceinline__ void regs_inc() {
@@ -126,6 +158,21 @@ __device__ __forceinline__ void regs_dec() {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const AttnParams& p,
                                           volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status));
+}
+
+// Bounded wait for every MMA this thread issued (its commit on `bar`), then the warp goes on.
+__device__ __forceinline__ void drain_own_mmas(uint64_t* bar, bool leader, const AttnParams& p,
+                                               volatile int* abort_flag) {
+  if (leader) umma_commit(bar);
+  __syncwarp();
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(smem_u32(bar), 0)) {
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(p.status, kDevTimeout);
+      break;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -155,17 +202,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                       // 2 tiles
-  uint8_t* sK = smem + 2 * AT_TILE_BYTES;   // 2 stages
-  uint8_t* sV = smem + 4 * AT_TILE_BYTES;   // 2 stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * AT_TILE_BYTES);
+  uint8_t* sQ = smem;                               // 2 tiles
+  uint8_t* sK = smem + 2 * AT_Q_BYTES;              // AT_STAGES stages
+  uint8_t* sV = sK + AT_STAGES * AT_KV_BYTES;       // AT_STAGES stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + AT_STAGES * AT_KV_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2 stages]
-  uint64_t* kv_empty = bars + 3;  // [2 stages]
-  uint64_t* s_full = bars + 5;    // [2 tiles]
-  uint64_t* p_full = bars + 7;    // [2 tiles]
-  uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* kv_full = bars + 1;                     // [AT_STAGES]
+  uint64_t* kv_empty = kv_full + AT_STAGES;         // [tile][AT_STAGES]: P V of the tile read the stage
+  uint64_t* s_full = kv_empty + 2 * AT_STAGES;      // [tile]
+  uint64_t* s_free = s_full + 2;                    // [tile]: the softmax has read S
+  uint64_t* p_full = s_free + 2;                    // [tile]
+  uint64_t* pv_done = p_full + 2;                   // [tile]
+  uint64_t* issuer_done = pv_done + 2;              // [4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(issuer_done + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -175,18 +224,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < AT_STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], AT_ROWS);
+      mbar_init(&kv_empty[AT_STAGES + s], 1);
     }
-    mbar_init(mma_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], AT_ROWS);
+      mbar_init(&p_full[t], AT_ROWS);
+      mbar_init(&pv_done[t], 1);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&issuer_done[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == AT_WARP_MMA) {
+  if (warp == AT_WARP_MMA0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -194,126 +248,111 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S_t at columns [128 t, 128 t + 128) (P_t over its first 64), O_t at [256 + 128 t, ...)
 
   if (warp >= 8) {
-    // the control warpgroup (producer, MMA, two idle warps) hands registers to the softmax
+    // ---------------------------------------------------------- control warpgroups
     regs_dec<AT_REGS_CONTROL>();
-  }
-  if (warp == AT_WARP_PRODUCER) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int issued = 0;
-      const int n_q_tiles = chunks_b > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, n_q_tiles * AT_TILE_BYTES);
-      for (int t = 0; t < n_q_tiles; ++t)
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_2d(sQ + t * AT_TILE_BYTES + kb * (AT_TILE_BYTES / 2), &tmQ, q_full, h * AT_D + kb * 64,
-                      q0 + (tileA + t) * AT_ROWS);
-      for (int c = 0; c < n_all; ++c) {
-        const int s = c & 1;
-        if (c >= 2 && !mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, p.timeout_ns, abort_flag, p.status)) break;
-        const int krow = kbase + c * AT_KEYS;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE_BYTES);
-        uint8_t* k_dst = sK + s * AT_TILE_BYTES;
-        uint8_t* v_dst = sV + s * AT_TILE_BYTES;
-        // K: two 64-dim boxes of 128 keys (K-major B of Q K^T)
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_2d(k_dst + kb * (AT_TILE_BYTES / 2), &tmK, &kv_full[s], g * AT_D + kb * 64, krow);
-        // V: per 64-key block, two 64-dim boxes (MN-major B of P V)
-        for (int kb = 0; kb < 2; ++kb)
-          for (int half = 0; half < 2; ++half)
-            tma_load_2d(v_dst + kb * (AT_TILE_BYTES / 2) + half * (AT_TILE_BYTES / 4), &tmV, &kv_full[s],
-                        g * AT_D + half * 64, krow + kb * 64);
-        issued = c + 1;
-      }
-      // before the CTA may exit: every load this thread issued has landed (bounded; normally
-      // the MMA has consumed them all and these phases are long complete)
-      const uint64_t t0 = globaltimer_ns();
-      bool landed = false;
-      while (!landed && globaltimer_ns() - t0 <= p.timeout_ns) {
-        landed = mbar_try_wait(smem_u32(q_full), 0);
-        for (int c = (issued > 2 ? issued - 2 : 0); c < issued && landed; ++c)
-          landed = mbar_try_wait(smem_u32(&kv_full[c & 1]), (c >> 1) & 1);
-      }
-      if (!landed) {
-        *abort_flag = 1;
-        atomicOr(p.status, kDevTimeout);
-      }
-    }
-  } else if (warp == AT_WARP_MMA) {
-    // --------------------------------------------------------------------- MMA
-    const bool leader = (lane == 0);
-    const uint64_t kdesc0 = sdesc_sw128(0, 16, 1024);    // K-major operand template
-    const uint64_t vdesc0 = sdesc_sw128(0, 8192, 1024);  // MN-major operand template
-    // S_t(c) = Q_t K_c^T into S_t's columns; K from stage c & 1 (already waited for)
-    auto issue_s = [&](int t, int c) {
-      if (leader) {
-        const uint32_t q_lo = smem_u32(sQ + t * AT_TILE_BYTES) >> 4;
-        const uint32_t k_lo = smem_u32(sK + (c & 1) * AT_TILE_BYTES) >> 4;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t ad = kdesc0 + q_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 2;
-            const uint64_t bd = kdesc0 + k_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 2;
-            umma_bf16(tmem + t * 128, ad, bd, kIdescS, (kb | k16) != 0 ? 1u : 0u);
+    if (warp == AT_WARP_PRODUCER) {
+      if (lane == 0) {
+        int issued = 0;
+        const int n_q_tiles = chunks_b > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(q_full, n_q_tiles * AT_Q_BYTES);
+        for (int t = 0; t < n_q_tiles; ++t)
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(sQ + t * AT_Q_BYTES + kb * (AT_Q_BYTES / 2), &tmQ, q_full, h * AT_D + kb * 64,
+                        q0 + (tileA + t) * AT_ROWS);
+        for (int c = 0; c < n_all; ++c) {
+          const int s = c % AT_STAGES;
+          if (c >= AT_STAGES) {
+            // the stage held chunk c - 4: every tile that used it has finished its P V
+            const int old = c - AT_STAGES;
+            const uint32_t par = ((c / AT_STAGES) - 1) & 1;
+            bool ok = true;
+            if (old < chunks_a) ok = mbar_wait(&kv_empty[s], par, p.timeout_ns, abort_flag, p.status);
+            if (ok && old < chunks_b)
+              ok = mbar_wait(&kv_empty[AT_STAGES + s], par, p.timeout_ns, abort_flag, p.status);
+            if (!ok) break;
           }
-        umma_commit(&s_full[t]);
-      }
-      __syncwarp();
-    };
-    // O_t += P_t(c) V_c; P_t from the first 64 columns of S_t, V from stage c & 1
-    auto issue_pv = [&](int t, int c) {
-      if (leader) {
-        const uint32_t v_lo = smem_u32(sV + (c & 1) * AT_TILE_BYTES) >> 4;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t bd = vdesc0 + v_lo + kb * (AT_TILE_BYTES / 2 / 16) + k16 * 128;
-            umma_bf16_tmem_a(tmem + 256 + t * 128, tmem + t * 128 + (kb * 4 + k16) * 8, bd, kIdescPV,
-                             (c | kb | k16) != 0 ? 1u : 0u);
+          const int krow = kbase + c * AT_KEYS;
+          mbar_arrive_expect_tx(&kv_full[s], 2 * AT_KV_BYTES);
+          // K (K-major B of Q K^T) and V (MN-major B of P V): each two {64 dims, 80 keys} boxes
+          for (int half = 0; half < 2; ++half) {
+            tma_load_2d(sK + s * AT_KV_BYTES + half * AT_KV_HALF, &tmK, &kv_full[s], g * AT_D + half * 64, krow);
+            tma_load_2d(sV + s * AT_KV_BYTES + half * AT_KV_HALF, &tmV, &kv_full[s], g * AT_D + half * 64, krow);
           }
-      }
-      __syncwarp();
-    };
-    bool ok = warp_wait(q_full, 0, p, abort_flag) && warp_wait(&kv_full[0], 0, p, abort_flag);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, 0);
-      if (chunks_b > 0) issue_s(1, 0);
-    }
-    for (int c = 0; c < n_all && ok; ++c) {
-      for (int t = 0; t < 2 && ok; ++t) {
-        const int nct = t ? chunks_b : chunks_a;
-        if (c >= nct) continue;
-        ok = warp_wait(&p_full[t], c & 1, p, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(t, c);
-        if (c + 1 < nct) {
-          ok = warp_wait(&kv_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(t, c + 1);
+          issued = c + 1;
+        }
+        // before the CTA may exit: every load this thread issued has landed (bounded; normally
+        // the MMAs have consumed them all and these phases are long complete)
+        const uint64_t t0 = globaltimer_ns();
+        bool landed = false;
+        while (!landed && globaltimer_ns() - t0 <= p.timeout_ns) {
+          landed = mbar_try_wait(smem_u32(q_full), 0);
+          for (int c = (issued > AT_STAGES ? issued - AT_STAGES : 0); c < issued && landed; ++c)
+            landed = mbar_try_wait(smem_u32(&kv_full[c % AT_STAGES]), (c / AT_STAGES) & 1);
+        }
+        if (!landed) {
+          *abort_flag = 1;
+          atomicOr(p.status, kDevTimeout);
         }
       }
-      if (leader) umma_commit(&kv_empty[c & 1]);  // every MMA reading stage c & 1 is issued
-      __syncwarp();
-    }
-    if (leader) umma_commit(mma_done);
-    __syncwarp();
-    // drain: the CTA exits only after its MMAs completed
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(smem_u32(mma_done), 0)) {
-      if (globaltimer_ns() - t0 > p.timeout_ns) {
-        *abort_flag = 1;
-        atomicOr(p.status, kDevTimeout);
-        break;
+    } else if (warp >= AT_WARP_MMA0 && warp < AT_WARP_MMA0 + 4) {
+      // ------------------------------------------------------------------ MMA issuers
+      const int role = warp - AT_WARP_MMA0;  // 0: S_A, 1: PV_A, 2: S_B, 3: PV_B
+      const int t = role >> 1;
+      const bool is_pv = (role & 1) != 0;
+      const int nct = t ? chunks_b : chunks_a;
+      const bool leader = lane == 0;
+      const uint32_t tS = tmem + t * 256 + AT_COL_S;
+      const uint32_t tP = tmem + t * 256 + AT_COL_P;
+      const uint32_t tO = tmem + t * 256 + AT_COL_O;
+      const uint64_t kdesc0 = sdesc_sw128(0, 16, 1024);           // K-major operand template
+      const uint64_t vdesc0 = sdesc_sw128(0, AT_KV_HALF, 1024);   // MN-major: 64-column halves 10 KB apart
+      bool ok = nct > 0 && warp_wait(q_full, 0, p, abort_flag);
+      if (!is_pv) {
+        // S_t(c) = Q_t K_c^T, as soon as K_c has landed and the softmax has read S_t(c - 1)
+        const uint32_t q_lo = smem_u32(sQ + t * AT_Q_BYTES) >> 4;
+        for (int c = 0; c < nct && ok; ++c) {
+          ok = warp_wait(&kv_full[c % AT_STAGES], (c / AT_STAGES) & 1, p, abort_flag);
+          if (ok && c > 0) ok = warp_wait(&s_free[t], (c - 1) & 1, p, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            const uint32_t k_lo = smem_u32(sK + (c % AT_STAGES) * AT_KV_BYTES) >> 4;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+              for (int k16 = 0; k16 < 4; ++k16) {
+                const uint64_t ad = kdesc0 + q_lo + kb * (AT_Q_BYTES / 2 / 16) + k16 * 2;
+                const uint64_t bd = kdesc0 + k_lo + kb * (AT_KV_HALF / 16) + k16 * 2;
+                umma_bf16(tS, ad, bd, kIdescS, (kb | k16) != 0 ? 1u : 0u);
+              }
+            umma_commit(&s_full[t]);
+          }
+          __syncwarp();
+        }
+      } else {
+        // O_t += P_t(c) V_c, once the softmax has written P_t(c) (and rescaled O_t)
+        for (int c = 0; c < nct && ok; ++c) {
+          ok = warp_wait(&kv_full[c % AT_STAGES], (c / AT_STAGES) & 1, p, abort_flag);
+          if (ok) ok = warp_wait(&p_full[t], c & 1, p, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            const uint32_t v_lo = smem_u32(sV + (c % AT_STAGES) * AT_KV_BYTES) >> 4;
+#pragma unroll
+            for (int k16 = 0; k16 < AT_KEYS / 16; ++k16)
+              umma_bf16_tmem_a(tO, tP + k16 * 8, vdesc0 + v_lo + k16 * 128, kIdescPV, (c | k16) != 0 ? 1u : 0u);
+            umma_commit(&pv_done[t]);
+            umma_commit(&kv_empty[t * AT_STAGES + c % AT_STAGES]);  // S_t(c) finished before P_t(c) existed
+          }
+          __syncwarp();
+        }
       }
+      // the CTA exits only after this thread's MMAs completed
+      drain_own_mmas(&issuer_done[role], leader, p, abort_flag);
     }
-  } else if (warp < 8) {
+  } else {
     // ----------------------------------------------------- softmax / correction
     regs_inc<AT_REGS_SOFTMAX>();
     // Scores are handled in the base-2 domain: t_j = S_j * scale * log2(e) (one FMA with the
@@ -324,8 +363,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + t * 128 + lane_off;
-    const uint32_t tO = tmem + 256 + t * 128 + lane_off;
+    const uint32_t tS = tmem + t * 256 + AT_COL_S + lane_off;
+    const uint32_t tP = tmem + t * 256 + AT_COL_P + lane_off;
+    const uint32_t tO = tmem + t * 256 + AT_COL_O + lane_off;
     const int nc = t ? chunks_b : chunks_a;
     const int rows_valid = t ? rows_b : rows_a;
     const int pos = pos_a + t * AT_ROWS + r;  // this row's position (rows past rows_valid compute unused values)
@@ -334,16 +374,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     float m = -INFINITY, l = 0.f;
     bool ok = nc > 0;
     for (int c = 0; c < nc && ok; ++c) {
-      // S_t(c) complete; for c > 0 so is P V of chunk c - 1 (issued before it)
       ok = warp_wait(&s_full[t], c & 1, p, abort_flag);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[AT_KEYS];
-#pragma unroll
-      for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld32p(tS + q * 32, v + q * 32);
+      tmem_ld32p(tS, v);
+      tmem_ld32p(tS + 32, v + 32);
+      tmem_ld16p(tS + 64, v + 64);
       tmem_ld_wait_only();
-#pragma unroll
-      for (int q = 0; q < AT_KEYS / 32; ++q) tmem_ld_tie(v + q * 32);
+      tmem_ld_tie(v);
+      tmem_ld_tie(v + 32);
+      tmem_ld_tie16(v + 64);
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);  // S_t(c) is in registers: Q K^T of chunk c + 1 may overwrite it
       const int kpos0 = c * AT_KEYS;
       if (kpos0 + AT_KEYS - 1 > warp_pos_min) {  // a key of this chunk is past some row of the warp
 #pragma unroll
@@ -355,7 +398,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(u2f(v[i]), u2f(v[i + 8]));
 #pragma unroll
-      for (int j = 16; j < AT_KEYS; j += 16)  // keys j .. j + 15, j + 15 <= 127
+      for (int j = 16; j < AT_KEYS; j += 16)  // keys j .. j + 15, j + 15 <= 79
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], u2f(v[j + i]), u2f(v[j + 8 + i]));
       const float mc = __fmul_rn(max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])), c2);
@@ -375,28 +418,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         v[j >> 1] = pack_bf16x2(e0, e1);
       }
       l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])));
-      // the rescale is taken by the whole warp when any of its rows needs it (x * 1 = x
-      // exactly, so a row whose maximum did not move keeps its bits)
-      if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (c > 0) {
+        // P V of chunk c - 1 done: O is current and P may be overwritten (every phase is
+        // waited for, in order)
+        ok = warp_wait(&pv_done[t], (c - 1) & 1, p, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        // the rescale is taken by the whole warp when any of its rows needs it (x * 1 = x
+        // exactly, so a row whose maximum did not move keeps its bits)
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int q = 0; q < AT_D / 32; ++q) {
-          uint32_t o[32];
-          tmem_ld32p(tO + q * 32, o);
-          tmem_ld_wait_only();
-          tmem_ld_tie(o);
+          for (int q = 0; q < AT_D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32p(tO + q * 32, o);
+            tmem_ld_wait_only();
+            tmem_ld_tie(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(__fmul_rn(u2f(o[i]), alpha));
-          tmem_st32p(tO + q * 32, o);
+            for (int i = 0; i < 32; ++i) o[i] = f2u(__fmul_rn(u2f(o[i]), alpha));
+            tmem_st32p(tO + q * 32, o);
+          }
         }
       }
-      // P over the first 64 columns of S_t: column k holds keys 2k (low half) and 2k + 1
-      tmem_st32p(tS, v);
-      tmem_st32p(tS + 32, v + 32);
+      // P: 40 columns, column k holds keys 2k (low half) and 2k + 1
+      tmem_st32p(tP, v);
+      tmem_st8p(tP + 32, v + 32);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
-    if (ok) ok = warp_wait(mma_done, 0, p, abort_flag);
+    if (ok) ok = warp_wait(&pv_done[t], (nc - 1) & 1, p, abort_flag);
     if (ok) {
       tc_fence_after();
       uint32_t o[AT_D];
@@ -426,7 +476,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == AT_WARP_MMA) {
+  if (warp == AT_WARP_MMA0) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
@@ -449,7 +499,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   if (B == 0 || Tq == 0 || max_q_rows == 0) return ISO_OK;
   if (!Q || !K || !V || !q_start || !k_start || !pos0 || !out) return ISO_ERR_INVALID_ARG;
   if (Tk == 0) return ISO_ERR_SHAPE;  // a query row sees at least one key
-  const int pairs = ((max_q_rows + AT_ROWS - 1) / AT_ROWS + 1) / 2;
+  const int pairs = ((max_q_rows + AT_ROWS - 1) / AT_ROWS + 1) / 2;  // 128-row tiles, two per CTA
   if (B > 65535 || pairs > 65535) return ISO_ERR_UNSUPPORTED;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
@@ -460,7 +510,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   if (st == ISO_OK)
     st = make_tmap_bf16(&tK, K, Tk, static_cast<uint64_t>(Hkv) * d, static_cast<uint64_t>(Hkv) * d, 64, AT_KEYS);
   if (st == ISO_OK)
-    st = make_tmap_bf16(&tV, V, Tk, static_cast<uint64_t>(Hkv) * d, static_cast<uint64_t>(Hkv) * d, 64, 64);
+    st = make_tmap_bf16(&tV, V, Tk, static_cast<uint64_t>(Hkv) * d, static_cast<uint64_t>(Hkv) * d, 64, AT_KEYS);
   if (st != ISO_OK) return st;
   AttnParams p;
   p.q_start = q_start;
