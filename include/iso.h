@@ -361,7 +361,7 @@ iso_status iso_rmsnorm_selected_logprob(const iso_contract* c, const iso_bf16* x
  * d == 128 (else ISO_ERR_UNSUPPORTED).  max_q_rows >= the largest query row
  * count of a sequence (it sizes the grid).  out [Tq x Hq x d] bf16 =
  * softmax(scale q.k) V; lse [Tq x Hq] fp32 = m + log l (NULL to skip).
- * The merge runs over fixed 128-key chunks of each sequence, in ascending
+ * The merge runs over fixed 80-key chunks of each sequence, in ascending
  * order, one online-softmax step per chunk; nothing depends on the other
  * rows of the call, so a row's bits are the same in a prefill (many rows) and
  * a decode call (one row at the same position), whatever the batch.  Keys

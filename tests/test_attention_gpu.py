@@ -66,9 +66,9 @@ def test_attention_vs_oracle_ragged(c8, Hq, Hkv):
 
 
 def test_attention_exact_tile_and_chunk_boundaries(c8):
-    # rows and positions that sit exactly on the 128-row tile and 128-key chunk grid
-    q_lens = [128, 256, 127, 129]
-    pos0 = [0, 128, 1, 127]
+    # rows and positions that sit exactly on the 128-row tile and the 80-key chunk grid
+    q_lens = [128, 256, 127, 129, 81, 160]
+    pos0 = [0, 80, 1, 79, 159, 240]
     Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, pos0, 2, 1, D, seed=22)
     out, lse = _run(c8, Q, K, V, qs, ks, p0)
     _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0)
@@ -81,7 +81,7 @@ def test_attention_prefill_equals_decode_bitwise(c8):
     Q, K, V, qs, ks, p0 = inputs.attention_inputs([300], [0], Hq, Hkv, D, seed=23)
     Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
     out, lse = B.attention(c8, Qd, Kd, Vd, qs.to(DEV), ks.to(DEV), p0.to(DEV), SCALE)
-    for r in (0, 1, 126, 127, 128, 129, 200, 255, 256, 299):
+    for r in (0, 1, 79, 80, 81, 126, 127, 128, 129, 159, 160, 200, 239, 240, 255, 256, 299):
         one = torch.tensor([0, 1], dtype=torch.int32, device=DEV)
         kv = torch.tensor([0, r + 1], dtype=torch.int32, device=DEV)
         o1, l1 = B.attention(c8, Qd[r:r + 1].contiguous(), Kd[:r + 1].contiguous(), Vd[:r + 1].contiguous(), one, kv,
