@@ -23,8 +23,10 @@
 // A chunk wholly past a row's position changes nothing in that row: t = -inf, a = 1, P = 0,
 // O + 0 = O.
 //
-// Structure: one CTA per (query head, sequence, pair of 128-row query tiles A and B), the
+// Structure: one CTA per (query-head group, sequence, pair of 128-row query tiles A and B), the
 // pairs with the most chunks first; 512 threads (4 warpgroups, registers rebalanced at entry).
+// A tile row is one (token, query head) pair: tiles hold 128 / G tokens x the G = Hq / Hkv heads
+// that share a KV head (when G divides 128), so one K / V stream serves all of them.
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread per query row
 //              (TMEM lane); each also rescales its O rows and writes the output
 //   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 4-stage ring
@@ -44,6 +46,10 @@
 #include "iso_ptx.cuh"
 
 namespace iso {
+
+// capi.cu: tensor map over a 3-D bf16 array [d2][d1][d0] (d0 innermost), 128-byte swizzle
+iso_status make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                             uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 
 namespace {
 
@@ -75,6 +81,8 @@ struct AttnParams {
   const int32_t* k_start;  // [B+1]
   const int32_t* pos0;     // [B]
   int B, Hq, Hkv;
+  int gp;   // query heads per tile (the G = Hq / Hkv heads of a KV group when G divides 128, else 1)
+  int tpt;  // tokens per tile, 128 / gp: tile row r is token r / gp, head r % gp of the group
   float scale_log2e;  // scale * log2(e), rounded to fp32
   __nv_bfloat16* out;  // [Tq x Hq x d]
   float* lse;          // [Tq x Hq]
@@ -143,6 +151,15 @@ __device__ __forceinline__ void tmem_st8p(uint32_t taddr, const uint32_t* r) {
                : "memory");
 }
 
+// 3-D tiled load; x is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 template <int R>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
@@ -178,26 +195,28 @@ __device__ __forceinline__ void drain_own_mmas(uint64_t* bar, bool leader, const
 __global__ void __launch_bounds__(AT_THREADS, 1)
     iso_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  // grid (Hq, B, tile pairs): the pairs furthest into their sequences (the most chunks) start first
-  const int h = blockIdx.x, b = blockIdx.y, pair = gridDim.z - 1 - blockIdx.z;
+  // grid (Hq / gp head groups, B, tile pairs): the pairs furthest into their sequences (the most
+  // chunks) start first.  A tile holds tpt tokens x gp heads (row r: token r / gp, head r % gp).
+  const int h0 = blockIdx.x * p.gp, b = blockIdx.y, pair = gridDim.z - 1 - blockIdx.z;
+  const int gp = p.gp, tpt = p.tpt;
   const int q0 = p.q_start[b], nq = p.q_start[b + 1] - q0;
   // shape checks, uniform over the CTA and taken before any barrier or TMEM use: the grid
   // must cover every query row, and the last row's keys must lie inside the sequence
-  if (threadIdx.x == 0 && h == 0 && pair == static_cast<int>(gridDim.z) - 1 &&
-      (nq > static_cast<int>(gridDim.z) * 2 * AT_ROWS || nq < 0 || p.pos0[b] < 0 ||
+  if (threadIdx.x == 0 && h0 == 0 && pair == static_cast<int>(gridDim.z) - 1 &&
+      (nq > static_cast<int>(gridDim.z) * 2 * tpt || nq < 0 || p.pos0[b] < 0 ||
        p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]))
     atomicOr(p.status, kDevBadShape);
   if (nq <= 0 || p.pos0[b] < 0 || p.k_start[b] + p.pos0[b] + nq > p.k_start[b + 1]) return;
   const int tileA = 2 * pair;
-  if (tileA * AT_ROWS >= nq) return;  // empty unit
-  // per tile (A, B): valid rows, position of row 0, chunks its last row sees
-  const int rows_a = min(AT_ROWS, nq - tileA * AT_ROWS);
-  const int rows_b = max(0, min(AT_ROWS, nq - (tileA + 1) * AT_ROWS));
-  const int pos_a = p.pos0[b] + tileA * AT_ROWS;
-  const int chunks_a = (pos_a + rows_a - 1) / AT_KEYS + 1;
-  const int chunks_b = rows_b > 0 ? (pos_a + AT_ROWS + rows_b - 1) / AT_KEYS + 1 : 0;
+  if (tileA * tpt >= nq) return;  // empty unit
+  // per tile (A, B): valid tokens, position of its first token, chunks its last token sees
+  const int tok_a = min(tpt, nq - tileA * tpt);
+  const int tok_b = max(0, min(tpt, nq - (tileA + 1) * tpt));
+  const int pos_a = p.pos0[b] + tileA * tpt;
+  const int chunks_a = (pos_a + tok_a - 1) / AT_KEYS + 1;
+  const int chunks_b = tok_b > 0 ? (pos_a + tpt + tok_b - 1) / AT_KEYS + 1 : 0;
   const int n_all = max(chunks_a, chunks_b);
-  const int g = h / (p.Hq / p.Hkv);
+  const int g = h0 / (p.Hq / p.Hkv);
   const int kbase = p.k_start[b];
 
   extern __shared__ uint8_t smem_raw[];
@@ -257,10 +276,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         int issued = 0;
         const int n_q_tiles = chunks_b > 0 ? 2 : 1;
         mbar_arrive_expect_tx(q_full, n_q_tiles * AT_Q_BYTES);
+        // Q of a tile: {64 dims, gp heads, tpt tokens} boxes, rows token-major
         for (int t = 0; t < n_q_tiles; ++t)
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(sQ + t * AT_Q_BYTES + kb * (AT_Q_BYTES / 2), &tmQ, q_full, h * AT_D + kb * 64,
-                        q0 + (tileA + t) * AT_ROWS);
+            tma_load_3d(sQ + t * AT_Q_BYTES + kb * (AT_Q_BYTES / 2), &tmQ, q_full, kb * 64, h0,
+                        q0 + (tileA + t) * tpt);
         for (int c = 0; c < n_all; ++c) {
           const int s = c % AT_STAGES;
           if (c >= AT_STAGES) {
@@ -367,9 +387,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t tP = tmem + t * 256 + AT_COL_P + lane_off;
     const uint32_t tO = tmem + t * 256 + AT_COL_O + lane_off;
     const int nc = t ? chunks_b : chunks_a;
-    const int rows_valid = t ? rows_b : rows_a;
-    const int pos = pos_a + t * AT_ROWS + r;  // this row's position (rows past rows_valid compute unused values)
-    const int warp_pos_min = pos_a + t * AT_ROWS + quarter * 32;
+    const int tok = r / gp;  // this row's token within the tile and head within the group
+    const int head = h0 + r % gp;
+    const bool row_valid = tok < (t ? tok_b : tok_a);
+    const int pos = pos_a + t * tpt + tok;  // this row's position (invalid rows compute unused values)
+    const int warp_pos_min = pos_a + t * tpt + (quarter * 32) / gp;
     const float c2 = p.scale_log2e;
     float m = -INFINITY, l = 0.f;
     bool ok = nc > 0;
@@ -455,9 +477,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tmem_ld_wait_only();
 #pragma unroll
       for (int q = 0; q < AT_D / 32; ++q) tmem_ld_tie(o + q * 32);
-      if (r < rows_valid) {
-        const int64_t row = q0 + (tileA + t) * AT_ROWS + r;
-        __nv_bfloat16* dst = p.out + (row * p.Hq + h) * AT_D;
+      if (row_valid) {
+        const int64_t row = q0 + (tileA + t) * tpt + tok;
+        __nv_bfloat16* dst = p.out + (row * p.Hq + head) * AT_D;
         const float inv_l = __frcp_rn(l);
 #pragma unroll
         for (int q = 0; q < AT_D / 8; ++q) {
@@ -468,7 +490,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           w.w = pack_bf16x2(__fmul_rn(u2f(o[q * 8 + 6]), inv_l), __fmul_rn(u2f(o[q * 8 + 7]), inv_l));
           *reinterpret_cast<uint4*>(dst + q * 8) = w;
         }
-        if (p.lse) p.lse[row * p.Hq + h] = __fadd_rn(__fmul_rn(m, kLn2), logf(l));
+        if (p.lse) p.lse[row * p.Hq + head] = __fadd_rn(__fmul_rn(m, kLn2), logf(l));
       }
     }
   }
@@ -499,14 +521,19 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   if (B == 0 || Tq == 0 || max_q_rows == 0) return ISO_OK;
   if (!Q || !K || !V || !q_start || !k_start || !pos0 || !out) return ISO_ERR_INVALID_ARG;
   if (Tk == 0) return ISO_ERR_SHAPE;  // a query row sees at least one key
-  const int pairs = ((max_q_rows + AT_ROWS - 1) / AT_ROWS + 1) / 2;  // 128-row tiles, two per CTA
+  // a tile packs the G = Hq / Hkv query heads of a KV group with 128 / G tokens each when G divides
+  // 128 (one KV stream serves all G heads: decode reads each KV head once), else 1 head x 128 tokens
+  const int G = Hq / Hkv;
+  const int gp = (G <= AT_ROWS && AT_ROWS % G == 0) ? G : 1;
+  const int tpt = AT_ROWS / gp;
+  const int pairs = ((max_q_rows + tpt - 1) / tpt + 1) / 2;  // tiles of tpt tokens, two per CTA
   if (B > 65535 || pairs > 65535) return ISO_ERR_UNSUPPORTED;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
   if (mis & 15u) return ISO_ERR_ALIGNMENT;
   if (!device_ready()) return ISO_ERR_CUDA;
   CUtensorMap tQ, tK, tV;
-  iso_status st = make_tmap_bf16(&tQ, Q, Tq, static_cast<uint64_t>(Hq) * d, static_cast<uint64_t>(Hq) * d, 64, AT_ROWS);
+  iso_status st = make_tmap_bf16_3d(&tQ, Q, d, Hq, Tq, d, static_cast<uint64_t>(Hq) * d, 64, gp, tpt);
   if (st == ISO_OK)
     st = make_tmap_bf16(&tK, K, Tk, static_cast<uint64_t>(Hkv) * d, static_cast<uint64_t>(Hkv) * d, 64, AT_KEYS);
   if (st == ISO_OK)
@@ -519,6 +546,8 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
+  p.gp = gp;
+  p.tpt = tpt;
   p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -533,7 +562,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
       return ISO_ERR_CUDA;
     attr_dev = dev;
   }
-  const dim3 grid(Hq, B, pairs);
+  const dim3 grid(Hq / gp, B, pairs);
   iso_attention_kernel<<<grid, AT_THREADS, AT_SMEM, static_cast<cudaStream_t>(stream)>>>(tQ, tK, tV, p);
   return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
