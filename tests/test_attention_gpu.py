@@ -53,7 +53,9 @@ def _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0):
     return ref
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (4, 1)])
+# G = Hq / Hkv query heads per KV head: 4, 1, 4; 8 and 16 pack 16 and 8 tokens per tile;
+# 3 does not divide 128 and runs one head per tile
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (4, 1), (8, 1), (16, 1), (6, 2)])
 def test_attention_vs_oracle_ragged(c8, Hq, Hkv):
     # several tiles and KV chunks, ragged tails, a KV cache before the rows (pos0 > 0),
     # keys past the last row, a one-row sequence and an empty one
@@ -105,10 +107,11 @@ def test_attention_batch_composition_invariant(c8):
         assert torch.equal(l1, lse[q0:q1]), b
 
 
-def test_attention_batched_decode_matches_prefill(c8):
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (16, 2), (6, 2)])
+def test_attention_batched_decode_matches_prefill(c8, Hq, Hkv):
     # one decode call over several sequences (one row each, at different positions) against
-    # the prefill of each sequence
-    Hq, Hkv = 4, 1
+    # the prefill of each sequence; the decode tiles pack the heads of a KV group differently
+    # from the prefill tiles, the bits must not change
     q_lens = [150, 33, 260]
     Q, K, V, qs, ks, p0 = inputs.attention_inputs(q_lens, [0, 0, 0], Hq, Hkv, D, seed=25)
     out, lse = _run(c8, Q, K, V, qs, ks, p0)
