@@ -34,12 +34,25 @@ def _parity(c, n_seq, max_len, H, V, seed, n_decode_samples):
     W = inputs.normal_bf16((H, V), 0.02, seed + 3, device=DEV)
     ids = inputs.uniform_ids(total, V, seed + 4, device=DEV)
     packed = run(c, states, gamma, W, ids)  # trainer: one packed batch
-    # rollout decode: one token per call
+    # rollout decode: one token per call (one workspace and output buffer reused, compared at the end)
     g = torch.Generator().manual_seed(seed + 5)
     sample = torch.randperm(total, generator=g)[:n_decode_samples].tolist()
-    for t in sample:
-        one = run(c, states[t:t + 1].contiguous(), gamma, W, ids[t:t + 1].contiguous())
-        assert torch.equal(f32_bits(one), f32_bits(packed[t:t + 1])), t
+    ws1 = torch.empty(B.selected_logprob_workspace(c, 1, V), dtype=torch.uint8, device=DEV)
+    h1 = torch.empty(1, H, dtype=torch.bfloat16, device=DEV)
+    dec = torch.empty(len(sample), 4, dtype=torch.float32, device=DEV)  # a 16-byte row per result (out alignment)
+    for i, t in enumerate(sample):
+        B.rmsnorm(c, states[t:t + 1], gamma, 1e-6, out=h1)
+        B.selected_logprob(c, h1, W, ids[t:t + 1], out=dec[i, :1], ws=ws1)
+    idx = torch.tensor(sample, device=DEV)
+    diff = (f32_bits(dec[:, 0]) != f32_bits(packed[idx])).nonzero()
+    assert diff.numel() == 0, sample[int(diff[0])]
+    # the fused RMSNorm + logprob call, one token per call, on part of the sample
+    wsf = torch.empty(B.rmsnorm_selected_logprob_workspace(c, 1, V), dtype=torch.uint8, device=DEV)
+    nf = min(64, len(sample))
+    fused = torch.empty(nf, 4, dtype=torch.float32, device=DEV)
+    for i, t in enumerate(sample[:nf]):
+        B.rmsnorm_selected_logprob(c, states[t:t + 1], gamma, 1e-6, W, ids[t:t + 1], out=fused[i, :1], ws=wsf)
+    assert torch.equal(f32_bits(fused[:, 0]), f32_bits(packed[idx[:nf]]))
     # decode-step emulation: step s batches token s of every sequence longer than s
     starts = np.cumsum([0] + lens[:-1])
     for s in list(range(0, min(max_len, 24))) + [max(lens) - 1]:
@@ -67,4 +80,4 @@ def test_packed_prefill_vs_decode_small():
 @pytest.mark.slow
 def test_config5_packed_prefill_vs_decode_full():
     c = B.Contract(8)
-    _parity(c, n_seq=64, max_len=8192, H=4096, V=151936, seed=4, n_decode_samples=256)
+    _parity(c, n_seq=64, max_len=8192, H=4096, V=151936, seed=4, n_decode_samples=4096)
