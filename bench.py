@@ -534,6 +534,15 @@ def profile_target(target: str, calls: int):
         o = torch.empty_like(Q)
         lse = torch.empty(Q.shape[0], ATT_HQ, dtype=torch.float32, device=dev)
         fn = lambda: B.attention(c, Q, K, V, qs, ks, p0, 1.0 / math.sqrt(ATT_D), max_q_rows=max(lens), out=o, lse=lse)
+    elif target == "diagnostics":
+        gen = torch.Generator().manual_seed(4)
+        lens = torch.randint(1, 8193, (64,), generator=gen)
+        offs = torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(lens, 0)]).to(torch.int32).to(dev)
+        n = int(lens.sum())
+        lp_r = (-torch.abs(torch.randn(n, generator=gen)) * 2).to(dev)
+        lp_t = lp_r + (torch.rand(n, generator=gen) < 0.5).to(dev) * torch.randn(n, generator=gen).to(dev) * 1e-3
+        dg = B.mismatch_diagnostics(c, lp_t, lp_r, offs)
+        fn = lambda: B.mismatch_diagnostics(c, lp_t, lp_r, offs, out=dg)
     elif target == "rmsnorm":
         x, g = inputs.rmsnorm_inputs(262144, 4096, seed=4, device=dev)
         y = torch.empty_like(x)
@@ -554,7 +563,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small"],
+    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small",
+                                                     "diagnostics"],
                     help="run one workload --steps times without timing (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_target:

@@ -15,7 +15,7 @@
 // K3 = (r - 1) - delta = expm1(delta) - delta, and the rejection decision is taken in double.
 // Identical logprobs give delta = 0, r = 1, K = 0 exactly; for |delta| < 2^-6 the K3 term comes
 // from its Taylor series in double (cheaper than exp on this part's few FP64 units), otherwise
-// from exp.  One 1024-thread block
+// from exp; identical logprobs skip the FP64 arithmetic altogether (their terms are exact zeros).  One 1024-thread block
 // per sequence: thread i adds its tokens t = start + i + 1024 j in ascending j, an xor-shuffle
 // tree (16, 8, 4, 2, 1) combines each warp, and thread 0 adds the 32 warp sums in warp order --
 // a fixed order that depends only on the sequence, never on the launch.
@@ -44,12 +44,16 @@ __global__ void __launch_bounds__(kDiagThreads)
     int nm = 0;
     for (int32_t t = t0 + static_cast<int32_t>(threadIdx.x); t < t1; t += kDiagThreads) {
       const float a = lp_train[t], r0 = lp_rollout[t];
+      if (a == r0) {
+        // identical logprobs: delta = 0, r_corr = 1, K1 = K3 = 0 exactly; adding those zeros
+        // leaves every sum's bits unchanged and max(mx, 0) = mx, so no FP64 work is needed
+        if (delta) delta[t] = 0.f;
+        if (tis_weight) tis_weight[t] = 1.0 < tau_tok ? 1.f : static_cast<float>(tau_tok);
+        continue;
+      }
       const double d = static_cast<double>(a) - static_cast<double>(r0);
       double r, k3;  // r_corr = exp(d) and K3 = (r_corr - 1) - d = expm1(d) - d
-      if (d == 0.0) {
-        r = 1.0;
-        k3 = 0.0;
-      } else if (fabs(d) < 0.015625) {
+      if (fabs(d) < 0.015625) {
         // expm1(d) - d by its Taylor series (terms through d^9: truncation below 1e-21 relative)
         k3 = d * d *
              (1.0 / 2 + d * (1.0 / 6 + d * (1.0 / 24 + d * (1.0 / 120 + d * (1.0 / 720 + d * (1.0 / 5040 +
