@@ -45,7 +45,7 @@ typedef enum {
   ISO_ERR_SHAPE = 2,             /* shape outside the contract (e.g. K % (16 L) != 0) */
   ISO_ERR_ALIGNMENT = 3,         /* pointer / leading dimension alignment */
   ISO_ERR_UNPROVEN_TOPOLOGY = 4, /* rank count not a power of two dividing L */
-  ISO_ERR_UNSUPPORTED = 5,       /* valid, but not supported by this build */
+  ISO_ERR_UNSUPPORTED = 5,       /* valid, but not supported by this library */
   ISO_ERR_CONTRACT_MISMATCH = 6, /* peer digest differs */
   ISO_ERR_WORKSPACE = 7,         /* workspace / buffer too small */
   ISO_ERR_CUDA = 8,              /* a CUDA runtime call failed */
@@ -65,7 +65,7 @@ typedef void* iso_stream;                 /* cudaStream_t */
  *  identities (SHA-256 digests of the serialized contract)]
  *
  * iso_contract_init: leaf_count = number of contiguous K-leaves (a power of
- * two, 1..8 in this build); schedule must be ISO_TREE_BALANCED_BINARY;
+ * two, 1..8 in this library); schedule must be ISO_TREE_BALANCED_BINARY;
  * acc_dtype must be ISO_F32; out_dtype must be ISO_BF16.  On success *out
  * receives a new contract (free with iso_contract_destroy) and digest (if not
  * NULL) the 32-byte SHA-256 of its canonical serialization, which covers every

@@ -223,7 +223,7 @@ const char* iso_status_string(iso_status s) {
     case ISO_ERR_SHAPE: return "unsupported shape (K must be a multiple of 16 x leaf count; see header)";
     case ISO_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
     case ISO_ERR_UNPROVEN_TOPOLOGY: return "rank count is not a power of two dividing the leaf count";
-    case ISO_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case ISO_ERR_UNSUPPORTED: return "configuration not supported by this library";
     case ISO_ERR_CONTRACT_MISMATCH: return "peer contract digest differs";
     case ISO_ERR_WORKSPACE: return "workspace or buffer too small";
     case ISO_ERR_CUDA: return "CUDA runtime error";
