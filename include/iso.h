@@ -280,7 +280,8 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
                            int T, int k, int H, iso_stream stream);
 /* The expert layer: for each partition p (experts with expert_partition[e] ==
  * p; NULL = one partition): permute, gather, grouped gate/up leaf-tree GEMM
- * (K = H) with G rounded to bf16, h = bf16_rn(silu(g) u), grouped down
+ * (K = H) with G rounded to bf16, h = bf16_rn(silu(g) u) (silu(g) = g / (1 + e^-g)
+ * in fp32 from the fast exp and divide intrinsics: a few fp32 ulps), grouped down
  * leaf-tree GEMM (K = F) rounded to bf16 into y_slots; then iso_moe_combine.
  * The result does not depend on the partition map.
  * x [T x H] bf16; topk_ids / topk_w as produced by iso_moe_route;

@@ -34,7 +34,9 @@
 //             also owns the TMEM allocation.
 //   warps 4-7 epilogue: one thread per accumulator row (TMEM lane); they run
 //             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMAs
-//             fill the next leaves, and write the output.
+//             fill the next leaves, and write the output.  With short leaves
+//             (bf16 and SwiGLU outputs) warps 8-11 join them: each warp then
+//             takes one 64-column half of its lane quarter's rows.
 // The tree's working set lives in four 128-column TMEM buffers.  Buffer
 // assignment is a FIFO free list replayed identically by the MMA thread and
 // the epilogue, so both sides agree without exchanging buffer ids.
@@ -264,13 +266,23 @@ __device__ __forceinline__ void rmsnorm_a_rows_inplace(uint8_t* sA, const GemmPa
   }
 }
 
+// Staging slot of 16-byte chunk c of row r in rows of CH chunks.  Rows of 128 or 256 bytes
+// (CH = 8, 16): key r % 8.  Rows of 64 bytes (CH = 4, two rows per 128-byte line): key
+// (r / 2) % 4.  Either way a quarter-warp's row-per-lane writes and its row-contiguous reads
+// touch distinct banks.
+template <int CH>
+__device__ __forceinline__ int stage_slot(int c, int r) {
+  static_assert(CH == 4 || CH == 8 || CH == 16, "staged rows of 64, 128 or 256 bytes");
+  return CH >= 8 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+}
+
 // One epilogue warp writes the bf16 tile rows of its 32 TMEM lanes.  Lane r holds
 // row r as CH chunks of 8 bf16 (16 bytes) and its destination row `orow` (-1: row not
 // stored).  The rows go through the warp's staging area (32 rows x CH*16 bytes, chunk c of
-// row r at slot c ^ (r & 7): conflict-free for both the row-per-lane writes and the
-// row-contiguous reads), then out whole rows at a time: each store instruction covers
-// 512/(CH*16) complete rows, so global writes are full 128-byte lines instead of 32
-// scattered 16-byte pieces.  Columns at or past col_end are not stored.
+// row r at slot stage_slot(c, r)), then out whole rows at a time: each store instruction
+// covers 512/(CH*16) complete rows, so global writes are whole rows (whole 128-byte lines
+// for CH >= 8) instead of 32 scattered 16-byte pieces.  Columns at or past col_end are not
+// stored.
 template <int CH>
 __device__ __forceinline__ void store_rows_staged(uint8_t* wst, int lane, const uint4 (&w)[CH], int orow,
                                                   __nv_bfloat16* out, int64_t ldo, int n0, int col_end) {
@@ -278,14 +290,14 @@ __device__ __forceinline__ void store_rows_staged(uint8_t* wst, int lane, const 
   constexpr int ROWS_PER_STEP = 32 / CH;
 #pragma unroll
   for (int c = 0; c < CH; ++c)
-    *reinterpret_cast<uint4*>(wst + lane * ROW_BYTES + ((c ^ (lane & 7)) << 4)) = w[c];
+    *reinterpret_cast<uint4*>(wst + lane * ROW_BYTES + (stage_slot<CH>(c, lane) << 4)) = w[c];
   __syncwarp();
   const int c = lane % CH;
 #pragma unroll 4
   for (int t = 0; t < 32 / ROWS_PER_STEP; ++t) {
     const int r = t * ROWS_PER_STEP + lane / CH;
     const int dst_row = __shfl_sync(0xffffffffu, orow, r);
-    const uint4 x = *reinterpret_cast<const uint4*>(wst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
+    const uint4 x = *reinterpret_cast<const uint4*>(wst + r * ROW_BYTES + (stage_slot<CH>(c, r) << 4));
     const int col = n0 + c * 8;
     if (dst_row >= 0 && col < col_end)
       *reinterpret_cast<uint4*>(out + static_cast<int64_t>(dst_row) * ldo + col) = x;
@@ -313,7 +325,7 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_
 constexpr uint32_t kIdescPair = idesc_bf16_f32(2 * BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
 
 // An epilogue warp is done with TMEM buffer b (its tcgen05 accesses completed and fenced).
-// One CTA: every epilogue thread arrives (count 128).  CTA pair: the MMA issuer sits in rank
+// One CTA: every epilogue thread arrives (count 32 x epilogue warps).  CTA pair: the MMA issuer sits in rank
 // 0, so one lane per warp of either CTA arrives on rank 0's barrier (count 8).
 template <bool PAIR>
 __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int lane) {
@@ -333,8 +345,11 @@ __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int 
 // FUSED: the fused RMSNorm prologue (single CTA, EPI_BF16 / EPI_LOGPROB): 12 warps, warps 8-11
 // normalise the A stages in place; registers rebalanced by setmaxnreg (epilogue 256, the rest
 // 120: 128 x 256 + 256 x 120 = 63,488 <= the launch's 384 x 168).
-template <int EPI, bool PAIR, bool FUSED>
-__global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
+// EPW: epilogue warps, 4 or 8 (8: single CTA, EPI_BF16 / EPI_SWIGLU, 12 warps; warp 4 + 4h + q
+// holds lane quarter q, column half h; setmaxnreg gives the 8 epilogue warps 200 registers and
+// warps 0-3 104: 256 x 200 + 128 x 104 = 64,512 = the launch's 384 x 168).
+template <int EPI, bool PAIR, bool FUSED, int EPW>
+__global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
     iso_leaf_tree_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -342,6 +357,9 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
   constexpr int BSTAGE = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // B bytes per stage in this CTA
   constexpr int CL = PAIR ? 2 : 1;
   static_assert(!FUSED || (!PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB)), "fused prologue: single CTA, bf16/logprob");
+  static_assert(EPW == 4 || (EPW == 8 && !PAIR && !FUSED && (EPI == EPI_BF16 || EPI == EPI_SWIGLU)),
+                "8 epilogue warps: single CTA, bf16/SwiGLU outputs");
+  static_assert(GEMM_THREADS_FUSED == 384 && GEMM_THREADS_EPI8 == 384, "12-warp launches");
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
@@ -376,7 +394,7 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
     }
     for (int b = 0; b < NUM_TMEM_BUFS; ++b) {
       mbar_init(&leaf_full[b], 1);
-      mbar_init(&buf_free[b], PAIR ? 8 : 128);
+      mbar_init(&buf_free[b], PAIR ? 8 : 32 * EPW);
     }
     mbar_init(&drain_bar[0], 1);
     mbar_init(&drain_bar[1], 1);
@@ -407,8 +425,9 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
   // k in [l*leaf_len + 64 j, min(+64, (l+1)*leaf_len)).
   const int per = (p.L >= 2) ? 2 : 1;
 
-  if (warp < 4 || warp >= 8) {
+  if (warp < 4 || (FUSED && warp >= 8)) {
   if constexpr (FUSED) regs_dec<GEMM_REGS_CONTROL_FUSED>();
+  if constexpr (EPW == 8) regs_dec<GEMM_REGS_CONTROL_EPI8>();
   if (warp == 0 || warp == 3) {
     const int me = warp == 0 ? 0 : 1;  // stage parity loaded by this warp
     if (me < per) {
@@ -642,7 +661,11 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
   } else {
     // --------------------------------------------------------------- epilogue
     if constexpr (FUSED) regs_inc<256>();
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    if constexpr (EPW == 8) regs_inc<GEMM_REGS_EPILOGUE_EPI8>();
+    const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+    const int chalf = (warp - 4) >> 2;  // EPW == 8: the 64-column half of every tile this warp takes
+    // this warp's bf16 output staging: 8 KB per lane quarter, or 4 KB per warp with 8 warps
+    uint8_t* const wstage = epi_stage + (EPW == 8 ? (warp - 4) * (32 * 128) : quarter * (32 * 256));
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     TreeBufs tb;
@@ -672,7 +695,7 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
             else
               (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, 32 * EPW);
           if (*abort_flag) {
             ok = false;
             break;
@@ -683,16 +706,22 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
           for (int m = 0; m < nm; ++m) {
             const int rb = tb.pop();
             const int lb = tb.top();
-            // left (lower leaves) += right, in place in TMEM, 64 columns per step
+            // left (lower leaves) += right, in place in TMEM, 64 columns per step as two
+            // 32-column pieces at ca and cb.  With 8 epilogue warps each warp merges exactly the
+            // columns it reads at the root (bf16: its 64-column half; SwiGLU: its 32 gate
+            // columns and the matching 32 up columns), so no warp reads TMEM columns that the
+            // other warp of its lane quarter writes.
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = 0; c < (EPW == 8 ? 1 : BN / 64); ++c) {
+              const int ca = EPW == 8 ? (EPI == EPI_SWIGLU ? chalf * 32 : chalf * 64) : c * 64;
+              const int cb = (EPW == 8 && EPI == EPI_SWIGLU) ? 64 + chalf * 32 : ca + 32;
               uint32_t x[64], y[64];
-              const uint32_t lo = tmem_base + lane_off + static_cast<uint32_t>(lb * BN + c * 64);
-              const uint32_t ro = tmem_base + lane_off + static_cast<uint32_t>(rb * BN + c * 64);
-              tmem_ld32p(lo, x);
-              tmem_ld32p(lo + 32, x + 32);
-              tmem_ld32p(ro, y);
-              tmem_ld32p(ro + 32, y + 32);
+              const uint32_t lo = tmem_base + lane_off + static_cast<uint32_t>(lb * BN);
+              const uint32_t ro = tmem_base + lane_off + static_cast<uint32_t>(rb * BN);
+              tmem_ld32p(lo + ca, x);
+              tmem_ld32p(lo + cb, x + 32);
+              tmem_ld32p(ro + ca, y);
+              tmem_ld32p(ro + cb, y + 32);
               tmem_ld_wait_only();
               tmem_ld_tie(x);
               tmem_ld_tie(x + 32);
@@ -700,8 +729,8 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
               tmem_ld_tie(y + 32);
 #pragma unroll
               for (int i = 0; i < 64; ++i) x[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
-              tmem_st32p(lo, x);
-              tmem_st32p(lo + 32, x + 32);
+              tmem_st32p(lo + ca, x);
+              tmem_st32p(lo + cb, x + 32);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -716,26 +745,34 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
         const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
         if (EPI == EPI_SWIGLU) {
           // columns [0,64) hold gate, [64,128) up (the second B box came from the up half):
-          // g, u = bf16_rn(root); h = bf16_rn(silu(g) * u), silu(g) = g / (1 + expf(-g)).
-          uint32_t v[BN];
+          // g, u = bf16_rn(root); h = bf16_rn(silu(g) * u) with silu(g) = g / (1 + e^-g) in fp32
+          // from the fast exp and divide intrinsics (a few fp32 ulps, far below the bf16 rounding
+          // of h; the same instructions for every row, tile and schedule).  This warp's h
+          // columns: all 64, or with 8 epilogue warps 32 (gate [h0, h0+32), up [64+h0, ...)).
+          constexpr int HC = 64 / (EPW / 4);
+          const int h0 = EPW == 8 ? chalf * HC : 0;
+          uint32_t v[2 * HC];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
+          for (int c = 0; c < HC / 32; ++c) {
+            tmem_ld32p(root_addr + h0 + c * 32, v + c * 32);
+            tmem_ld32p(root_addr + 64 + h0 + c * 32, v + HC + c * 32);
+          }
           tmem_ld_wait_only();
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          for (int c = 0; c < 2 * HC / 32; ++c) tmem_ld_tie(v + c * 32);
           tc_fence_before();
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
-          uint4 hw[8];
+          uint4 hw[HC / 8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < HC / 8; ++q) {
             float hv[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float g = __bfloat162float(__float2bfloat16_rn(u2f(v[q * 8 + i])));
-              const float u = __bfloat162float(__float2bfloat16_rn(u2f(v[64 + q * 8 + i])));
-              hv[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+              const float u = __bfloat162float(__float2bfloat16_rn(u2f(v[HC + q * 8 + i])));
+              hv[i] = __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
             }
             hw[q].x = pack_bf16x2(hv[0], hv[1]);
             hw[q].y = pack_bf16x2(hv[2], hv[3]);
@@ -743,44 +780,47 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
             hw[q].w = pack_bf16x2(hv[6], hv[7]);
           }
           if (p.epi_staged) {
-            store_rows_staged<8>(epi_stage + quarter * (32 * 256), lane, hw, row_ok ? row : -1,
-                                 reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0, n0 + 64);
+            store_rows_staged<HC / 8>(wstage, lane, hw, row_ok ? row : -1, reinterpret_cast<__nv_bfloat16*>(p.out),
+                                      p.ldo, n0 + h0, n0 + h0 + HC);
           } else if (row_ok) {
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + q * 8) = hw[q];
+            for (int q = 0; q < HC / 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + h0 + q * 8) = hw[q];
           }
         } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
-          // the root into registers, its TMEM buffer released, then convert and store
-          uint32_t v[BN];
+          // the root into registers, its TMEM buffer released, then convert and store; this
+          // warp's columns: all 128, or with 8 epilogue warps the 64 of its half
+          constexpr int RC = BN / (EPW / 4);
+          const int c0 = EPW == 8 ? chalf * RC : 0;
+          uint32_t v[RC];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
+          for (int c = 0; c < RC / 32; ++c) tmem_ld32p(root_addr + c0 + c * 32, v + c * 32);
           tmem_ld_wait_only();
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          for (int c = 0; c < RC / 32; ++c) tmem_ld_tie(v + c * 32);
           tc_fence_before();
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
           if (EPI == EPI_BF16 && p.epi_staged) {
-            uint4 w[BN / 8];
+            uint4 w[RC / 8];
 #pragma unroll
-            for (int q = 0; q < BN / 8; ++q) {
+            for (int q = 0; q < RC / 8; ++q) {
               w[q].x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
               w[q].y = pack_bf16x2(u2f(v[q * 8 + 2]), u2f(v[q * 8 + 3]));
               w[q].z = pack_bf16x2(u2f(v[q * 8 + 4]), u2f(v[q * 8 + 5]));
               w[q].w = pack_bf16x2(u2f(v[q * 8 + 6]), u2f(v[q * 8 + 7]));
             }
             const int orow = row_ok ? ((p.row_scatter != nullptr) ? p.row_scatter[row] : row) : -1;
-            store_rows_staged<BN / 8>(epi_stage + quarter * (32 * 256), lane, w, orow,
-                                      reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0, p.N);
+            store_rows_staged<RC / 8>(wstage, lane, w, orow, reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0 + c0,
+                                      p.N);
           } else if (row_ok) {
             if (EPI == EPI_BF16) {
               const int orow = (p.row_scatter != nullptr) ? p.row_scatter[row] : row;
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
 #pragma unroll
-              for (int q = 0; q < BN / 8; ++q) {
-                const int col = n0 + q * 8;
+              for (int q = 0; q < RC / 8; ++q) {
+                const int col = n0 + c0 + q * 8;
                 if (col < p.N) {
                   uint4 w;
                   w.x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
@@ -794,8 +834,8 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
               float* dst = reinterpret_cast<float*>(p.out) + U.chunk * p.out_group_stride +
                            static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
-              for (int q = 0; q < BN / 4; ++q) {
-                const int col = n0 + q * 4;
+              for (int q = 0; q < RC / 4; ++q) {
+                const int col = n0 + c0 + q * 4;
                 if (col < p.N)
                   *reinterpret_cast<uint4*>(dst + col) = make_uint4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
               }
@@ -886,15 +926,15 @@ __global__ void __launch_bounds__(FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS, 1)
 
 namespace {
 
-template <int EPI, bool PAIR, bool FUSED = false>
+template <int EPI, bool PAIR, bool FUSED = false, int EPW = 4>
 iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                       cudaStream_t s) {
-  constexpr int kThreads = FUSED ? GEMM_THREADS_FUSED : GEMM_THREADS;
+  constexpr int kThreads = FUSED ? GEMM_THREADS_FUSED : (EPW == 8 ? GEMM_THREADS_EPI8 : GEMM_THREADS);
   static int attr_dev = -1;  // device whose function attributes are set
   static int slots = 0;      // CTAs (pairs: clusters) resident at once on that device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
-  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED>;
+  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED, EPW>;
   if (attr_dev != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
       return ISO_ERR_CUDA;
@@ -920,8 +960,8 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     attr_dev = dev;
     const char* tr = getenv("ISO_TRACE");
     if (tr && tr[0] == '1')
-      fprintf(stderr, "[iso] gemm kernel epi=%d pair=%d: %d %s resident\n", EPI, PAIR ? 1 : 0, slots,
-              PAIR ? "CTA pairs" : "CTAs");
+      fprintf(stderr, "[iso] gemm kernel epi=%d pair=%d epilogue warps=%d: %d %s resident\n", EPI, PAIR ? 1 : 0,
+              EPW, slots, PAIR ? "CTA pairs" : "CTAs");
   }
   const int units = max_units < slots ? max_units : slots;
   if (units <= 0) return ISO_OK;
@@ -956,14 +996,19 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
     if (epi == EPI_LOGPROB) return launch_one<EPI_LOGPROB, false, true>(tmA, tmB, p, max_units, s);
     return ISO_ERR_INVALID_ARG;
   }
+  // short leaves: 8 epilogue warps (the expert layer's grouped GEMMs: 1.07 -> 0.94 ms per layer)
   switch (epi) {
     case EPI_BF16:
+      if (!pair && p.leaf_len <= EPI8_MAX_LEAF_BF16)
+        return launch_one<EPI_BF16, false, false, 8>(tmA, tmB, p, max_units, s);
       return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s)
                   : launch_one<EPI_BF16, false>(tmA, tmB, p, max_units, s);
     case EPI_F32:
       return pair ? launch_one<EPI_F32, true>(tmA, tmB, p, max_units, s)
                   : launch_one<EPI_F32, false>(tmA, tmB, p, max_units, s);
     case EPI_SWIGLU:
+      if (!pair && p.leaf_len <= EPI8_MAX_LEAF_SWIGLU)
+        return launch_one<EPI_SWIGLU, false, false, 8>(tmA, tmB, p, max_units, s);
       return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s)
                   : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s);
     case EPI_LOGPROB:

@@ -27,9 +27,10 @@ constexpr int UMMA_K = 16;
 // The A box has a_rows rows (128, or 16/32/64 when the whole problem has that few
 // rows); the freed space buys more pipeline stages for the weight stream.  The MMA
 // always reads 128 A rows; rows past the box hold stale data whose outputs are
-// never stored.  The staging area (8 KB per epilogue warp: 32 rows x 256 bytes)
-// lets a warp write its bf16 rows to global memory whole rows at a time; it
-// exists when the stages leave room for it (A boxes of 64 and 128 rows).
+// never stored.  The staging area (32 KB: per epilogue warp 32 rows x 256 bytes, or
+// x 128 bytes with 8 epilogue warps) lets a warp write its bf16 rows to global memory
+// whole rows at a time; it exists when the stages leave room for it (A boxes of 64 and
+// 128 rows).
 constexpr int MAX_STAGES = 12;
 constexpr int A_TILE_BYTES_MAX = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BK * BN * 2;
@@ -38,13 +39,25 @@ constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int GEMM_THREADS_FUSED = 384;      // + warps 8..11: the fused RMSNorm prologue
+// Short leaves: the tree merges and the root of a tile outlast its MMAs, so warps 8..11 join
+// the epilogue (two warps per TMEM lane quarter, each with its own columns of the tile).
+// Measured on GB300: a gain for SwiGLU roots with leaves up to 256 k and bf16 roots up to
+// 128 k; with bf16 roots and 256-k leaves the MMAs already hide the epilogue and the extra
+// warps cost 2-3 %.
+constexpr int GEMM_THREADS_EPI8 = 384;
+constexpr int EPI8_MAX_LEAF_SWIGLU = 256;
+constexpr int EPI8_MAX_LEAF_BF16 = 128;
+constexpr int GEMM_REGS_CONTROL_EPI8 = 104;   // setmaxnreg of warps 0-3 with 8 epilogue warps
+constexpr int GEMM_REGS_EPILOGUE_EPI8 = 200;  // and of warps 4-11
+static_assert(128 * GEMM_REGS_CONTROL_EPI8 + 256 * GEMM_REGS_EPILOGUE_EPI8 <= 384 * 168,
+              "register split within the launch's allocation");
 constexpr int GEMM_REGS_CONTROL_FUSED = 120;  // setmaxnreg of warps 0-3 and 8-11 (epilogue: 256)
 constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
 constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
 constexpr int MOE_MAX_EXPERTS = 256;
 constexpr int MOE_PERM_CHUNK = 1024;   // pairs per chunk of the permutation's counting sort
 constexpr int MOE_PERM_THREADS = 256;
-constexpr int EPI_STAGE_BYTES = 4 * 32 * BN * 2;  // 4 epilogue warps x 32 rows x 128 bf16
+constexpr int EPI_STAGE_BYTES = 4 * 32 * BN * 2;  // 4 epilogue warps x 32 rows x 128 bf16 (or 8 x 64)
 
 // Logprob vocab tiling: statistics per 128-column tile, 19 tiles per chunk.
 constexpr int LP_TILE_COLS = BN;

@@ -126,6 +126,19 @@ def test_layer_partition_invariance_bitwise(c8):
     assert same_bits(out_sub, base[sub])
 
 
+def test_layer_repeatable_mid_size(c8):
+    # many tiles per CTA with leaves of 256 (gate/up) and 96 (down) k: repeated calls and an
+    # expert partition give the same bits (catches races between epilogue warps that a
+    # one-tile-per-CTA problem cannot show)
+    T, H, E, F, k = 1024, 2048, 128, 768, 8
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=12, device=DEV)
+    ids, w = B.moe_route(c8, logits, k)
+    base = _layer(c8, x, ids, w, W1, W2)
+    for _ in range(3):
+        assert same_bits(_layer(c8, x, ids, w, W1, W2), base)
+    assert same_bits(_layer(c8, x, ids, w, W1, W2, [e * 2 // E for e in range(E)]), base)
+
+
 @pytest.mark.slow
 def test_config4_full_size_sampled(c8):
     T, H, E, F, k = 8192, 2048, 128, 768, 8
