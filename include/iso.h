@@ -296,6 +296,21 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
                                 const float* topk_w, const iso_bf16* W1, const iso_bf16* W2,
                                 const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
                                 int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream);
+/* The expert GEMMs of one expert-parallel rank, without the combine [IsoExec blog,
+ * "Parallelism-invariant kernels": expert outputs are combined in a fixed routing order, not
+ * in rank order].  For every routing slot (t, j) whose expert topk_ids[t, j] has
+ * expert_mask[e] != 0: y_slots[t * k + j] = bf16 of the down projection of
+ * h = bf16_rn(silu(g) u), exactly the slot rows iso_grouped_gemm_moe computes.  Rows of other
+ * slots are not written.  So ranks that own disjoint expert sets fill disjoint slot rows, and
+ * after the rows are exchanged, iso_moe_combine gives iso_grouped_gemm_moe's output bit for bit.
+ * expert_mask: HOST array [E] uint8.  y_slots [T x k x H] bf16.  Other arguments, shape rules
+ * and errors as iso_grouped_gemm_moe.  ws: iso_moe_experts_partial_workspace(c, T, E, k, H, F)
+ * bytes. */
+size_t iso_moe_experts_partial_workspace(const iso_contract* c, int T, int E, int k, int H, int F);
+iso_status iso_moe_experts_partial(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
+                                   const iso_bf16* W1, const iso_bf16* W2, const uint8_t* expert_mask,
+                                   iso_bf16* y_slots, int T, int E, int k, int H, int F, void* ws, size_t ws_bytes,
+                                   iso_stream stream);
 
 /* ------------------------------------------------- mismatch diagnostics
  * [VeXact paper, §2 Eq. (1): delta_t = log pi_train - log pi_rollout; §4.1:

@@ -75,6 +75,9 @@ _SIGNATURES = {
     "iso_grouped_gemm_moe_workspace": (_sz, [_vp, _int, _int, _int, _int, _int]),
     "iso_grouped_gemm_moe": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _int, _int, _int, _int,
                                     _vp, _sz, _vp]),
+    "iso_moe_experts_partial_workspace": (_sz, [_vp, _int, _int, _int, _int, _int]),
+    "iso_moe_experts_partial": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _sz,
+                                       _vp]),
     "iso_selftest_bounded_wait": (_int, [_u64, _vp]),
     "iso_selected_logprob_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]),
     "iso_rmsnorm_gemm_workspace": (_sz, [_vp, _int]),
@@ -440,6 +443,30 @@ def grouped_gemm_moe(c: Contract, x, ids, w, W1, W2, expert_partition=None, out=
                                     T, E, k, H, F, _ptr(ws), ws.numel(), _stream(stream))
     c.lib.check(st, "iso_grouped_gemm_moe")
     return out
+
+
+def moe_experts_partial_workspace(c: Contract, T, E, k, H, F) -> int:
+    return int(c.lib.iso_moe_experts_partial_workspace(c.handle, T, E, k, H, F))
+
+
+def moe_experts_partial(c: Contract, x, ids, W1, W2, expert_mask, y_slots=None, ws=None, stream=None):
+    """The slot rows [T*k, H] of the experts with expert_mask[e] set (a host sequence of E
+    flags); other rows of y_slots are left as they were (uninitialised when y_slots is None)."""
+    import torch
+    T, H = x.shape
+    E, _, F2 = W1.shape
+    F = F2 // 2
+    k = ids.shape[1]
+    if y_slots is None:
+        y_slots = torch.empty(T * k, H, dtype=torch.bfloat16, device=x.device)
+    need = moe_experts_partial_workspace(c, T, E, k, H, F)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    mask = (ctypes.c_uint8 * E)(*[1 if v else 0 for v in expert_mask])
+    st = c.lib.iso_moe_experts_partial(c.handle, _ptr(x), _ptr(ids), _ptr(W1), _ptr(W2), ctypes.cast(mask, _vp),
+                                       _ptr(y_slots), T, E, k, H, F, _ptr(ws), ws.numel(), _stream(stream))
+    c.lib.check(st, "iso_moe_experts_partial")
+    return y_slots
 
 
 def last_device_status(c: Contract, stream=None) -> int:

@@ -644,7 +644,8 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
 constexpr bool kMoePairs = false;
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
-//   y_slots [P x H] bf16 | x_perm [P x H] bf16 | h [P x F] bf16 |
+//   y_slots [P x H] bf16 (the full layer only; iso_moe_experts_partial writes the caller's) |
+//   x_perm [P x H] bf16 | h [P x F] bf16 |
 //   perm [P] | offsets [E+1] | counts [E] | up_prefix [E+1] | down_prefix [E+1] | part_map [E] |
 //   hist [chunks x E] (the permutation's chunk histogram)
 namespace {
@@ -652,11 +653,11 @@ struct MoeWs {
   size_t y, xp, h, perm, offs, counts, up, dn, part, hist, total;
 };
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
-MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
+MoeWs moe_ws_layout(int T, int E, int k, int H, int F, bool with_y) {
   const size_t P = static_cast<size_t>(T) * k;
   MoeWs w;
   size_t o = 0;
-  w.y = o; o += al(P * H * 2);
+  w.y = o; if (with_y) o += al(P * H * 2);
   w.xp = o; o += al(P * H * 2);
   w.h = o; o += al(P * F * 2);
   w.perm = o; o += al(P * 4);
@@ -669,37 +670,24 @@ MoeWs moe_ws_layout(int T, int E, int k, int H, int F) {
   w.total = o;
   return w;
 }
-}  // namespace
 
-size_t iso_grouped_gemm_moe_workspace(const iso_contract* c, int T, int E, int k, int H, int F) {
-  if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return 0;
-  return moe_ws_layout(T, E, k, H, F).total;
-}
-
-iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
-                                const float* topk_w, const iso_bf16* W1, const iso_bf16* W2,
-                                const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
-                                int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream) {
+// Shared argument checks of the expert-layer entry points.
+iso_status check_moe_args(const iso_contract* c, int T, int E, int k, int H, int F) {
   if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return ISO_ERR_INVALID_ARG;
   if (E > MOE_MAX_EXPERTS || !is_pow2(k) || k > 8) return ISO_ERR_UNSUPPORTED;
-  if (T == 0) return ISO_OK;
-  if (!x || !topk_ids || !topk_w || !W1 || !W2 || !out || !ws) return ISO_ERR_INVALID_ARG;
   const int L = iso_contract_leaf_count(c);
   if (H % (UMMA_K * L) || F % (UMMA_K * L) || H % BN || F % 64) return ISO_ERR_SHAPE;
-  if (expert_partition) {
-    if (num_partitions <= 0) return ISO_ERR_INVALID_ARG;
-    for (int e = 0; e < E; ++e)
-      if (expert_partition[e] < 0 || expert_partition[e] >= num_partitions) return ISO_ERR_INVALID_ARG;
-  } else {
-    num_partitions = 1;
-  }
-  if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) || !aligned16(ws)) return ISO_ERR_ALIGNMENT;
-  const MoeWs lay = moe_ws_layout(T, E, k, H, F);
-  if (ws_bytes < lay.total) return ISO_ERR_WORKSPACE;
-  if (!ensure_device_state()) return ISO_ERR_CUDA;
-  cudaStream_t s = S(stream);
-  char* base = static_cast<char*>(ws);
-  uint16_t* y = reinterpret_cast<uint16_t*>(base + lay.y);
+  return ISO_OK;
+}
+
+// The expert GEMMs of one partition (the experts e with part_map[e] == partition; all experts
+// when part_map is null): permute the routing slots by expert, gather their token rows, the
+// grouped gate/up GEMM with SwiGLU, and the grouped down GEMM, whose bf16 rows go to their
+// routing slots in y [P x H].  Slots of other experts are not written.
+iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids, const iso_bf16* W1,
+                            const iso_bf16* W2, const int32_t* part_map, int partition, uint16_t* y, int T, int E,
+                            int k, int H, int F, const MoeWs& lay, char* base, cudaStream_t s) {
+  const int L = iso_contract_leaf_count(c);
   uint16_t* xp = reinterpret_cast<uint16_t*>(base + lay.xp);
   uint16_t* hb = reinterpret_cast<uint16_t*>(base + lay.h);
   int32_t* perm = reinterpret_cast<int32_t*>(base + lay.perm);
@@ -707,13 +695,8 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   int32_t* counts = reinterpret_cast<int32_t*>(base + lay.counts);
   int32_t* up = reinterpret_cast<int32_t*>(base + lay.up);
   int32_t* dn = reinterpret_cast<int32_t*>(base + lay.dn);
-  int32_t* part = reinterpret_cast<int32_t*>(base + lay.part);
   int32_t* hist = reinterpret_cast<int32_t*>(base + lay.hist);
   const int64_t P = static_cast<int64_t>(T) * k;
-  if (expert_partition &&
-      cudaMemcpyAsync(part, expert_partition, sizeof(int32_t) * E, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return ISO_ERR_CUDA;
-
   CUtensorMap tX, tW1, tH, tW2;
   iso_status st = make_tmap_bf16(&tX, xp, P, H, H, BK, BM);
   if (st == ISO_OK) st = make_tmap_bf16(&tW1, W1, static_cast<uint64_t>(E) * H, 2 * F, 2 * F, 64, BK);
@@ -722,46 +705,113 @@ iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const 
   if (st != ISO_OK) return st;
   const int up_nb = F / 64, dn_nb = H / BN;
   const int unit_rows = kMoePairs ? 2 * BM : BM;  // rows of an expert per grouped work unit
+  if (launch_moe_permute(topk_ids, P, E, part_map, partition, counts, hist, perm, offs, up, up_nb, dn, dn_nb,
+                         unit_rows, s) != cudaSuccess)
+    return ISO_ERR_CUDA;
+  if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
+  // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns
+  // [F+64j, F+64j+64) and writes h columns [64j, 64j+64).
+  GemmParams p = base_params(0, F, H, L);
+  p.n_blocks = F / 64;
+  p.b_tile_cols = 64;
+  p.b_box2_off = F;
+  p.unit_mode = UNIT_GROUPED;
+  p.g_offsets = offs;
+  p.g_unit_prefix = up;
+  p.E = E;
+  p.out = hb;
+  p.ldo = F;
+  if (kMoePairs) {
+    p.pair = 1;
+    set_a_rows(p, 128);
+  }
+  st = launch_gemm(EPI_SWIGLU, tX, tW1, p, sm_count(), s);
+  if (st != ISO_OK) return st;
+  GemmParams q = base_params(0, H, F, L);
+  q.unit_mode = UNIT_GROUPED;
+  q.g_offsets = offs;
+  q.g_unit_prefix = dn;
+  q.E = E;
+  q.out = y;
+  q.ldo = H;
+  q.row_scatter = perm;
+  if (kMoePairs) {
+    q.pair = 1;
+    set_a_rows(q, 128);
+  }
+  return launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s);
+}
+}  // namespace
+
+size_t iso_grouped_gemm_moe_workspace(const iso_contract* c, int T, int E, int k, int H, int F) {
+  if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return 0;
+  return moe_ws_layout(T, E, k, H, F, true).total;
+}
+
+iso_status iso_grouped_gemm_moe(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
+                                const float* topk_w, const iso_bf16* W1, const iso_bf16* W2,
+                                const int32_t* expert_partition, int num_partitions, iso_bf16* out, int T, int E,
+                                int k, int H, int F, void* ws, size_t ws_bytes, iso_stream stream) {
+  iso_status st = check_moe_args(c, T, E, k, H, F);
+  if (st != ISO_OK) return st;
+  if (T == 0) return ISO_OK;
+  if (!x || !topk_ids || !topk_w || !W1 || !W2 || !out || !ws) return ISO_ERR_INVALID_ARG;
+  if (expert_partition) {
+    if (num_partitions <= 0) return ISO_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e)
+      if (expert_partition[e] < 0 || expert_partition[e] >= num_partitions) return ISO_ERR_INVALID_ARG;
+  } else {
+    num_partitions = 1;
+  }
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) || !aligned16(ws)) return ISO_ERR_ALIGNMENT;
+  const MoeWs lay = moe_ws_layout(T, E, k, H, F, true);
+  if (ws_bytes < lay.total) return ISO_ERR_WORKSPACE;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  char* base = static_cast<char*>(ws);
+  uint16_t* y = reinterpret_cast<uint16_t*>(base + lay.y);
+  int32_t* part = reinterpret_cast<int32_t*>(base + lay.part);
+  if (expert_partition &&
+      cudaMemcpyAsync(part, expert_partition, sizeof(int32_t) * E, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return ISO_ERR_CUDA;
   trace("grouped_gemm_moe", T, E, k, num_partitions);
   for (int pi = 0; pi < num_partitions; ++pi) {
-    if (launch_moe_permute(topk_ids, P, E, expert_partition ? part : nullptr, pi, counts, hist, perm, offs, up, up_nb,
-                           dn, dn_nb, unit_rows, s) != cudaSuccess)
-      return ISO_ERR_CUDA;
-    if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
-    // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns
-    // [F+64j, F+64j+64) and writes h columns [64j, 64j+64).
-    GemmParams p = base_params(0, F, H, L);
-    p.n_blocks = F / 64;
-    p.b_tile_cols = 64;
-    p.b_box2_off = F;
-    p.unit_mode = UNIT_GROUPED;
-    p.g_offsets = offs;
-    p.g_unit_prefix = up;
-    p.E = E;
-    p.out = hb;
-    p.ldo = F;
-    if (kMoePairs) {
-      p.pair = 1;
-      set_a_rows(p, 128);
-    }
-    st = launch_gemm(EPI_SWIGLU, tX, tW1, p, sm_count(), s);
-    if (st != ISO_OK) return st;
-    GemmParams q = base_params(0, H, F, L);
-    q.unit_mode = UNIT_GROUPED;
-    q.g_offsets = offs;
-    q.g_unit_prefix = dn;
-    q.E = E;
-    q.out = y;
-    q.ldo = H;
-    q.row_scatter = perm;
-    if (kMoePairs) {
-      q.pair = 1;
-      set_a_rows(q, 128);
-    }
-    st = launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s);
+    st = moe_experts_pass(c, x, topk_ids, W1, W2, expert_partition ? part : nullptr, pi, y, T, E, k, H, F, lay, base,
+                          s);
     if (st != ISO_OK) return st;
   }
   return launch_moe_combine(y, topk_w, T, k, H, out, s) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+}
+
+size_t iso_moe_experts_partial_workspace(const iso_contract* c, int T, int E, int k, int H, int F) {
+  if (!c || T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return 0;
+  return moe_ws_layout(T, E, k, H, F, false).total;
+}
+
+iso_status iso_moe_experts_partial(const iso_contract* c, const iso_bf16* x, const int32_t* topk_ids,
+                                   const iso_bf16* W1, const iso_bf16* W2, const uint8_t* expert_mask,
+                                   iso_bf16* y_slots, int T, int E, int k, int H, int F, void* ws, size_t ws_bytes,
+                                   iso_stream stream) {
+  iso_status st = check_moe_args(c, T, E, k, H, F);
+  if (st != ISO_OK) return st;
+  if (T == 0) return ISO_OK;
+  if (!x || !topk_ids || !W1 || !W2 || !expert_mask || !y_slots || !ws) return ISO_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(y_slots) || !aligned16(ws))
+    return ISO_ERR_ALIGNMENT;
+  const MoeWs lay = moe_ws_layout(T, E, k, H, F, false);
+  if (ws_bytes < lay.total) return ISO_ERR_WORKSPACE;
+  if (!ensure_device_state()) return ISO_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  char* base = static_cast<char*>(ws);
+  int32_t* part = reinterpret_cast<int32_t*>(base + lay.part);
+  // the mask as a two-partition map, partition 1 = the masked experts (cudaMemcpyAsync from
+  // pageable host memory returns once the source has been read, so a stack array is safe)
+  int32_t map[MOE_MAX_EXPERTS];
+  for (int e = 0; e < E; ++e) map[e] = expert_mask[e] ? 1 : 0;
+  if (cudaMemcpyAsync(part, map, sizeof(int32_t) * E, cudaMemcpyHostToDevice, s) != cudaSuccess) return ISO_ERR_CUDA;
+  trace("moe_experts_partial", T, E, k, 1);
+  return moe_experts_pass(c, x, topk_ids, W1, W2, part, 1, reinterpret_cast<uint16_t*>(y_slots), T, E, k, H, F, lay,
+                          base, s);
 }
 
 iso_status iso_selftest_bounded_wait(uint64_t timeout_ns, iso_stream stream) {

@@ -111,6 +111,24 @@ def test_host_validation_launches_nothing(lib):
     # moe: k not a power of two for the combine; E too large for routing
     assert lib.iso_moe_combine(c.handle, fake, fake, fake, 4, 3, 256, s0) == 5
     assert lib.iso_moe_route(c.handle, fake, 4, 512, 8, fake, fake, s0) == 5
+    # expert layer: the one-rank partial needs the layer's workspace minus the slot rows
+    # (T k H bf16, here 16*8*256*2 bytes, 256-byte aligned); shape, alignment, workspace and
+    # missing-mask errors come from the host checks
+    full = lib.iso_grouped_gemm_moe_workspace(c.handle, 16, 8, 8, 256, 128)
+    part = lib.iso_moe_experts_partial_workspace(c.handle, 16, 8, 8, 256, 128)
+    assert full - part == 16 * 8 * 256 * 2
+    assert lib.iso_moe_experts_partial(c.handle, fake, fake, fake, fake, None, fake, 16, 8, 8, 256, 128, fake, part,
+                                       s0) == 1
+    mask = (ctypes.c_uint8 * 8)(*([1] * 8))
+    mk = ctypes.cast(mask, ctypes.c_void_p)
+    assert lib.iso_moe_experts_partial(c.handle, fake, fake, fake, fake, mk, fake, 16, 8, 8, 264, 128, fake, part,
+                                       s0) == 2
+    assert lib.iso_moe_experts_partial(c.handle, fake, fake, fake, fake, mk, odd, 16, 8, 8, 256, 128, fake, part,
+                                       s0) == 3
+    assert lib.iso_moe_experts_partial(c.handle, fake, fake, fake, fake, mk, fake, 16, 8, 8, 256, 128, fake,
+                                       part - 1, s0) == 7
+    assert lib.iso_moe_experts_partial(c.handle, fake, fake, fake, fake, mk, fake, 0, 8, 8, 256, 128, fake, part,
+                                       s0) == B.ISO_OK
     # bounded-wait self test: limit out of range
     assert lib.iso_selftest_bounded_wait(0, s0) == 1
 

@@ -139,6 +139,58 @@ def test_layer_repeatable_mid_size(c8):
     assert same_bits(_layer(c8, x, ids, w, W1, W2, [e * 2 // E for e in range(E)]), base)
 
 
+@pytest.mark.parametrize("T,H,E,F,seed", [(300, 256, 16, 128, 13), (1024, 2048, 128, 768, 15)])
+def test_experts_partial_ranks_combine_to_layer(c8, T, H, E, F, seed):
+    # expert parallelism through the lower-level entry: two ranks own disjoint expert sets,
+    # each writes exactly the slot rows of its experts, and the combine of the exchanged rows
+    # equals the whole layer bit for bit (the second size runs the engine's short-leaf path)
+    k = 8
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=seed, device=DEV)
+    ids, w = B.moe_route(c8, logits, k)
+    base = _layer(c8, x, ids, w, W1, W2)
+    owner = inputs.random_partition(E, 2, seed=seed + 1).tolist()
+    slot_owner = torch.tensor(owner, device=DEV)[ids.flatten().long()]
+    assert 0 < int(slot_owner.sum()) < T * k  # both ranks serve slots
+    ys = []
+    for r in range(2):
+        y = torch.full((T * k, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+        B.moe_experts_partial(c8, x, ids, W1, W2, [o == r for o in owner], y_slots=y)
+        mine = slot_owner == r
+        assert not torch.isnan(y[mine].float()).any()
+        assert torch.isnan(y[~mine].float()).all()  # other ranks' rows untouched
+        ys.append(y)
+    full = torch.where((slot_owner == 0)[:, None], ys[0], ys[1])
+    assert same_bits(B.moe_combine(c8, full.view(T, k, H), w), base)
+    # one rank owning every expert: all rows, the same bits
+    y_all = B.moe_experts_partial(c8, x, ids, W1, W2, [1] * E)
+    assert same_bits(y_all, full)
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
+def test_experts_partial_argument_errors(c8):
+    lib = B.load()
+    T, H, E, F, k = 16, 256, 8, 128, 8
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=17, device=DEV)
+    ids, _ = B.moe_route(c8, logits, k)
+    y = torch.empty(T * k, H, dtype=torch.bfloat16, device=DEV)
+    need = B.moe_experts_partial_workspace(c8, T, E, k, H, F)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    mask = (B.ctypes.c_uint8 * E)(*([1] * E))
+    P = B._ptr
+    s = B._stream()
+
+    def call(maskp=B.ctypes.cast(mask, B._vp), yp=P(y), nbytes=need, Hh=H):
+        return lib.iso_moe_experts_partial(c8.handle, P(x), P(ids), P(W1), P(W2), maskp, yp, T, E, k, Hh, F, P(ws),
+                                           nbytes, s)
+
+    assert call(maskp=None) == B.ISO_ERR_INVALID_ARG
+    assert call(yp=B._vp(y.data_ptr() + 2)) == B.ISO_ERR_ALIGNMENT
+    assert call(nbytes=need - 1) == B.ISO_ERR_WORKSPACE
+    assert call(Hh=H + 8) == B.ISO_ERR_SHAPE
+    assert call() == B.ISO_OK
+    assert lib.iso_last_device_status(s) == B.ISO_OK
+
+
 @pytest.mark.slow
 def test_config4_full_size_sampled(c8):
     T, H, E, F, k = 8192, 2048, 128, 768, 8
