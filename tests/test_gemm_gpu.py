@@ -73,6 +73,23 @@ def test_exact_integer_multi_tile_ragged(M, N, K, L):
     assert np.array_equal(bits(C), oracle.gemm(bits(A), bits(Bm), L))
 
 
+@pytest.mark.parametrize("M,K", [(1, 1024), (7, 768), (16, 512), (33, 1024)])
+def test_short_leaves_small_m_exact_and_row_invariant(c8, M, K):
+    # leaves of 64-128 k with few rows: 8 epilogue warps, A boxes of 16-64 rows, and (for
+    # 16- and 32-row boxes) the unstaged store path; exact integers equal the oracle, and the
+    # rows have the same bits as inside a 300-row product (staged stores, 128-row boxes)
+    N = 392
+    A = inputs.small_int_bf16((300, K), -3, 3, seed=K + M)
+    Bm = inputs.small_int_bf16((K, N), -3, 3, seed=K)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    C = B.gemm(c8, Ad[:M].contiguous(), Bd)
+    assert np.array_equal(bits(C), oracle.gemm(bits(A[:M]), bits(Bm), 8))
+    An = inputs.gemm_inputs(300, K, N, seed=M)[0].to(DEV)
+    Bn = inputs.gemm_inputs(300, K, N, seed=M + 1)[1].to(DEV)
+    big = B.gemm(c8, An, Bn)
+    assert same_bits(B.gemm(c8, An[:M].contiguous(), Bn), big[:M])
+
+
 def test_identity_and_permutation_are_exact(c8):
     A, _ = inputs.gemm_inputs(200, 256, 1, seed=3)
     I = torch.eye(256, dtype=torch.bfloat16)
