@@ -109,17 +109,29 @@ static bool resolve_encode() {
   return true;
 }
 
-iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
-                          uint32_t box_cols, uint32_t box_rows) {
+namespace {
+iso_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                        uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   if (!resolve_encode()) return ISO_ERR_CUDA;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {ld * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ISO_OK : ISO_ERR_CUDA;
+}
+}  // namespace
+
+iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                          uint32_t box_cols, uint32_t box_rows) {
+  return make_tmap_2d(map, base, rows, cols, ld, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+iso_status make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                               uint32_t box_cols, uint32_t box_rows) {
+  return make_tmap_2d(map, base, rows, cols, ld, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Tensor map over a 3-D bf16 array [d2][d1][d0] (d0 innermost, contiguous), strides s1 and s2
@@ -149,6 +161,20 @@ void set_a_rows(GemmParams& p, int a_rows) {
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
   p.epi_staged = (room - p.stages * (p.a_bytes + b_bytes) >= EPI_STAGE_BYTES) ? 1 : 0;
+}
+
+// Whole-leaf stages (leaves of 96 k, bf16 roots on one CTA): a stage holds a leaf, A in a
+// 64-column and a 32-column box, B in 96-row boxes; the stage count that fits.
+void set_leaf_stage(GemmParams& p) {
+  p.leaf_stage = 1;
+  p.kb_per_leaf = 1;
+  p.a_rows = BM;
+  p.a_bytes = LS_A_BYTES;
+  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES;
+  int st = room / (LS_A_BYTES + LS_B_BYTES);
+  if (st > MAX_STAGES) st = MAX_STAGES;
+  p.stages = st & ~1;
+  p.epi_staged = (room - p.stages * (LS_A_BYTES + LS_B_BYTES) >= EPI_STAGE_BYTES) ? 1 : 0;
 }
 
 // Row blocks per raster group of the GEMM unit order: the CTAs running at once share a few
@@ -697,11 +723,15 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   int32_t* dn = reinterpret_cast<int32_t*>(base + lay.dn);
   int32_t* hist = reinterpret_cast<int32_t*>(base + lay.hist);
   const int64_t P = static_cast<int64_t>(T) * k;
-  CUtensorMap tX, tW1, tH, tW2;
+  // the down projection's leaves of 96 k (F = 768 with 8 leaves) run on whole-leaf stages
+  const bool leaf_stage = F / L == LS_LEAF && !kMoePairs;
+  CUtensorMap tX, tW1, tH, tH2, tW2;
   iso_status st = make_tmap_bf16(&tX, xp, P, H, H, BK, BM);
   if (st == ISO_OK) st = make_tmap_bf16(&tW1, W1, static_cast<uint64_t>(E) * H, 2 * F, 2 * F, 64, BK);
   if (st == ISO_OK) st = make_tmap_bf16(&tH, hb, P, F, F, BK, BM);
-  if (st == ISO_OK) st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, BK);
+  if (st == ISO_OK && leaf_stage) st = make_tmap_bf16_sw64(&tH2, hb, P, F, F, 32, BM);
+  if (st == ISO_OK)
+    st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, leaf_stage ? LS_LEAF : BK);
   if (st != ISO_OK) return st;
   const int up_nb = F / 64, dn_nb = H / BN;
   const int unit_rows = kMoePairs ? 2 * BM : BM;  // rows of an expert per grouped work unit
@@ -738,6 +768,10 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   if (kMoePairs) {
     q.pair = 1;
     set_a_rows(q, 128);
+  }
+  if (leaf_stage) {
+    set_leaf_stage(q);
+    return launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s, &tH2);
   }
   return launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s);
 }

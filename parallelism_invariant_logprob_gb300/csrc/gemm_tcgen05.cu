@@ -348,18 +348,22 @@ __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int 
 // EPW: epilogue warps, 4 or 8 (8: single CTA, EPI_BF16 / EPI_SWIGLU, 12 warps; warp 4 + 4h + q
 // holds lane quarter q, column half h; setmaxnreg gives the 8 epilogue warps 200 registers and
 // warps 0-3 104: 256 x 200 + 128 x 104 = 64,512 = the launch's 384 x 168).
-template <int EPI, bool PAIR, bool FUSED, int EPW>
+// LS: whole-leaf stages for leaves of 96 k (GemmParams::leaf_stage; single CTA, bf16 roots,
+// 8 epilogue warps): tmA2 maps the A operand with 32-column boxes and a 64-byte swizzle.
+template <int EPI, bool PAIR, bool FUSED, int EPW, bool LS>
 __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
     iso_leaf_tree_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                              const GemmParams p) {
+                              const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int BSTAGE = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // B bytes per stage in this CTA
+  // B bytes per stage in this CTA
+  constexpr int BSTAGE = LS ? LS_B_BYTES : (PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES);
   constexpr int CL = PAIR ? 2 : 1;
   static_assert(!FUSED || (!PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB)), "fused prologue: single CTA, bf16/logprob");
   static_assert(EPW == 4 || (EPW == 8 && !PAIR && !FUSED && (EPI == EPI_BF16 || EPI == EPI_SWIGLU)),
                 "8 epilogue warps: single CTA, bf16/SwiGLU outputs");
   static_assert(GEMM_THREADS_FUSED == 384 && GEMM_THREADS_EPI8 == 384, "12-warp launches");
+  static_assert(!LS || (EPI == EPI_BF16 && !PAIR && !FUSED && EPW == 8), "whole-leaf stages: the 8-warp bf16 path");
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
@@ -387,6 +391,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (LS) tma_prefetch_desc(&tmA2);
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full_bar[s], FUSED ? 1 + 4 : 1);  // + one arrival per transform warp
       if (FUSED) mbar_init(&raw_bar[s], 1);
@@ -474,6 +479,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 } else {
                   mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.a_bytes + BSTAGE));
                   tma_load_2d(sA, &tmA, &full_bar[stage], U.a_col0 + kx, U.a_row0);
+                  if (LS)  // the leaf's last 32 columns, 64-byte swizzle
+                    tma_load_2d(sA + LS_A2_OFF, &tmA2, &full_bar[stage], U.a_col0 + kx + 64, U.a_row0);
                   tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
                   tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
                 }
@@ -523,7 +530,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       const uint32_t smem_base = smem_u32(smem);
       // descriptor templates; the start-address field (bits 0..13, 16-byte units) is added per use
       const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
-      const uint64_t bdesc0 = sdesc_sw128(0, 8192, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(0, LS ? LS_B_BYTES / 2 : 8192, 1024);  // LBO: the second 64 columns
+      const uint64_t a2desc0 = sdesc_sw64(0, 16, 512);                          // LS: 64-byte rows, 8-row atoms
       uint32_t seq = 0;  // sequence number of the current leaf (all tiles, both threads' leaves)
       for (int u = unit0; u < nunits && ok; u += unit_step) {
         Unit U;
@@ -583,7 +591,19 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                     if (j == p.kb_per_leaf - 1) umma_commit_pair(&leaf_full[b], 3);
                     umma_commit_pair(&empty_bar[stage], 3);
                   } else {
-                    if (rem >= BK) {
+                    if (LS) {
+                      // one whole 96-k leaf: k 0..63 from the 128-byte-swizzled A box, k 64..95 from
+                      // the 64-byte-swizzled one (+32 bytes per K = 16 within its 64-byte rows);
+                      // B rows 0..95 of the stage, +2 KB per K = 16
+                      const uint64_t a2desc =
+                          a2desc0 + static_cast<uint64_t>((smem_base + stage * p.a_bytes + LS_A2_OFF) >> 4);
+                      umma_bf16(d, adesc, bdesc, kIdesc, 0u);
+                      umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
+                      umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
+                      umma_bf16(d, adesc + 6, bdesc + 384, kIdesc, 1u);
+                      umma_bf16(d, a2desc, bdesc + 512, kIdesc, 1u);
+                      umma_bf16(d, a2desc + 2, bdesc + 640, kIdesc, 1u);
+                    } else if (rem >= BK) {
                       umma_bf16(d, adesc, bdesc, kIdesc, j != 0 ? 1u : 0u);
                       umma_bf16(d, adesc + 2, bdesc + 128, kIdesc, 1u);
                       umma_bf16(d, adesc + 4, bdesc + 256, kIdesc, 1u);
@@ -663,7 +683,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
     if constexpr (FUSED) regs_inc<256>();
     if constexpr (EPW == 8) regs_inc<GEMM_REGS_EPILOGUE_EPI8>();
     const int quarter = warp & 3;       // TMEM lane quarter this warp may access
-    const int chalf = (warp - 4) >> 2;  // EPW == 8: the 64-column half of every tile this warp takes
+    // EPW == 8: which of the two column sets of every tile this warp takes (bf16 roots: the
+    // 64-column half; SwiGLU roots: 32 gate and the matching 32 up columns)
+    const int chalf = (warp - 4) >> 2;
     // this warp's bf16 output staging: 8 KB per lane quarter, or 4 KB per warp with 8 warps
     uint8_t* const wstage = epi_stage + (EPW == 8 ? (warp - 4) * (32 * 128) : quarter * (32 * 256));
     const int row_in_tile = quarter * 32 + lane;
@@ -926,15 +948,15 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
 
 namespace {
 
-template <int EPI, bool PAIR, bool FUSED = false, int EPW = 4>
+template <int EPI, bool PAIR, bool FUSED = false, int EPW = 4, bool LS = false>
 iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
-                      cudaStream_t s) {
+                      cudaStream_t s, const CUtensorMap& tmA2) {
   constexpr int kThreads = FUSED ? GEMM_THREADS_FUSED : (EPW == 8 ? GEMM_THREADS_EPI8 : GEMM_THREADS);
   static int attr_dev = -1;  // device whose function attributes are set
   static int slots = 0;      // CTAs (pairs: clusters) resident at once on that device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
-  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED, EPW>;
+  auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED, EPW, LS>;
   if (attr_dev != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
       return ISO_ERR_CUDA;
@@ -966,7 +988,7 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
   const int units = max_units < slots ? max_units : slots;
   if (units <= 0) return ISO_OK;
   if (!PAIR) {
-    kern<<<units, kThreads, GEMM_SMEM_BYTES, s>>>(tmA, tmB, p);
+    kern<<<units, kThreads, GEMM_SMEM_BYTES, s>>>(tmA, tmB, tmA2, p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
@@ -980,7 +1002,7 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return ISO_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, p) != cudaSuccess) return ISO_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
@@ -988,32 +1010,38 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 }  // namespace
 
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
-                       cudaStream_t s) {
+                       cudaStream_t s, const CUtensorMap* tmA2) {
+  const CUtensorMap& a2 = tmA2 != nullptr ? *tmA2 : tmA;  // unused unless p.leaf_stage
+  if (p.leaf_stage) {
+    if (epi != EPI_BF16 || p.pair || p.a_transform || tmA2 == nullptr || p.leaf_len != LS_LEAF)
+      return ISO_ERR_INVALID_ARG;
+    return launch_one<EPI_BF16, false, false, 8, true>(tmA, tmB, p, max_units, s, a2);
+  }
   const bool pair = p.pair != 0;
   if (p.a_transform) {
     if (pair) return ISO_ERR_INVALID_ARG;
-    if (epi == EPI_BF16) return launch_one<EPI_BF16, false, true>(tmA, tmB, p, max_units, s);
-    if (epi == EPI_LOGPROB) return launch_one<EPI_LOGPROB, false, true>(tmA, tmB, p, max_units, s);
+    if (epi == EPI_BF16) return launch_one<EPI_BF16, false, true>(tmA, tmB, p, max_units, s, a2);
+    if (epi == EPI_LOGPROB) return launch_one<EPI_LOGPROB, false, true>(tmA, tmB, p, max_units, s, a2);
     return ISO_ERR_INVALID_ARG;
   }
   // short leaves: 8 epilogue warps (the expert layer's grouped GEMMs: 1.07 -> 0.94 ms per layer)
   switch (epi) {
     case EPI_BF16:
       if (!pair && p.leaf_len <= EPI8_MAX_LEAF_BF16)
-        return launch_one<EPI_BF16, false, false, 8>(tmA, tmB, p, max_units, s);
-      return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s)
-                  : launch_one<EPI_BF16, false>(tmA, tmB, p, max_units, s);
+        return launch_one<EPI_BF16, false, false, 8>(tmA, tmB, p, max_units, s, a2);
+      return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s, a2)
+                  : launch_one<EPI_BF16, false>(tmA, tmB, p, max_units, s, a2);
     case EPI_F32:
-      return pair ? launch_one<EPI_F32, true>(tmA, tmB, p, max_units, s)
-                  : launch_one<EPI_F32, false>(tmA, tmB, p, max_units, s);
+      return pair ? launch_one<EPI_F32, true>(tmA, tmB, p, max_units, s, a2)
+                  : launch_one<EPI_F32, false>(tmA, tmB, p, max_units, s, a2);
     case EPI_SWIGLU:
       if (!pair && p.leaf_len <= EPI8_MAX_LEAF_SWIGLU)
-        return launch_one<EPI_SWIGLU, false, false, 8>(tmA, tmB, p, max_units, s);
-      return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s)
-                  : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s);
+        return launch_one<EPI_SWIGLU, false, false, 8>(tmA, tmB, p, max_units, s, a2);
+      return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s, a2)
+                  : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s, a2);
     case EPI_LOGPROB:
-      return pair ? launch_one<EPI_LOGPROB, true>(tmA, tmB, p, max_units, s)
-                  : launch_one<EPI_LOGPROB, false>(tmA, tmB, p, max_units, s);
+      return pair ? launch_one<EPI_LOGPROB, true>(tmA, tmB, p, max_units, s, a2)
+                  : launch_one<EPI_LOGPROB, false>(tmA, tmB, p, max_units, s, a2);
     default:
       return ISO_ERR_INVALID_ARG;
   }

@@ -47,6 +47,11 @@ constexpr int GEMM_THREADS_FUSED = 384;      // + warps 8..11: the fused RMSNorm
 constexpr int GEMM_THREADS_EPI8 = 384;
 constexpr int EPI8_MAX_LEAF_SWIGLU = 256;
 constexpr int EPI8_MAX_LEAF_BF16 = 128;
+// Whole-leaf stages for leaves of 96 k: A 128 x 64 (16 KB) + 128 x 32 (8 KB), B 96 x 128 (24 KB).
+constexpr int LS_LEAF = 96;
+constexpr int LS_A2_OFF = BM * 64 * 2;            // the 32-column A box, after the 64-column one
+constexpr int LS_A_BYTES = BM * LS_LEAF * 2;      // 24 KB
+constexpr int LS_B_BYTES = LS_LEAF * BN * 2;      // 24 KB
 constexpr int GEMM_REGS_CONTROL_EPI8 = 104;   // setmaxnreg of warps 0-3 with 8 epilogue warps
 constexpr int GEMM_REGS_EPILOGUE_EPI8 = 200;  // and of warps 4-11
 static_assert(128 * GEMM_REGS_CONTROL_EPI8 + 256 * GEMM_REGS_EPILOGUE_EPI8 <= 384 * 168,
@@ -106,6 +111,10 @@ struct GemmParams {
   // [RL-Kernel blog, §6 table row 02; the same arithmetic as iso_rmsnorm], built in shared memory
   // by the producer warps from x [M x K] (leading dimension lda_src) instead of loaded by TMA
   int a_transform;
+  // whole-leaf stages (leaf_stage = 1, leaves of 96 k, single CTA, bf16 roots): a stage holds one
+  // leaf, A as a 64-column box (128-byte swizzle) and a 32-column box (64-byte swizzle, second
+  // tensor map), B as two 64-column x 96-row boxes; kb_per_leaf = 1
+  int leaf_stage;
   const void* a_src;      // x, bf16
   int64_t lda_src;
   const float* a_rinv;    // [M] per-row 1 / sqrt(mean x^2 + eps)
@@ -126,10 +135,14 @@ bool trace_enabled();
 // dimension ld (elements), box {box_cols, box_rows}, 128-byte swizzle.
 iso_status make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                           uint32_t box_cols, uint32_t box_rows);
+// The same with a 64-byte swizzle (boxes 32 columns wide).
+iso_status make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                               uint32_t box_cols, uint32_t box_rows);
 
 // Launchers (gemm_tcgen05.cu).  max_units bounds the number of CTAs (p.pair: CTA pairs)
 // worth launching; the grid is that or the number that fit on the GPU at once.
+// tmA2: the 32-column A boxes of whole-leaf stages (p.leaf_stage), else unused (may be null).
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
-                       cudaStream_t s);
+                       cudaStream_t s, const CUtensorMap* tmA2 = nullptr);
 
 }  // namespace iso
