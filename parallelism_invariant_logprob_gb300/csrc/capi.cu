@@ -193,11 +193,13 @@ int raster_group(const GemmParams& p, int K) {
 }
 
 // CTA pairs (M = 256 per MMA): units of 256 rows, 128-row A boxes, half the B tile per CTA.
-// A pair moves fewer bytes per MMA (more stages in flight), but the next tile's first leaves
-// wait at every tile boundary until both CTAs' epilogues have merged the last leaf (all four
-// TMEM buffers hold the tree there).  Measured on GB300: a win with leaves of 1536 k
-// (K = 12288, 8 leaves: 1317 -> 1469 TFLOP/s), a loss with leaves of 512 k or fewer.
-constexpr int kPairMinLeafLen = 1024;
+// A pair issues half the MMA instructions per SM and moves fewer bytes per MMA (more stages in
+// flight).  Its fixed cost is at every tile boundary: the next tile's first leaves wait until
+// both CTAs' epilogues have merged the last leaf (all four TMEM buffers hold the tree there).
+// Measured on GB300 (same-box A/B, bits identical): with leaves of 512 k the pairs win
+// (4096 x 4096 x 4096: 1188 -> 1409 TFLOP/s; 4096 x 4096 x 12288: 1350 -> 1596; the T = 4096
+// logprob 3.50 -> 3.01 ms); with 256 k they tie and with 128 k they lose (745 -> 668).
+constexpr int kPairMinLeafLen = 512;
 bool use_pair(int rows, int K, int L) { return rows > BM && K / L >= kPairMinLeafLen; }
 
 void set_pair(GemmParams& p, int rows) {

@@ -331,7 +331,7 @@ template <bool PAIR>
 __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int lane) {
   if (PAIR) {
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(cluster_addr(&buf_free[b], 0));
+    if (lane == 0) mbar_arrive_cluster_relaxed(cluster_addr(&buf_free[b], 0));
   } else {
     mbar_arrive(&buf_free[b]);
   }

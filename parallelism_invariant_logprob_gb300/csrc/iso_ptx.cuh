@@ -103,9 +103,14 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t ran
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's), with
+// relaxed ordering: for signals whose only meaning is "this thread's TMEM reads are complete"
+// (tcgen05.wait::ld has returned before the arrive, so the signal cannot overtake the reads), a
+// cluster-scope release would only add a wait for the thread's earlier global stores to become
+// visible cluster-wide.  Measured on GB300: that wait, paid at every TMEM buffer release, cost
+// CTA-pair GEMMs 15-19 % at 512-k leaves.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 // As mbar_wait, with acquire at cluster scope (for barriers the peer CTA arrives on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {

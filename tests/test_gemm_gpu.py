@@ -193,12 +193,12 @@ def test_sp_reduce_scatter_slices_equal_rows_of_iso_gemm(c8, R):
         assert same_bits(B.tree_combine(c8, S[:, r0:r1].contiguous()), full[r0:r1]), (R, q)
 
 
-@pytest.mark.parametrize("M", [129, 200, 257, 384])
-def test_cta_pair_units_ragged_exact(c8, M):
-    """Leaves of 1024 k (K = 8192, 8 leaves) run on CTA pairs: a unit is 256 rows, the
-    second CTA's 128 rows may be partly or wholly past M.  Exact integer inputs: the bits
-    must equal the oracle's, and every row must equal its single-row (one CTA) result."""
-    K, N = 8192, 136
+@pytest.mark.parametrize("M,K", [(129, 8192), (200, 8192), (257, 8192), (384, 8192), (129, 4096), (300, 4096)])
+def test_cta_pair_units_ragged_exact(c8, M, K):
+    """Leaves of 512 k and more (K = 4096 or 8192, 8 leaves) run on CTA pairs: a unit is 256
+    rows, the second CTA's 128 rows may be partly or wholly past M.  Exact integer inputs: the
+    bits must equal the oracle's, and every row must equal its single-row (one CTA) result."""
+    N = 136
     A = inputs.small_int_bf16((M, K), -3, 3, seed=M)
     Bm = inputs.small_int_bf16((K, N), -3, 3, seed=N + M)
     Ad, Bd = A.to(DEV), Bm.to(DEV)
@@ -211,7 +211,7 @@ def test_cta_pair_units_ragged_exact(c8, M):
 
 def test_cta_pair_normal_inputs_and_partials(c8):
     """Normal inputs through CTA pairs: tolerance against the oracle on sampled rows, and
-    the R-rank partial + combine path (also on pairs while K / (8 / R) >= 1024) reproduces the
+    the R-rank partial + combine path (also on pairs while K / (8 / R) >= 512) reproduces the
     single pass bit for bit."""
     M, K, N = 300, 8192, 256
     A, Bm = inputs.gemm_inputs(M, K, N, seed=4)
