@@ -209,6 +209,19 @@ def test_cta_pair_units_ragged_exact(c8, M, K):
         assert same_bits(B.gemm(c8, Ad[r:r + 1].contiguous(), Bd), C[r:r + 1]), r
 
 
+def test_cta_pair_repeatable_many_tiles(c8):
+    """Many 256-row tiles per CTA pair (K = 4096, 512-k leaves): repeated launches give the
+    same bits, and rows equal their one-CTA results (guards the pair's TMEM-buffer release
+    protocol, where a race would show as tiles that differ between runs)."""
+    M, K, N = 2048, 4096, 2048
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=41, device=DEV)
+    base = B.gemm(c8, A, Bm)
+    for _ in range(3):
+        assert same_bits(B.gemm(c8, A, Bm), base)
+    for r in (0, 255, 256, 1029, 2047):
+        assert same_bits(B.gemm(c8, A[r:r + 1].contiguous(), Bm), base[r:r + 1]), r
+
+
 def test_cta_pair_normal_inputs_and_partials(c8):
     """Normal inputs through CTA pairs: tolerance against the oracle on sampled rows, and
     the R-rank partial + combine path (also on pairs while K / (8 / R) >= 512) reproduces the
