@@ -448,7 +448,8 @@ def secondary(c, dev, stream, peaks, rank):
     ids_m, w_m = B.moe_route(c, logits, k)
     om = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     wsm = torch.empty(B.grouped_gemm_moe_workspace(c, T, E, k, H, F), dtype=torch.uint8, device=dev)
-    tt = time_call(lambda: B.grouped_gemm_moe(c, xm, ids_m, w_m, W1, W2, out=om, ws=wsm, stream=stream), 3, 1, stream)
+    tt = time_call(lambda: B.grouped_gemm_moe(c, xm, ids_m, w_m, W1, W2, out=om, ws=wsm, stream=stream), 10, 3, stream,
+                   flush)
     fl = 2.0 * T * k * (H * 2 * F + F * H)
     out["moe"] = dict(workload="T=8192, H=2048, E=128, F=768, k=8", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
                       roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3))
