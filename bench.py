@@ -34,7 +34,9 @@ sys.path.insert(0, ROOT)
 SHAPES = [(4096, 4096), (4096, 12288), (12288, 4096)]  # (K, N)
 M_TOKENS = 4096
 LEAVES = 8
-E2E_CHUNKS = 2  # row chunks per shape in the end-to-end pipeline (GB300: 1 -> 705, 2 -> 778, 4 -> 735, 8 -> 555 TFLOP/s)
+# row chunks per shape in the end-to-end pipeline (measured on GB300: 1 chunk 705, 2 chunks 778,
+# 4 chunks 735, 8 chunks 555 TFLOP/s)
+E2E_CHUNKS = 2
 METRIC = "invariant GEMM TFLOP/s & logprob tokens/s on 1 GB300; % of roofline; bitwise checks"
 WORKLOAD = ("dense projection GEMMs of an 8B-class decoder: M=4096 tokens, (K,N) in "
             "{(4096,4096),(4096,12288),(12288,4096)}, bf16 in / fp32 accumulate / bf16 out, 8 contiguous K-leaves, "
