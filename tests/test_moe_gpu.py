@@ -96,7 +96,9 @@ def _layer(c, x, ids, w, W1, W2, part=None):
     return B.grouped_gemm_moe(c, x, ids, w, W1, W2, expert_partition=part)
 
 
-@pytest.mark.parametrize("T,H,E,F,k", [(64, 256, 8, 128, 4), (200, 512, 16, 256, 8)])
+# the third case has F = 768 (down-projection leaves of 96 k: whole-leaf stages) with experts of
+# zero to a few rows
+@pytest.mark.parametrize("T,H,E,F,k", [(64, 256, 8, 128, 4), (200, 512, 16, 256, 8), (17, 256, 16, 768, 4)])
 def test_layer_vs_oracle(c8, T, H, E, F, k):
     x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=T)
     ids, w = B.moe_route(c8, logits.to(DEV), k)
