@@ -34,9 +34,10 @@ sys.path.insert(0, ROOT)
 SHAPES = [(4096, 4096), (4096, 12288), (12288, 4096)]  # (K, N)
 M_TOKENS = 4096
 LEAVES = 8
-# row chunks per shape in the end-to-end pipeline (measured on GB300: 1 chunk 705, 2 chunks 778,
-# 4 chunks 735, 8 chunks 555 TFLOP/s)
-E2E_CHUNKS = 2
+# row chunks of each shape in the end-to-end pipeline, in order.  Measured on GB300: equal chunks
+# 1 -> 705, 2 -> 762-781, 4 -> 735, 8 -> 555 TFLOP/s; smaller first and last chunks (1024 or 512
+# rows) 702-758)
+E2E_SPLITS = [[2048, 2048], [2048, 2048], [2048, 2048]]
 METRIC = "invariant GEMM TFLOP/s & logprob tokens/s on 1 GB300; % of roofline; bitwise checks"
 WORKLOAD = ("dense projection GEMMs of an 8B-class decoder: M=4096 tokens, (K,N) in "
             "{(4096,4096),(4096,12288),(12288,4096)}, bf16 in / fp32 accumulate / bf16 out, 8 contiguous K-leaves, "
@@ -263,7 +264,7 @@ def run_ours(args, rank, world):
                                       for i, (K, N) in enumerate(SHAPES)})
 
     # end to end through the C ABI with host buffers: H2D of the step's activations, D2H of its
-    # outputs, pipelined over three streams in row chunks of E2E_CHUNKS per shape: the next
+    # outputs, pipelined over three streams in the row chunks of E2E_SPLITS: the next
     # chunk's activations upload while the GEMM of the current chunk runs, and each chunk's
     # outputs download as soon as its GEMM is done, so both copy directions and the tensor cores
     # work at once and only the last chunk's GEMM and download follow the last upload.  A row's
@@ -282,9 +283,9 @@ def run_ours(args, rank, world):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s_in)
         for i in range(len(SHAPES)):
-            rows = M_TOKENS // E2E_CHUNKS
-            for j in range(E2E_CHUNKS):
-                r0, r1 = j * rows, (j + 1) * rows
+            r1 = 0
+            for rows in E2E_SPLITS[i]:
+                r0, r1 = r1, r1 + rows
                 with torch.cuda.stream(s_in):
                     Xs[i][r0:r1].copy_(pinned_x[i][r0:r1], non_blocking=True)
                 landed = torch.cuda.Event()
