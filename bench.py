@@ -36,7 +36,7 @@ M_TOKENS = 4096
 LEAVES = 8
 # row chunks of each shape in the end-to-end pipeline, in order.  Measured on GB300: equal chunks
 # 1 -> 705, 2 -> 762-781, 4 -> 735, 8 -> 555 TFLOP/s; smaller first and last chunks (1024 or 512
-# rows) 702-758)
+# rows) 702-758.
 E2E_SPLITS = [[2048, 2048], [2048, 2048], [2048, 2048]]
 METRIC = "invariant GEMM TFLOP/s & logprob tokens/s on 1 GB300; % of roofline; bitwise checks"
 WORKLOAD = ("dense projection GEMMs of an 8B-class decoder: M=4096 tokens, (K,N) in "
