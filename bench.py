@@ -388,6 +388,32 @@ def secondary(c, dev, stream, peaks, rank):
                         5, 2, stream, flush)
     out["logprob"]["rmsnorm_fused"] = dict(workload="iso_rmsnorm + iso_selected_logprob vs iso_rmsnorm_selected_logprob, "
                                                     "T=4096, H=4096, V=151936", ms_separate=t_sep, ms_fused=t_fused)
+    # vocab-parallel logprob: R chunk-aligned vocabulary shards (one per simulated rank, each timed
+    # on its own shard of W), then the combine over the rank-ordered statistics; one rank's time is
+    # its partial, the job's the slowest partial plus the combine
+    vp = {}
+    chunk_cols = 19 * 128
+    for R in (2, 4):
+        v0s = [int(round(LP_V * r / R / chunk_cols)) * chunk_cols for r in range(R)]
+        bounds = v0s + [LP_V]
+        parts, stats, zs = [], [], []
+        for r in range(R):
+            v0, v1 = bounds[r], bounds[r + 1]
+            Wr = W[:, v0:v1]
+            ws_r = torch.empty(max(int(c.lib.iso_selected_logprob_partial_workspace(c.handle, LP_T, v1 - v0)), 16),
+                               dtype=torch.uint8, device=dev)
+            s_r, z_r = B.selected_logprob_partial(c, h, Wr, ids, LP_V, v0, ws=ws_r, stream=stream)
+            parts.append(time_call(lambda: B.selected_logprob_partial(c, h, Wr, ids, LP_V, v0, stats_r=s_r, zsel_r=z_r,
+                                                                       ws=ws_r, stream=stream), 3, 1, stream, flush))
+            stats.append(s_r)
+            zs.append(z_r)
+        st_all, z_all = torch.cat(stats, 0), torch.stack(zs)
+        t_comb = time_call(lambda: B.selected_logprob_combine(c, v0s, st_all, z_all, ids, LP_V, out=lp_out, stream=stream),
+                           5, 2, stream, flush)
+        vp[f"R{R}"] = dict(shard_v0=v0s, ms_partial_max=max(parts), ms_partial_min=min(parts), ms_combine=t_comb,
+                           ms_single_call_over_R=t / R,
+                           same_bits_as_single_call=bool(torch.equal(lp_out, B.selected_logprob(c, h, W, ids))))
+    out["logprob"]["vocab_parallel"] = vp
     del h, W, ids, ws, xr, hn, ws_f
 
     # GEMM at small M (weight-streaming, HBM-bound) and the cuBLAS non-invariant reference
