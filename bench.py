@@ -489,6 +489,23 @@ def secondary(c, dev, stream, peaks, rank):
     fl = 2.0 * T * k * (H * 2 * F + F * H)
     out["moe"] = dict(workload="T=8192, H=2048, E=128, F=768, k=8", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
                       roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3))
+    # expert parallelism: R ranks own contiguous expert sets; a rank's time is its partial (the slot
+    # rows of its experts), the job's the slowest partial plus the combine after the exchange
+    ep = {}
+    ys = torch.empty(T * k, H, dtype=torch.bfloat16, device=dev)
+    ws_p = torch.empty(B.moe_experts_partial_workspace(c, T, E, k, H, F), dtype=torch.uint8, device=dev)
+    for R in (2, 4):
+        parts = []
+        for r in range(R):
+            mask = [e * R // E == r for e in range(E)]
+            parts.append(time_call(lambda: B.moe_experts_partial(c, xm, ids_m, W1, W2, mask, y_slots=ys, ws=ws_p,
+                                                                  stream=stream), 5, 2, stream, flush))
+        t_comb = time_call(lambda: B.moe_combine(c, ys.view(T, k, H), w_m, out=om, stream=stream), 5, 2, stream, flush)
+        ep[f"R{R}"] = dict(ms_partial_max=max(parts), ms_partial_min=min(parts), ms_combine=t_comb,
+                           ms_layer_over_R=tt / R,
+                           same_bits_as_layer=bool(torch.equal(om.view(torch.int16), B.grouped_gemm_moe(
+                               c, xm, ids_m, w_m, W1, W2, ws=wsm, stream=stream).view(torch.int16))))
+    out["moe"]["expert_parallel"] = ep
     return out
 
 
