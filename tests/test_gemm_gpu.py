@@ -276,9 +276,13 @@ def test_config2_full_size_m4096_sampled(c8):
     assert same_bits(B.gemm(c8, A[1:65].contiguous(), Bm), full[1:65])
 
 
-def test_canary_guard_bands(c8):
+# the three store paths of the bf16 epilogue: 8 warps on one CTA (leaves of 64 k), 4 warps on one
+# CTA (16 rows, 256-k leaves, unstaged stores), and CTA pairs (300 rows, 512-k leaves, the second
+# CTA of the last pair partly past M)
+@pytest.mark.parametrize("M,K", [(70, 512), (16, 2048), (300, 4096)])
+def test_canary_guard_bands(c8, M, K):
     """Output written exactly inside its [M x N] window of a wider ldc buffer."""
-    M, N, K, ldc = 70, 136, 512, 264
+    N, ldc = 136, 264
     A, Bm = inputs.gemm_inputs(M, K, N, seed=4)
     buf = torch.full((M + 2, ldc), 7.0, dtype=torch.bfloat16, device=DEV)
     out = buf[1:M + 1]
