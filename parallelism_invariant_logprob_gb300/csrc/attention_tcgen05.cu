@@ -54,7 +54,7 @@ iso_status make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, ui
 namespace {
 
 constexpr int AT_ROWS = 128;    // query rows per tile (the MMA's M)
-constexpr int AT_KEYS = 80;     // keys per chunk (N of Q K^T, K of P V)
+constexpr int AT_KEYS = ATT_CHUNK_KEYS;  // keys per chunk (N of Q K^T, K of P V)
 constexpr int AT_D = 128;       // head dimension
 constexpr int AT_STAGES = 4;    // K / V ring depth (chunk c in stage c % 4)
 constexpr int AT_THREADS = 512;  // 4 warpgroups
@@ -113,7 +113,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-constexpr float kLazy = 8.0f;  // base-2 headroom before the running maximum moves
+constexpr float kLazy = ATT_LAZY_LOG2;  // base-2 headroom before the running maximum moves
 constexpr float kLn2 = 0.693147180559945309f;
 
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A: 128 lanes (rows) x K, two bf16 per

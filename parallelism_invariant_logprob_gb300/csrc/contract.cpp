@@ -17,7 +17,7 @@
 
 #include <string>
 
-#include "../../include/iso.h"
+#include "iso_internal.h"
 
 struct iso_contract {
   int leaf_count;
@@ -113,8 +113,13 @@ void sha256(const uint8_t* data, size_t n, uint8_t out[32]) {
 
 const char* dtype_name(iso_dtype d) { return d == ISO_F32 ? "fp32" : "bf16"; }
 
-// Canonical serialization: fixed field order, no whitespace.  Every constant
-// that can change an output bit appears here; nothing else does.
+// Canonical serialization: fixed field order, no whitespace.  Every constant and every
+// rounding step that can change an output bit appears here, written as the kernels execute
+// it: `__fadd_rn` etc. are the IEEE round-to-nearest-even fp32 operations (never contracted),
+// `expf` / `logf` are CUDA's math library functions of the toolkit named under "impl",
+// `__expf` / `__fdividef` / `ex2.approx.ftz` are the hardware approximations.  The numbers come
+// from the same constants the kernels are compiled with (iso_internal.h), so a kernel change
+// of a tile width, chunk size or merge threshold changes the digest.
 std::string serialize(const iso_contract& c) {
   char claim[64];
   int n = 0;
@@ -122,32 +127,46 @@ std::string serialize(const iso_contract& c) {
   for (int r = 1; r <= c.leaf_count; r *= 2) n += snprintf(claim + n, sizeof claim - n, r == 1 ? "%d" : ",%d", r);
   claim[n++] = ']';
   claim[n] = 0;
-  char buf[2048];
+  char buf[4096];
   snprintf(buf, sizeof buf,
-           "{\"identity\":\"numerical_policy\",\"contract_version\":1,"
-           "\"impl\":{\"id\":\"iso_leaf_tree_tcgen05\",\"version\":2,\"arch\":\"sm_103a\"},"
+           "{\"identity\":\"numerical_policy\",\"contract_version\":2,"
+           "\"impl\":{\"id\":\"iso_leaf_tree_tcgen05\",\"version\":3,\"arch\":\"sm_103a\",\"cuda\":\"%d.%d\"},"
            "\"gemm\":{\"leaves\":%d,\"rank_to_leaf\":\"contiguous\","
-           "\"leaf_chain\":{\"instr\":\"tcgen05.mma.kind::f16\",\"rows_per_cta\":128,"
-           "\"cta_group\":\"1(m=128)|2(m=256)\",\"n\":128,\"k\":16,"
+           "\"leaf_chain\":{\"instr\":\"tcgen05.mma.kind::f16\",\"rows_per_cta\":%d,"
+           "\"cta_group\":\"1(m=128)|2(m=256)\",\"n\":%d,\"k\":%d,"
            "\"order\":\"ascending_k\",\"first\":\"overwrite\"},"
-           "\"tree\":\"%s\",\"tree_add\":\"fp32_rn\",\"acc_dtype\":\"%s\",\"out_dtype\":\"%s\","
-           "\"convert\":\"once_at_root_rn\"},"
+           "\"tree\":\"%s\",\"tree_add\":\"__fadd_rn\",\"acc_dtype\":\"%s\",\"out_dtype\":\"%s\","
+           "\"convert\":\"once_at_root_bf16_rn\"},"
            "\"claims\":{\"topology\":{\"simulated_ranks\":%s}},"
-           "\"logprob\":{\"logit\":\"tree_root_fp32_unrounded\",\"tile_cols\":128,\"chunk_tiles\":19,"
-           "\"tile_stat\":\"max;ascending_sum_expf(z-m)_fp32_rn\","
+           "\"logprob\":{\"logit\":\"tree_root_fp32_unrounded\",\"tile_cols\":%d,\"chunk_tiles\":%d,"
+           "\"tile_stat\":\"m=max;s=ascending_columns(__fadd_rn(s,expf(__fsub_rn(z,m))))\","
            "\"chunk_fold\":\"left_to_right_two_block_merge\",\"chunk_tree\":\"pairwise_odd_carried\","
-           "\"merge\":\"m=fmaxf;s=rn(rn(s1*expf(m1-m))+rn(s2*expf(m2-m)))\",\"lse\":\"m+logf(s)\","
-           "\"out\":\"rn(z_sel-lse)\",\"vocab_parallel\":\"contiguous_chunk_aligned_shards_in_rank_order\"},"
+           "\"merge\":\"m=fmaxf(m1,m2);s=__fadd_rn(__fmul_rn(s1,expf(__fsub_rn(m1,m))),"
+           "__fmul_rn(s2,expf(__fsub_rn(m2,m))))\",\"lse\":\"__fadd_rn(m,logf(s))\","
+           "\"out\":\"__fsub_rn(z_sel,lse)\",\"vocab_parallel\":\"contiguous_chunk_aligned_shards_in_rank_order\"},"
            "\"rmsnorm\":{\"map\":\"warp_per_row;lane_owns_8_element_vectors_v_mod_32\","
-           "\"lane_sum\":\"ascending_rn(acc+rn(x*x))\",\"tree\":\"shfl_xor_16_8_4_2_1\","
-           "\"scale\":\"rn(1/sqrt_rn(rn(ss/H)+eps))\",\"out\":\"bf16_rn(rn(rn(x*r)*gamma))\"},"
-           "\"moe\":{\"route\":\"topk_logit_desc_id_asc\",\"gates\":\"expf(l-l0)/ascending_sum_fp32_rn\","
-           "\"stages\":[\"gate_up_root_bf16\",\"silu(g)=g/(1+expf(-g));h=bf16_rn(silu*u)\",\"down_root_bf16\"],"
-           "\"combine\":{\"order\":\"routing_slot\",\"leaf\":\"rn(w*y)_fp32\",\"tree\":\"balanced_binary\","
+           "\"lane_sum\":\"ascending(__fadd_rn(acc,__fmul_rn(x,x)))\",\"tree\":\"shfl_xor_16_8_4_2_1\","
+           "\"scale\":\"__fdiv_rn(1,__fsqrt_rn(__fadd_rn(__fdiv_rn(ss,H),eps)))\","
+           "\"out\":\"bf16_rn(__fmul_rn(__fmul_rn(x,r),gamma))\"},"
+           "\"moe\":{\"route\":\"topk_logit_desc_id_asc\","
+           "\"gates\":\"__fdiv_rn(expf(__fsub_rn(l,l0)),slot_order(__fadd_rn))\","
+           "\"stages\":[\"gate_up_root_bf16_rn\","
+           "\"h=bf16_rn(__fmul_rn(__fdividef(g,__fadd_rn(1,__expf(-g))),u))\",\"down_root_bf16_rn\"],"
+           "\"combine\":{\"order\":\"routing_slot\",\"leaf\":\"__fmul_rn(w,y)\",\"tree\":\"balanced_binary\","
            "\"out\":\"bf16_rn\"}},"
-           "\"math\":{\"exp\":\"expf\",\"log\":\"logf\",\"fast_math\":false,\"fma_contraction\":false}}",
-           c.leaf_count, c.schedule == ISO_TREE_BALANCED_BINARY ? "balanced_binary_left_lower_index" : "?",
-           dtype_name(c.acc_dtype), dtype_name(c.out_dtype), claim);
+           "\"attention\":{\"kv_split\":\"none\",\"chunk_keys\":%d,\"chunk_order\":\"ascending\","
+           "\"qk\":\"tcgen05.mma.kind::f16,m=128,n=%d,k=16,ascending_dims\",\"c2\":\"fp32_rn(scale*log2(e))\","
+           "\"t\":\"__fmul_rn(chunk_max(S),c2)\",\"lazy_log2\":%g,"
+           "\"m\":\"t_if_first_chunk_or_t>m+lazy_else_m\",\"p\":\"ex2.approx.ftz(__fmaf_rn(S,c2,-m))\","
+           "\"p_operand\":\"bf16_rn\",\"l_chunk\":\"4_partials_key_mod_4(__fadd_rn);(p0+p1)+(p2+p3)\","
+           "\"a\":\"ex2.approx.ftz(__fsub_rn(m_old,m))\",\"l\":\"__fadd_rn(__fmul_rn(l,a),l_chunk)\","
+           "\"o_rescale\":\"__fmul_rn(O,a)\",\"pv\":\"tcgen05.mma.kind::f16,m=128,n=128,k=16,ascending_keys\","
+           "\"out\":\"bf16_rn(__fmul_rn(O,__frcp_rn(l)))\",\"lse\":\"__fadd_rn(__fmul_rn(m,fp32(ln2)),logf(l))\"},"
+           "\"math\":{\"fp32_add_mul\":\"rn_intrinsics_never_contracted\",\"libm\":\"cuda_toolkit_expf_logf\"}}",
+           CUDART_VERSION / 1000, (CUDART_VERSION % 1000) / 10, c.leaf_count, iso::BM, iso::BN, iso::UMMA_K,
+           c.schedule == ISO_TREE_BALANCED_BINARY ? "balanced_binary_left_lower_index" : "?",
+           dtype_name(c.acc_dtype), dtype_name(c.out_dtype), claim, iso::LP_TILE_COLS, iso::LP_CHUNK_TILES,
+           iso::ATT_CHUNK_KEYS, iso::ATT_CHUNK_KEYS, static_cast<double>(iso::ATT_LAZY_LOG2));
   return std::string(buf);
 }
 
@@ -162,7 +181,7 @@ iso_status iso_contract_init(int leaf_count, iso_tree_schedule schedule, iso_dty
   if (!out) return ISO_ERR_INVALID_ARG;
   *out = nullptr;
   if (!is_pow2(leaf_count)) return ISO_ERR_INVALID_ARG;
-  if (leaf_count > 8) return ISO_ERR_UNSUPPORTED;
+  if (leaf_count > iso::MAX_LEAVES) return ISO_ERR_UNSUPPORTED;
   if (schedule != ISO_TREE_BALANCED_BINARY) return ISO_ERR_UNSUPPORTED;
   if (acc_dtype != ISO_F32) return ISO_ERR_UNSUPPORTED;
   if (out_dtype != ISO_BF16) return ISO_ERR_UNSUPPORTED;

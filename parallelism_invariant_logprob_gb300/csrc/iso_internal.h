@@ -68,6 +68,11 @@ constexpr int EPI_STAGE_BYTES = 4 * 32 * BN * 2;  // 4 epilogue warps x 32 rows 
 constexpr int LP_TILE_COLS = BN;
 constexpr int LP_CHUNK_TILES = 19;
 
+// Attention merge grid: keys in fixed chunks of 80 per sequence, merged in ascending order; the
+// running maximum (base 2) moves only when a chunk's maximum exceeds it by more than 8.
+constexpr int ATT_CHUNK_KEYS = 80;
+constexpr float ATT_LAZY_LOG2 = 8.0f;
+
 enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2, EPI_SWIGLU = 3 };
 enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2, UNIT_LEAF_SPLIT = 3 };
 

@@ -61,6 +61,67 @@ def test_contract_digest_is_sha256_of_serialization(lib):
     assert B.Contract(8, lib).digest == digests[8]  # deterministic
 
 
+def _leaves(obj, path=()):
+    if isinstance(obj, dict):
+        for k, v in obj.items():
+            yield from _leaves(v, path + (k,))
+    elif isinstance(obj, list) and obj and not all(isinstance(v, int) for v in obj):
+        for i, v in enumerate(obj):
+            yield from _leaves(v, path + (i,))
+    else:
+        yield path, obj
+
+
+def _set(obj, path, value):
+    for k in path[:-1]:
+        obj = obj[k]
+    obj[path[-1]] = value
+
+
+def _header_constant(name):
+    src = open(os.path.join(ROOT, "parallelism_invariant_logprob_gb300", "csrc", "iso_internal.h")).read()
+    m = re.search(r"constexpr (?:int|float) " + name + r" = ([0-9.]+)f?;", src)
+    assert m, name
+    return float(m.group(1))
+
+
+def test_contract_serialization_names_the_executed_numerics(lib):
+    """Each kernel family has its block, the block's constants are the ones the kernels are
+    compiled with, the stated arithmetic is the one in the kernel source (the fast SiLU
+    intrinsics, attention's base-2 approximate exponent), and every value is covered by the
+    digest (IsoExec blog, "Unified execution contract": equal identities mean equal numerics)."""
+    c = B.Contract(8, lib)
+    s = c.serialize()
+    obj = json.loads(s)
+    for block in ("impl", "gemm", "claims", "logprob", "rmsnorm", "moe", "attention", "math"):
+        assert block in obj, block
+    assert obj["gemm"]["leaf_chain"]["n"] == 128 and obj["gemm"]["leaf_chain"]["k"] == 16
+    assert obj["logprob"]["tile_cols"] == 128
+    assert obj["logprob"]["chunk_tiles"] == _header_constant("LP_CHUNK_TILES")
+    assert obj["attention"]["chunk_keys"] == _header_constant("ATT_CHUNK_KEYS")
+    assert obj["attention"]["lazy_log2"] == _header_constant("ATT_LAZY_LOG2")
+    assert "fast_math" not in obj["math"]
+    # the SiLU and the attention exponent as the kernel sources write them
+    csrc = os.path.join(ROOT, "parallelism_invariant_logprob_gb300", "csrc")
+    gemm_src = open(os.path.join(csrc, "gemm_tcgen05.cu")).read()
+    assert "__fdividef(g, __fadd_rn(1.0f, __expf(-g)))" in gemm_src
+    assert "h=bf16_rn(__fmul_rn(__fdividef(g,__fadd_rn(1,__expf(-g))),u))" in obj["moe"]["stages"]
+    att_src = open(os.path.join(csrc, "attention_tcgen05.cu")).read()
+    assert "ex2.approx.ftz.f32" in att_src and "__fmaf_rn(u2f(v[j]), c2, neg_m)" in att_src
+    assert obj["attention"]["p"] == "ex2.approx.ftz(__fmaf_rn(S,c2,-m))"
+    assert "__frcp_rn(l)" in att_src and "__frcp_rn(l)" in obj["attention"]["out"]
+    # the serialization is canonical JSON, and changing any one value changes the digest
+    assert json.dumps(obj, separators=(",", ":")) == s
+    assert hashlib.sha256(s.encode()).digest() == c.digest
+    n = 0
+    for path, v in _leaves(obj):
+        mutated = json.loads(s)
+        _set(mutated, path, v + 1 if isinstance(v, (int, float)) and not isinstance(v, bool) else str(v) + "'")
+        assert hashlib.sha256(json.dumps(mutated, separators=(",", ":")).encode()).digest() != c.digest, path
+        n += 1
+    assert n >= 50
+
+
 def test_contract_init_rejects(lib):
     h = ctypes.c_void_p()
     assert lib.iso_contract_init(3, 0, B.ISO_F32, B.ISO_BF16, ctypes.byref(h), None) == 1
@@ -136,3 +197,19 @@ def test_host_validation_launches_nothing(lib):
 def test_status_strings(lib):
     for s in range(12):
         assert lib.iso_status_string(s)
+
+
+def test_static_scratch_limit_on_host(lib):
+    """The allocation-free logprob entry point accepts exactly the problems whose minimum
+    workspace fits its fixed 8 MiB array (16,512 tokens at V = 151936) and rejects the next
+    size on the host, before any device call (so this runs without a GPU)."""
+    c = B.Contract(8, lib)
+    V, cap = 151936, 8 << 20
+    mw = lambda T: int(lib.iso_selected_logprob_min_workspace(c.handle, T, V))
+    assert mw(16512) <= cap < mw(16513)
+    al = lambda x: (x + 255) // 256 * 256
+    assert mw(16512) == al(16512 * 63 * 8) + al(16512 * 4)  # 63 chunks of (m, s) pairs + z_sel
+    assert int(lib.iso_selected_logprob_workspace(c.handle, 820, V)) <= cap
+    assert int(lib.iso_selected_logprob_workspace(c.handle, 840, V)) > cap
+    st = lib.iso_selected_logprob_static_scratch(c.handle, None, None, None, None, 16513, 128, V, None)
+    assert st == 7  # ISO_ERR_WORKSPACE
