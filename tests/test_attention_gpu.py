@@ -166,6 +166,100 @@ def test_attention_argument_errors(c8):
     assert lib.iso_last_device_status(s) == B.ISO_OK
 
 
+def _ramp_keys(K, ks, a):
+    """Key j of each sequence (j counted from the sequence's first key) scaled by 1 + a j / 80, then
+    rounded to bf16: the chunk maxima of the scores grow along the sequence, so the running
+    maximum of the chunk merge has to move after chunk 0 (input generation only)."""
+    Kf = K.float().clone()
+    for b in range(ks.numel() - 1):
+        k0, k1 = int(ks[b]), int(ks[b + 1])
+        j = torch.arange(k1 - k0, dtype=torch.float32)
+        Kf[k0:k1] *= (1.0 + a * j / 80.0)[:, None, None]
+    return Kf.to(torch.bfloat16)
+
+
+def _lazy_moves(Q, K, qs, ks, p0, Hq, Hkv):
+    """CPU replay of the merge's lazy maximum, for every (query row, head): the number of chunks
+    after chunk 0 at which the running maximum moves.  The kernel's rule: t_c = the chunk's largest
+    visible score times c2 = fp32(scale log2 e); m starts at t_0 and moves to t_c only when
+    t_c > m + 8.  Scores are taken in float64 here, so a decision within rounding distance of the
+    threshold may differ from the kernel's; the counts are only used in aggregate."""
+    G = Hq // Hkv
+    c2 = np.float32(np.float32(SCALE) * np.float32(math.log2(math.e)))
+    out = []
+    Qd, Kd = Q.double().numpy(), K.double().numpy()
+    for b in range(qs.numel() - 1):
+        q0, q1, k0 = int(qs[b]), int(qs[b + 1]), int(ks[b])
+        if q1 == q0:
+            continue
+        pos = int(p0[b]) + np.arange(q1 - q0)
+        nk = int(pos[-1]) + 1
+        nc = (nk + 79) // 80
+        Kh = np.repeat(Kd[k0:k0 + nk], G, axis=1)                    # [keys, Hq, d]
+        S = np.einsum("rhd,khd->rhk", Qd[q0:q1], Kh)                  # [rows, Hq, keys]
+        S = np.where(np.arange(nk)[None, None, :] > pos[:, None, None], -np.inf, S)
+        S = np.concatenate([S, np.full(S.shape[:2] + (nc * 80 - nk,), -np.inf)], axis=2)
+        t = (S.reshape(S.shape[0], Hq, nc, 80).max(axis=3).astype(np.float32) * c2).astype(np.float64)
+        m = t[:, :, 0].copy()
+        moves = np.zeros(m.shape, np.int64)
+        for c in range(1, nc):
+            mv = t[:, :, c] > m + 8.0
+            m = np.where(mv, t[:, :, c], m)
+            moves += mv
+        out.append(moves)
+    return np.concatenate(out, axis=0)
+
+
+def _decode_row_equals_prefill(c, Qd, Kd, Vd, k0, r, pos, out, lse, row):
+    one = torch.tensor([0, 1], dtype=torch.int32, device=DEV)
+    kv = torch.tensor([0, pos + 1], dtype=torch.int32, device=DEV)
+    o1, l1 = B.attention(c, Qd[row:row + 1].contiguous(), Kd[k0:k0 + pos + 1].contiguous(),
+                         Vd[k0:k0 + pos + 1].contiguous(), one, kv, torch.tensor([pos], dtype=torch.int32, device=DEV),
+                         SCALE)
+    return _same_bits(o1[0], out[row]) and torch.equal(l1[0], lse[row])
+
+
+def test_attention_lazy_rescale_vs_oracle(c8):
+    """Rows whose running maximum moves by more than 8 (base 2) after chunk 0, many of them in
+    several chunks: the O and l rescale of the merge runs, and its results must still match the
+    plain softmax of the oracle and be the same bits in a one-row decode call.
+    (RL-Kernel blog, §4 "Causal Chain: How Block Merge Order Alters LSE": the rescale-merge.)"""
+    Hq, Hkv = 8, 2
+    lens = [300, 700, 1200]
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs(lens, [0, 0, 0], Hq, Hkv, D, seed=31)
+    K = _ramp_keys(K, ks, 1.5)
+    moves = _lazy_moves(Q, K, qs, ks, p0, Hq, Hkv)
+    assert (moves >= 1).mean() > 0.6 and (moves >= 2).mean() > 0.4 and moves.max() >= 5
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    many = np.nonzero(moves.max(axis=1) >= 3)[0]
+    g = torch.Generator().manual_seed(32)
+    pick = many[torch.randint(0, many.size, (10,), generator=g).numpy()].tolist() + [299, 999, 2199]
+    for row in pick:
+        b = int(np.searchsorted(qs.numpy(), row, side="right")) - 1
+        pos = row - int(qs[b])
+        assert _decode_row_equals_prefill(c8, Qd, Kd, Vd, int(ks[b]), row, pos, out, lse, row), row
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
+def test_attention_lazy_rescale_long_sequence(c8):
+    """The last rows of a 4096-key sequence (52 chunks, a KV cache before the rows) with keys
+    ramped so the maximum keeps moving, next to a short sequence in the same call: within the
+    oracle's bounds, and decode = prefill bit for bit."""
+    Hq, Hkv = 4, 1
+    Q, K, V, qs, ks, p0 = inputs.attention_inputs([8, 90], [4088, 0], Hq, Hkv, D, seed=33)
+    K = _ramp_keys(K, ks, 0.4)
+    moves = _lazy_moves(Q, K, qs, ks, p0, Hq, Hkv)
+    assert moves[:8].min() >= 1 and moves[:8].max() >= 4
+    out, lse = _run(c8, Q, K, V, qs, ks, p0)
+    _check_vs_oracle(out, lse, Q, K, V, qs, ks, p0)
+    Qd, Kd, Vd = Q.to(DEV), K.to(DEV), V.to(DEV)
+    for row in (0, 3, 7):
+        assert _decode_row_equals_prefill(c8, Qd, Kd, Vd, 0, row, 4088 + row, out, lse, row), row
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
 @pytest.mark.slow
 def test_attention_full_size_sampled(c8):
     """The bench's workload (packed prefill, 4096 query rows in 4 sequences of 1024, 32 query

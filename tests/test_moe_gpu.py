@@ -111,6 +111,45 @@ def test_layer_vs_oracle(c8, T, H, E, F, k):
     assert B.last_device_status(c8) == B.ISO_OK
 
 
+def _check_slot_rows(y_gpu, y_ref):
+    """Slot rows y[t, j] (bf16, [T, k, H]) of the GPU against the oracle's, element by element.
+
+    Both sides round at the same three points (gate/up root -> bf16, h = bf16(silu(g) u), down
+    root -> bf16: RL-Kernel blog, §6 table row 04 and §7 "FFN"); they differ only in how the fp32
+    and float64 sums and the SiLU round before those points.  So each element lies within one
+    bf16 ulp of the oracle's, except where an upstream 1-ulp flip of g, u or h (rare: the two
+    sides land on different sides of a bf16 rounding boundary) moves a y near zero by more than
+    its own ulp: 2^-9 of the row's RMS covers that (a flip moves y by |W2| ulp(h), ~1e-4 of the
+    RMS here).  And at least 99 % of the elements carry identical bits: an fp32 emulation of the
+    kernel's chain matches the oracle on ~99.9 %, while a rounding point moved, dropped or added
+    (g, u or h left in fp32, silu rounded on its own) matches on 39-58 %."""
+    got = oracle.bf16_to_f64(bits(y_gpu)).reshape(y_ref.shape)
+    ref = oracle.bf16_to_f64(y_ref)
+    err = np.abs(got - ref)
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64) * 65536.0
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    assert np.all(err <= ulp + 2.0 ** -9 * rms), float((err - ulp - 2.0 ** -9 * rms).max())
+    same = float((bits(y_gpu).reshape(y_ref.shape) == y_ref).mean())
+    assert same >= 0.99, same
+
+
+@pytest.mark.parametrize("T,H,E,F,k", [(17, 256, 16, 768, 4), (200, 512, 16, 256, 8), (64, 2048, 128, 768, 8)])
+def test_slot_rows_vs_oracle(c8, T, H, E, F, k):
+    """The expert stages at slot level: every routing slot's down-projection row against the
+    oracle's (the 2e-2 row-norm bound on the combined output could not see a rounding point that
+    is off by a bf16 ulp)."""
+    x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=T + 40)
+    ids, w = B.moe_route(c8, logits.to(DEV), k)
+    y = B.moe_experts_partial(c8, x.to(DEV), ids, W1.to(DEV), W2.to(DEV), [1] * E)
+    ref = oracle.moe_layer(bits(x), ids.cpu().numpy(), w.cpu().double().numpy(), bits(W1), bits(W2), 8,
+                           with_slots=True)
+    _check_slot_rows(y.view(T, k, H), ref["y_slots"])
+    # the full layer's combine runs on exactly these rows
+    out = _layer(c8, x.to(DEV), ids, w, W1.to(DEV), W2.to(DEV))
+    assert same_bits(out, B.moe_combine(c8, y.view(T, k, H), w))
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
 def test_layer_partition_invariance_bitwise(c8):
     T, H, E, F, k = 300, 256, 16, 128, 8
     x, W1, W2, logits = inputs.moe_inputs(T, H, E, F, seed=11)
@@ -209,3 +248,11 @@ def test_config4_full_size_sampled(c8):
     assert np.all(np.abs(got - oe).max(axis=1) <= 2e-2 * np.linalg.norm(oe, axis=1))
     for P in (2, 8):
         assert same_bits(_layer(c8, x, ids, w, W1, W2, [e * P // E for e in range(E)]), base)
+    # slot level, sampled tokens: the rows the full-size grouped GEMMs write for them
+    y = B.moe_experts_partial(c8, x, ids, W1, W2, [1] * E).view(T, k, H)
+    g = torch.Generator().manual_seed(8)
+    tok = torch.randint(0, T, (13,), generator=g).tolist() + [0, 4095, 8191]
+    tk = torch.tensor(tok, device=DEV)
+    ref = oracle.moe_layer(bits(x[tk]), ids[tk].cpu().numpy(), w[tk].cpu().double().numpy(), bits(W1), bits(W2), 8,
+                           with_slots=True)
+    _check_slot_rows(y[tk], ref["y_slots"])
