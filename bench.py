@@ -45,6 +45,23 @@ WORKLOAD = ("dense projection GEMMs of an 8B-class decoder: M=4096 tokens, (K,N)
 LP_T, LP_H, LP_V = 4096, 4096, 151936
 
 
+def bench_config(world):
+    """The workload description both arms print (the same keys and values)."""
+    return dict(workload=WORKLOAD, global_batch=M_TOKENS * world, parallelism=f"replicas{world}",
+                l2="flushed before every step (256 MiB write, outside the event window)", leaves=LEAVES)
+
+
+def rnd(x, sig=5):
+    """Round every float of a nested structure to `sig` significant digits (a short JSON line)."""
+    if isinstance(x, float):
+        return float(f"{x:.{sig}g}")
+    if isinstance(x, dict):
+        return {k: rnd(v, sig) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [rnd(v, sig) for v in x]
+    return x
+
+
 def step_flops(M=M_TOKENS):
     return sum(2.0 * M * K * N for K, N in SHAPES)
 
@@ -187,7 +204,7 @@ def run_reference(args, rank, world):
     line = dict(impl="reference", metric=METRIC, value=v, unit="TFLOP/s", n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=1e3 * statistics.mean(times), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload=WORKLOAD, parallelism="replicas", l2="n/a (CPU)"),
+                config=bench_config(world),
                 cpu_baseline=dict(value=v, unit="TFLOP/s", cores=os.cpu_count() or 1, kind="oracle", sample=sample),
                 e2e=dict(value=v, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
@@ -313,18 +330,43 @@ def run_ours(args, rank, world):
         extra = secondary(c, dev, stream, peaks, rank)
 
     if rank == 0:
+        config = bench_config(world)
+        config["contract_digest"] = c.digest.hex()[:16]
         line = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                     ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
-                    data="synthetic",
-                    config=dict(workload=WORKLOAD, global_batch=M_TOKENS * world, parallelism=f"replicas{world}",
-                                l2="flushed before every step (256 MiB write, outside the event window)",
-                                leaves=LEAVES, contract_digest=c.digest.hex()),
-                    roofline=roofline, e2e=e2e, gpu_launches=args.steps * len(SHAPES), clocks=clocks,
-                    wall_s_timed_region=wall)
-        line.update(extra)
+                    data="synthetic", config=config, roofline=roofline, e2e=e2e, gpu_launches=args.steps * len(SHAPES),
+                    clocks=clocks, wall_s_timed_region=wall)
         if world == 1 and not args.skip_cpu:
             line["cpu_baseline"] = cpu_baseline()
-        print(json.dumps(line), flush=True)
+        if extra:
+            if args.details:
+                with open(args.details, "w") as f:
+                    json.dump(extra, f, indent=1)
+            line["secondary"] = secondary_summary(extra)
+            line["logprob"] = logprob_summary(extra["logprob"])  # last: the end of the line is what logs keep
+        print(json.dumps(rnd(line)), flush=True)
+
+
+def secondary_summary(x):
+    """The secondary measurements in a few keys (full figures: --details)."""
+    g = x["gemm_sweep"]
+    small = {f"M{M}_{K}x{N}": g[f"M{M}_K{K}_N{N}"]["ws_hbm_frac"] for K, N in SHAPES for M in (1, 64)}
+    at = x["attention"]
+    return dict(gemm_small_m_hbm_frac=small,
+                overhead_vs_cublas_M4096={f"{K}x{N}": g[f"M4096_K{K}_N{N}"]["overhead_vs_cublas"] for K, N in SHAPES},
+                rmsnorm_hbm_frac=x["rmsnorm"]["roofline_frac"],
+                attention=dict(prefill_tc_frac=at["roofline_frac"], decode_hbm_frac=at["decode"]["roofline_frac"]),
+                moe=dict(ms=x["moe"]["ms"], tflops=x["moe"]["tflops"], tc_frac=x["moe"]["roofline_frac"]),
+                diagnostics_ms=x["diagnostics"]["ms"])
+
+
+def logprob_summary(lp):
+    vp = lp["vocab_parallel"]
+    return dict(workload=lp["workload"], tokens_per_s=lp["tokens_per_s"], ms=lp["ms"], tflops=lp["tflops"],
+                roofline_frac=lp["roofline_frac"], bound=lp["bound"],
+                T1=dict(tokens_per_s=lp["T1"]["tokens_per_s"], hbm_frac=lp["T1"]["roofline_frac"]),
+                T64=dict(tokens_per_s=lp["T64"]["tokens_per_s"], hbm_frac=lp["T64"]["roofline_frac"]),
+                vocab_parallel_same_bits=all(v["same_bits_as_single_call"] for v in vp.values()))
 
 
 def time_call(fn, iters, warm, stream, flush=None):
@@ -356,15 +398,16 @@ def secondary(c, dev, stream, peaks, rank):
     out = {}
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    # selected-token logprob, T = 4096, H = 4096, V = 151936
-    h, W, ids = inputs.logprob_inputs(LP_T, LP_H, LP_V, seed=2, device=dev)
+    # selected-token logprob, T = 4096, H = 4096, V = 151936; the hidden states are RMS-normalised
+    # rows (iso_rmsnorm with unit gamma over N(0,1) rows, before the timed region)
+    h, W, ids = logprob_workload(c, dev)
     lp_out = torch.empty(LP_T, dtype=torch.float32, device=dev)
     ws = torch.empty(B.selected_logprob_workspace(c, LP_T, LP_V), dtype=torch.uint8, device=dev)
     t = time_call(lambda: B.selected_logprob(c, h, W, ids, out=lp_out, ws=ws, stream=stream), 5, 2, stream)
     fl = 2.0 * LP_T * LP_H * LP_V
     byt = 2.0 * LP_H * LP_V + 2.0 * LP_T * LP_H + 8.0 * LP_T
     ideal = max(fl / (peaks["tc"] * 1e12), byt / (peaks["hbm"] * 1e9))
-    out["logprob"] = dict(workload="T=4096, H=4096, V=151936, 8 leaves, 128-col tiles, 63 chunks",
+    out["logprob"] = dict(workload="T=4096, H=4096 (RMS-normalised rows), V=151936, 8 leaves, 63 chunks",
                           tokens_per_s=LP_T / (t * 1e-3), ms=t, tflops=fl / (t * 1e-3) / 1e12,
                           roofline_frac=ideal / (t * 1e-3), bound="tensor")
     for T in (1, 64):
@@ -509,6 +552,19 @@ def secondary(c, dev, stream, peaks, rank):
     return out
 
 
+def logprob_workload(c, dev):
+    """Selected-token logprob inputs: h = iso_rmsnorm(x, unit gamma) of x ~ N(0,1) [4096 x 4096]
+    (the final norm's output, as the LM head sees it), W ~ N(0, 0.02^2) [4096 x 151936], ids
+    uniform in [0, 151936)."""
+    import torch
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import inputs
+    x, W, ids = inputs.logprob_inputs(LP_T, LP_H, LP_V, seed=2, device=dev)
+    h = B.rmsnorm(c, x, torch.ones(LP_H, dtype=torch.bfloat16, device=dev), 1e-6)
+    torch.cuda.synchronize()
+    return h, W, ids
+
+
 ATT_HQ, ATT_HKV, ATT_D = 32, 8, 128  # 8B-class decoder: 32 query heads over 8 KV heads
 
 
@@ -571,7 +627,7 @@ def profile_target(target: str, calls: int):
         C = torch.empty(M_TOKENS, 12288, dtype=torch.bfloat16, device=dev)
         fn = lambda: B.gemm(c, X, W, out=C)
     elif target == "logprob":
-        h, W, ids = inputs.logprob_inputs(LP_T, LP_H, LP_V, seed=2, device=dev)
+        h, W, ids = logprob_workload(c, dev)
         out = torch.empty(LP_T, dtype=torch.float32, device=dev)
         ws = torch.empty(B.selected_logprob_workspace(c, LP_T, LP_V), dtype=torch.uint8, device=dev)
         fn = lambda: B.selected_logprob(c, h, W, ids, out=out, ws=ws)
@@ -617,6 +673,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--details", default=None, help="write the full secondary measurements to this JSON file")
     ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small",
                                                      "diagnostics"],
                     help="run one workload --steps times without timing (for ncu) and exit")
