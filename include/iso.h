@@ -28,6 +28,10 @@
  *     per-device status word that iso_last_device_status() reads and clears.
  *   - Alignment: device pointers 16-byte aligned; leading dimensions of bf16
  *     matrices multiples of 8 elements, of fp32 matrices multiples of 4.
+ *   - Per-device state (the status word's address, the SM count, the static
+ *     scratch's address) is looked up on a device's first call and kept for
+ *     the life of the process: the library must not be used across a
+ *     cudaDeviceReset of a device it has already run on.
  */
 #ifndef ISO_H_
 #define ISO_H_
@@ -236,7 +240,9 @@ iso_status iso_selected_logprob_combine(const iso_contract* c, int num_shards, c
  * nothing (8 MiB: up to 16,512 tokens at V = 151936); up to 820 tokens the
  * array also holds the per-tile statistics of the faster schedule.
  * The first call on a device looks up the array's device address; make that
- * first call before any stream capture.  All calls on a device share the one
+ * first call before any stream capture.  The address is kept for the life of
+ * the process: do not call this entry point across a cudaDeviceReset (or any
+ * other teardown and re-creation of the device's primary context).  All calls on a device share the one
  * array: calls whose kernels may overlap on the GPU (unordered streams) race
  * and must be serialized by the caller. */
 #define ISO_LOGPROB_STATIC_SCRATCH_BYTES (8u << 20)

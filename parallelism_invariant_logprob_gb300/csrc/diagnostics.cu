@@ -1,5 +1,5 @@
 // diagnostics.cu -- training/rollout mismatch diagnostics over packed sequences of
-// selected-token logprobs (memory-bound; one warp per sequence).
+// selected-token logprobs (one 1024-thread block per sequence).
 //
 // What it computes [VeXact paper, "Diagnosing Training Inference Mismatch in LLM
 // Reinforcement Learning"]: per token the mismatch delta_t = log pi_train - log pi_rollout

@@ -43,8 +43,9 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 def test_static_scratch_rejects_oversize():
     c = B.Contract(8)
     V = 151936
-    T = 20000  # needs more than the fixed scratch at this vocabulary
-    assert c.lib.iso_selected_logprob_workspace(c.handle, T, V) > SCRATCH_BYTES
+    T = 16513  # one token past what the fixed scratch holds at this vocabulary
+    assert c.lib.iso_selected_logprob_min_workspace(c.handle, T - 1, V) <= SCRATCH_BYTES
+    assert c.lib.iso_selected_logprob_min_workspace(c.handle, T, V) > SCRATCH_BYTES
     h = torch.zeros(T, 128, dtype=torch.bfloat16, device="cuda")
     W = torch.zeros(128, V, dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros(T, dtype=torch.int32, device="cuda")
