@@ -69,7 +69,7 @@ typedef void* iso_stream;                 /* cudaStream_t */
  *  identities (SHA-256 digests of the serialized contract)]
  *
  * iso_contract_init: leaf_count = number of contiguous K-leaves (a power of
- * two, 1..8 in this library); schedule must be ISO_TREE_BALANCED_BINARY;
+ * two, 1..16 in this library); schedule must be ISO_TREE_BALANCED_BINARY;
  * acc_dtype must be ISO_F32; out_dtype must be ISO_BF16.  On success *out
  * receives a new contract (free with iso_contract_destroy) and digest (if not
  * NULL) the 32-byte SHA-256 of its canonical serialization, which covers every

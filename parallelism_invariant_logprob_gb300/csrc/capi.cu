@@ -156,7 +156,7 @@ void set_a_rows(GemmParams& p, int a_rows) {
   p.a_rows = a_rows;
   p.a_bytes = a_rows * BK * 2;
   const int b_bytes = p.pair ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
-  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES;
+  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - (p.spill ? SPILL_BYTES : 0);
   int st = room / (p.a_bytes + b_bytes);
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
@@ -170,7 +170,7 @@ void set_leaf_stage(GemmParams& p) {
   p.kb_per_leaf = 1;
   p.a_rows = BM;
   p.a_bytes = LS_A_BYTES;
-  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES;
+  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - (p.spill ? SPILL_BYTES : 0);
   int st = room / (LS_A_BYTES + LS_B_BYTES);
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
@@ -223,6 +223,7 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.N = N;
   p.K = K;
   p.L = L;
+  p.spill = L > TMEM_TREE_LEAVES ? 1 : 0;
   p.leaf_len = K / L;
   p.num_kb = div_up(K, BK);
   p.kb_per_leaf = div_up(K / L, BK);

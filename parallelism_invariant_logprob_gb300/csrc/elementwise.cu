@@ -20,7 +20,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
 }
 
-// Balanced binary tree over v[0..n) (n a power of two <= 8), left = lower index.
+// Balanced binary tree over v[0..n) (n a power of two <= NMAX), left = lower index.
 template <int NMAX>
 __device__ __forceinline__ float tree_sum(float (&v)[NMAX], int n) {
 #pragma unroll
@@ -44,9 +44,9 @@ __global__ void tree_combine_kernel(const float* __restrict__ S, int64_t lds, in
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = idx / nvec_row;
     const int64_t j = (idx - i * nvec_row) * 4;
-    float a[8], b[8], c[8], d[8];
+    float a[MAX_LEAVES], b[MAX_LEAVES], c[MAX_LEAVES], d[MAX_LEAVES];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < MAX_LEAVES; ++r) {
       if (r < R) {
         const float4 v = __ldcs(reinterpret_cast<const float4*>(S + r * rank_stride + i * lds + j));
         a[r] = v.x;
@@ -57,7 +57,8 @@ __global__ void tree_combine_kernel(const float* __restrict__ S, int64_t lds, in
         a[r] = b[r] = c[r] = d[r] = 0.f;
       }
     }
-    const float ra = tree_sum<8>(a, R), rb = tree_sum<8>(b, R), rc = tree_sum<8>(c, R), rd = tree_sum<8>(d, R);
+    const float ra = tree_sum<MAX_LEAVES>(a, R), rb = tree_sum<MAX_LEAVES>(b, R), rc = tree_sum<MAX_LEAVES>(c, R),
+                rd = tree_sum<MAX_LEAVES>(d, R);
     uint2 o = make_uint2(pack2(ra, rb), pack2(rc, rd));
     *reinterpret_cast<uint2*>(C + i * ldc + j) = o;
   }

@@ -212,6 +212,13 @@ __device__ __forceinline__ bool elect_one() {
 
 __device__ __forceinline__ int merges_after_leaf(int l) { return __ffs(l + 1) - 1; }  // trailing zeros of l+1
 
+// Merges in TMEM after leaf l of an L-leaf tree.  With a parked subtree (L > TMEM_TREE_LEAVES)
+// the last leaf's merges stop one level short: the top merge, with the root of leaves [0, L/2)
+// kept in shared memory, is made by the epilogue as it reads the root.
+__device__ __forceinline__ int tmem_merges_after_leaf(int l, int L, int spill) {
+  return merges_after_leaf(l) - ((spill && l == L - 1) ? 1 : 0);
+}
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
@@ -384,6 +391,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
   volatile uint32_t* next_leaf = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   // bf16 output staging (valid when p.epi_staged): 8 KB per epilogue warp
   uint8_t* epi_stage = smem + b_region + nstages * BSTAGE + GEMM_BARRIER_BYTES;
+  // parked subtree root (valid when p.spill): fp32 [BN columns][BM rows]
+  float* parked = reinterpret_cast<float*>(epi_stage + (p.epi_staged ? EPI_STAGE_BYTES : 0));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -624,8 +633,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 }
               }
             }
-            const int nm = merges_after_leaf(leaf);
+            const int nm = tmem_merges_after_leaf(leaf, p.L, p.spill);
             for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
+            if (p.spill && leaf == p.L / 2 - 1) tb.push_free(tb.pop());  // parked in shared memory
             if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
           }
         }
@@ -724,7 +734,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           }
           fill_par ^= 1u << b;
           tc_fence_after();
-          const int nm = merges_after_leaf(l);
+          const int nm = tmem_merges_after_leaf(l, p.L, p.spill);
           for (int m = 0; m < nm; ++m) {
             const int rb = tb.pop();
             const int lb = tb.top();
@@ -759,6 +769,31 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             release_tmem_buf<PAIR>(buf_free, rb, lane);
             tb.push_free(rb);
           }
+          if (p.spill && l == p.L / 2 - 1) {
+            // park the root of leaves [0, L/2): this warp's columns of its rows (the columns it
+            // merges) into shared memory, then give the TMEM buffer back
+            const int sb = tb.pop();
+            const uint32_t so = tmem_base + lane_off + static_cast<uint32_t>(sb * BN);
+#pragma unroll 1
+            for (int c = 0; c < (EPW == 8 ? 1 : BN / 64); ++c) {
+              const int ca = EPW == 8 ? (EPI == EPI_SWIGLU ? chalf * 32 : chalf * 64) : c * 64;
+              const int cb = (EPW == 8 && EPI == EPI_SWIGLU) ? 64 + chalf * 32 : ca + 32;
+              uint32_t x[64];
+              tmem_ld32p(so + ca, x);
+              tmem_ld32p(so + cb, x + 32);
+              tmem_ld_wait_only();
+              tmem_ld_tie(x);
+              tmem_ld_tie(x + 32);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                parked[(ca + i) * BM + row_in_tile] = u2f(x[i]);
+                parked[(cb + i) * BM + row_in_tile] = u2f(x[32 + i]);
+              }
+            }
+            tc_fence_before();
+            release_tmem_buf<PAIR>(buf_free, sb, lane);
+            tb.push_free(sb);
+          }
         }
         if (!ok) break;
         // ---- the root of this tile
@@ -782,6 +817,13 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < 2 * HC / 32; ++c) tmem_ld_tie(v + c * 32);
+          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+#pragma unroll
+            for (int i = 0; i < HC; ++i) {
+              v[i] = f2u(__fadd_rn(parked[(h0 + i) * BM + row_in_tile], u2f(v[i])));
+              v[HC + i] = f2u(__fadd_rn(parked[(64 + h0 + i) * BM + row_in_tile], u2f(v[HC + i])));
+            }
+          }
           tc_fence_before();
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
@@ -820,6 +862,10 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < RC / 32; ++c) tmem_ld_tie(v + c * 32);
+          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+#pragma unroll
+            for (int i = 0; i < RC; ++i) v[i] = f2u(__fadd_rn(parked[(c0 + i) * BM + row_in_tile], u2f(v[i])));
+          }
           tc_fence_before();
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
@@ -874,6 +920,10 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
+          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+#pragma unroll
+            for (int i = 0; i < BN; ++i) v[i] = f2u(__fadd_rn(parked[i * BM + row_in_tile], u2f(v[i])));
+          }
           tc_fence_before();
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);

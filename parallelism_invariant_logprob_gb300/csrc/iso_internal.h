@@ -57,7 +57,14 @@ constexpr int GEMM_REGS_EPILOGUE_EPI8 = 200;  // and of warps 4-11
 static_assert(128 * GEMM_REGS_CONTROL_EPI8 + 256 * GEMM_REGS_EPILOGUE_EPI8 <= 384 * 168,
               "register split within the launch's allocation");
 constexpr int GEMM_REGS_CONTROL_FUSED = 120;  // setmaxnreg of warps 0-3 and 8-11 (epilogue: 256)
-constexpr int MAX_LEAVES = 8;      // tree depth 3 + incoming leaf fit 4 TMEM buffers
+// The eager merge stack of a tree over 8 leaves (depth 3) plus the incoming leaf fills the 4
+// TMEM buffers.  16 leaves need one more: the root of leaves [0, 8) is parked in shared memory
+// (fp32, 64 KB, [column][row] so consecutive rows are consecutive words) once its merges are
+// done, its TMEM buffer goes back to the free list, and the epilogue adds it to the root of
+// leaves [8, 16) at the top of the tree -- the same fp32 add the tree makes there.
+constexpr int TMEM_TREE_LEAVES = 8;
+constexpr int MAX_LEAVES = 16;
+constexpr int SPILL_BYTES = BM * BN * 4;
 constexpr int GEMM_SMEM_BYTES = 232448;  // the per-block maximum; 1 KB of it is alignment slack
 constexpr int MOE_MAX_EXPERTS = 256;
 constexpr int MOE_PERM_CHUNK = 1024;   // pairs per chunk of the permutation's counting sort
@@ -83,6 +90,7 @@ struct GemmParams {
   int num_kb;      // ceil(K / BK)
   int kb_per_leaf; // ceil(leaf_len / BK)
   int stages;      // pipeline stages (even, <= MAX_STAGES)
+  int spill;       // 1 when L > TMEM_TREE_LEAVES: the root of leaves [0, L/2) is parked in shared memory
   int epi_staged;  // 1: bf16 roots go out through the shared-memory staging area
   int pair;        // 1: clusters of two CTAs, M = 256 MMAs; a unit covers 2 x 128 rows
   int a_rows;      // rows of the A box (16, 32, 64 or 128)

@@ -46,16 +46,16 @@ def test_sha256_matches_hashlib(lib, n):
 
 def test_contract_digest_is_sha256_of_serialization(lib):
     digests = {}
-    for L in (1, 2, 4, 8):
+    for L in (1, 2, 4, 8, 16):
         c = B.Contract(L, lib)
         s = c.serialize()
         obj = json.loads(s)  # canonical form is valid JSON
         assert obj["gemm"]["leaves"] == L
-        assert obj["claims"]["topology"]["simulated_ranks"] == [r for r in (1, 2, 4, 8) if r <= L]
+        assert obj["claims"]["topology"]["simulated_ranks"] == [r for r in (1, 2, 4, 8, 16) if r <= L]
         assert c.digest == hashlib.sha256(s.encode()).digest()
         assert c.check_peer(c.digest) == B.ISO_OK
         digests[L] = c.digest
-    assert len(set(digests.values())) == 4
+    assert len(set(digests.values())) == 5
     c8 = B.Contract(8, lib)
     assert c8.check_peer(digests[4]) == 6  # ISO_ERR_CONTRACT_MISMATCH
     assert B.Contract(8, lib).digest == digests[8]  # deterministic
@@ -125,7 +125,7 @@ def test_contract_serialization_names_the_executed_numerics(lib):
 def test_contract_init_rejects(lib):
     h = ctypes.c_void_p()
     assert lib.iso_contract_init(3, 0, B.ISO_F32, B.ISO_BF16, ctypes.byref(h), None) == 1
-    assert lib.iso_contract_init(16, 0, B.ISO_F32, B.ISO_BF16, ctypes.byref(h), None) == 5
+    assert lib.iso_contract_init(32, 0, B.ISO_F32, B.ISO_BF16, ctypes.byref(h), None) == 5
     assert lib.iso_contract_init(8, 0, B.ISO_BF16, B.ISO_BF16, ctypes.byref(h), None) == 5
     assert lib.iso_contract_init(8, 1, B.ISO_F32, B.ISO_BF16, ctypes.byref(h), None) == 5
     assert lib.iso_contract_init(8, 0, B.ISO_F32, B.ISO_BF16, None, None) == 1

@@ -135,6 +135,35 @@ def test_gemm_tree_shape_golden():
     assert oracle.tree_combine(S)[0, 0] == fx["f64_balanced_tree"]
 
 
+def test_gemm_tree_shape_sixteen_leaves():
+    # leaf 0 = 2^53, leaf 8 = 1, leaf 15 = -2^53 (float64): the balanced tree's top add is
+    # 2^53 + (1 - 2^53) = 1; a left fold gives (2^53 + 1) - 2^53 = 0 (2^53 + 1 rounds to 2^53)
+    L = 16
+    vals = [0.0] * L
+    vals[0], vals[8], vals[15] = 2.0 ** 53, 1.0, -(2.0 ** 53)
+    A = np.array([bf16_bits_of([1.0] * L)])
+    B = bf16_bits_of([[v] for v in vals])
+    assert oracle.gemm_root(A, B, L)[0, 0] == 1.0
+    fold = 0.0
+    for v in vals:
+        fold += v
+    assert fold == 0.0
+    S = np.stack([oracle.gemm_leaf_partial(A[:, 8 * r:8 * r + 8], B[8 * r:8 * r + 8], L, 2) for r in range(2)])
+    assert oracle.tree_combine(S)[0, 0] == 1.0
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8, 16])
+def test_gemm_partial_plus_combine_sixteen_leaves(R):
+    L = 16
+    A, B = inputs.gemm_inputs(3, 256, 11, seed=9)
+    Ab, Bb = bits(A), bits(B)
+    full = oracle.gemm_root(Ab, Bb, L)
+    Kl = 256 // R
+    S = np.stack([oracle.gemm_leaf_partial(Ab[:, r * Kl:(r + 1) * Kl], Bb[r * Kl:(r + 1) * Kl], L, R)
+                  for r in range(R)])
+    assert np.array_equal(oracle.tree_combine(S), full)
+
+
 @pytest.mark.parametrize("R", [1, 2, 4, 8])
 def test_gemm_partial_plus_combine_equals_single_pass(R):
     L = 8
