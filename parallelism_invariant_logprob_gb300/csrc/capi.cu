@@ -156,7 +156,9 @@ void set_a_rows(GemmParams& p, int a_rows) {
   p.a_rows = a_rows;
   p.a_bytes = a_rows * BK * 2;
   const int b_bytes = p.pair ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
-  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - (p.spill ? SPILL_BYTES : 0);
+  // the parked subtree root (spill), or a leaf group's root in cluster mode (the A box's rows only)
+  const int reserve = p.spill ? SPILL_BYTES : (p.cluster > 1 ? a_rows * BN * 4 : 0);
+  const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - reserve;
   int st = room / (p.a_bytes + b_bytes);
   if (st > MAX_STAGES) st = MAX_STAGES;
   p.stages = st & ~1;
@@ -252,9 +254,46 @@ iso_status check_gemm_args(const void* A, int64_t lda, const void* B, int64_t ld
   return ISO_OK;
 }
 
+// Leaf groups for one row block: with fewer 128-column tiles than SMs, the L leaves split into
+// R groups (R a power of two <= min(L, 8), R x tiles <= SMs) that run as one cluster of R CTAs
+// per tile, so R times as many SMs stream B, and the cluster combines the group roots with the
+// top log2 R levels of the tree -- the partial + combine of R simulated ranks inside one launch,
+// so the bits are the single pass's.  Needs all tiles' clusters resident at once.
+int cluster_groups(int M, int N, int L) {
+  if (M > BM) return 1;
+  const int n_tiles = div_up(N, BN);
+  int R = 1;
+  while (R * 2 <= L && R * 2 <= MAX_CLUSTER_GROUPS && n_tiles * R * 2 <= sm_count()) R *= 2;
+  while (R > 1 && cluster_gemm_capacity(R) < n_tiles) R /= 2;
+  return R;
+}
+
+// iso_gemm for one row block on clusters of R leaf-group CTAs (EPI_CLUSTER).
+iso_status run_gemm_cluster(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M,
+                            int N, int K, int L, int R, cudaStream_t s) {
+  GemmParams p = base_params(M, N, K / R, L / R);  // per group: K / R columns of A, L / R leaves
+  p.cluster = R;
+  set_a_rows(p, a_rows_for(M));  // (the group root's shared-memory region comes off the stages)
+  CUtensorMap tA, tB;
+  iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, static_cast<uint32_t>(p.a_rows));
+  if (st != ISO_OK) return st;
+  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
+  if (st != ISO_OK) return st;
+  p.unit_mode = UNIT_CLUSTER;
+  p.num_units = p.n_blocks * R;
+  p.out = C;
+  p.ldo = ldc;
+  trace("gemm[cluster leaf groups]", M, N, K, R);
+  return launch_gemm(EPI_CLUSTER, tA, tB, p, p.num_units, s);
+}
+
 iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M,
                     int N, int K, int L, cudaStream_t s) {
   if (!ensure_device_state()) return ISO_ERR_CUDA;
+  if (epi == EPI_BF16 && M <= BM) {
+    const int R = cluster_groups(M, N, L);
+    if (R > 1) return run_gemm_cluster(A, lda, B, ldb, C, ldc, M, N, K, L, R, s);
+  }
   GemmParams p = base_params(M, N, K, L);
   if (p.m_blocks == 1)
     set_a_rows(p, a_rows_for(M));
@@ -343,6 +382,8 @@ iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, co
   iso_status st = check_gemm_args(A, lda, B, ldb, C, ldc, 8, M, N, K, L);
   if (st != ISO_OK || M == 0) return st;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
+  // one row block whose leaf groups fit as clusters: iso_gemm's own one-launch schedule
+  if (cluster_groups(M, N, L) > 1) return run_gemm(EPI_BF16, A, lda, B, ldb, C, ldc, M, N, K, L, S(stream));
   // Leaf groups: with one row block and fewer column tiles than SMs, R groups of L/R leaves run
   // as separate units (R = the largest power of two <= L with R x tiles <= SMs); each writes
   // its group's fp32 subtree root to ws and the tree combine applies the top log2 R levels --

@@ -44,6 +44,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "iso_internal.h"
 #include "iso_ptx.cuh"
 
@@ -94,6 +96,16 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U,
     U.n_tiles = 1;
     U.rows_valid = min(BM, p.M);
     U.chunk = r;
+  } else if (p.unit_mode == UNIT_CLUSTER) {
+    // one unit per CTA: tile u / R, leaf group u % R (the CTA's rank in its cluster of R)
+    const int g = u % p.cluster;
+    U.a_row0 = 0;
+    U.a_col0 = g * p.K;
+    U.b_row0 = g * p.K;
+    U.n_tile0 = u / p.cluster;
+    U.n_tiles = 1;
+    U.rows_valid = min(BM, p.M);
+    U.chunk = g;
   } else if (p.unit_mode == UNIT_LOGPROB) {
     // chunk-major: the row blocks working on one vocab chunk run together and
     // share its W columns in L2.
@@ -391,7 +403,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
   volatile uint32_t* next_leaf = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   // bf16 output staging (valid when p.epi_staged): 8 KB per epilogue warp
   uint8_t* epi_stage = smem + b_region + nstages * BSTAGE + GEMM_BARRIER_BYTES;
-  // parked subtree root (valid when p.spill): fp32 [BN columns][BM rows]
+  // parked subtree root (valid when p.spill): fp32 [BN columns][BM rows]; in cluster mode the
+  // leaf group's root, fp32 [BN columns][a_rows rows]
   float* parked = reinterpret_cast<float*>(epi_stage + (p.epi_staged ? EPI_STAGE_BYTES : 0));
 
   const int warp = threadIdx.x >> 5;
@@ -536,7 +549,12 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       int stage = me;          // this thread's blocks sit at global stage indices me, me+per, ...
       uint32_t round = 0;
       bool ok = true;
-      const uint32_t smem_base = smem_u32(smem);
+      // Descriptor start addresses are the low 18 bits of the shared::cta address (14 bits of
+      // address / 16).  In a launch with clusters of more than one CTA the generic-to-shared
+      // conversion also carries bits above the CTA's window; unmasked, they would run into the
+      // descriptor's leading-byte-offset field (bit 16 on) and move the second 64-column chunk of
+      // the MN-major B operand.
+      const uint32_t smem_base = smem_u32(smem) & 0x3FFFFu;
       // descriptor templates; the start-address field (bits 0..13, 16-byte units) is added per use
       const uint64_t adesc0 = sdesc_sw128(0, 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(0, LS ? LS_B_BYTES / 2 : 8192, 1024);  // LBO: the second 64 columns
@@ -851,7 +869,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < HC / 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + h0 + q * 8) = hw[q];
           }
-        } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
+        } else if (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_CLUSTER) {
           // the root into registers, its TMEM buffer released, then convert and store; this
           // warp's columns: all 128, or with 8 epilogue warps the 64 of its half
           constexpr int RC = BN / (EPW / 4);
@@ -870,7 +888,18 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           release_tmem_buf<PAIR>(buf_free, root, lane);
           tb.push_free(root);
           released = true;
-          if (EPI == EPI_BF16 && p.epi_staged) {
+          if (EPI == EPI_CLUSTER) {
+            // the group's subtree root stays in this CTA's shared memory ([column][row], the A
+            // box's rows) for the cluster combine after the main loop
+            // as column pairs: pair q of row r is the 8-byte word (q a_rows + r), so one warp's
+            // rows are consecutive words and a combine thread reads a pair in one load
+            if (row_in_tile < p.a_rows) {
+#pragma unroll
+              for (int i = 0; i < RC; i += 2)
+                *reinterpret_cast<float2*>(&parked[2 * (((c0 + i) >> 1) * p.a_rows + row_in_tile)]) =
+                    make_float2(u2f(v[i]), u2f(v[i + 1]));
+            }
+          } else if (EPI == EPI_BF16 && p.epi_staged) {
             uint4 w[RC / 8];
 #pragma unroll
             for (int q = 0; q < RC / 8; ++q) {
@@ -976,6 +1005,65 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (EPI == EPI_CLUSTER) {
+    // Every CTA of the cluster has its group root in shared memory (the barrier's release /
+    // acquire orders those stores before the peers' loads).  This CTA (rank r) combines columns
+    // [r BN/R, (r+1) BN/R) of the tile: for each (row, column pair) the R group roots in group
+    // order, the balanced tree over them (left operand = lower group, fp32 rn adds: the top
+    // log2 R levels of the contract's tree), one bf16 rounding.  The second barrier keeps every
+    // CTA's shared memory alive until the peers are done reading it.  Each CTA reaches both
+    // barriers whatever happened before, so an aborted CTA cannot leave its peers waiting.
+    cluster_sync_all();
+    if (unit0 < nunits) {
+      Unit U;
+      decode_unit(p, unit0, U, 1, 0);
+      const int R = p.cluster;
+      const int cols = BN / R;
+      const int npairs = cols / 2;
+      const int c_base = static_cast<int>(cluster_ctarank()) * cols;  // first column of this CTA's slice
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+      const int total = U.rows_valid * npairs;
+      // four (row, column pair) elements per thread per pass: every group's load of all four is
+      // issued before the first is used, so a pass costs one round trip to the peers
+      constexpr int EB = 4;
+      for (int e0 = threadIdx.x; e0 < total; e0 += EB * static_cast<int>(blockDim.x)) {
+        float2 x[EB][MAX_CLUSTER_GROUPS];
+#pragma unroll
+        for (int q = 0; q < EB; ++q) {
+          const int e = e0 + q * static_cast<int>(blockDim.x);
+          if (e < total) {
+            const int row = e / npairs;
+            const int pr = (c_base >> 1) + (e - row * npairs);  // column pair within the tile
+#pragma unroll
+            for (int g = 0; g < MAX_CLUSTER_GROUPS; ++g)
+              if (g < R)
+                x[q][g] = ld_cluster_f32x2(cluster_addr(&parked[2 * (pr * p.a_rows + row)], static_cast<uint32_t>(g)));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < EB; ++q) {
+          const int e = e0 + q * static_cast<int>(blockDim.x);
+          if (e >= total) continue;
+          const int row = e / npairs;
+          const int col = U.n_tile0 * BN + c_base + 2 * (e - row * npairs);
+          if (col >= p.N) continue;
+          // balanced tree over the groups, left operand = lower group (fp32 rn adds)
+#pragma unroll
+          for (int w = 1; w < MAX_CLUSTER_GROUPS; w *= 2) {
+#pragma unroll
+            for (int g = 0; g + w < MAX_CLUSTER_GROUPS; g += 2 * w) {
+              if (g + w < R) {
+                x[q][g].x = __fadd_rn(x[q][g].x, x[q][g + w].x);
+                x[q][g].y = __fadd_rn(x[q][g].y, x[q][g + w].y);
+              }
+            }
+          }
+          *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(row) * p.ldo + col) = pack_bf16x2(x[q][0].x, x[q][0].y);
+        }
+      }
+    }
+    cluster_sync_all();
+  }
   if (PAIR) {
     // After an abort the peer's last loads may still be landing in this CTA's shared memory
     // (their completion is counted on rank 0, which may have stopped waiting): give them time.
@@ -1035,6 +1123,24 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
       fprintf(stderr, "[iso] gemm kernel epi=%d pair=%d epilogue warps=%d: %d %s resident\n", EPI, PAIR ? 1 : 0,
               EPW, slots, PAIR ? "CTA pairs" : "CTAs");
   }
+  if constexpr (EPI == EPI_CLUSTER) {
+    // one CTA per unit, in clusters of p.cluster (the host checked that they fit at once)
+    if (max_units <= 0 || max_units % p.cluster != 0) return ISO_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(max_units));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, p) != cudaSuccess) return ISO_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
+  }
   const int units = max_units < slots ? max_units : slots;
   if (units <= 0) return ISO_OK;
   if (!PAIR) {
@@ -1058,6 +1164,37 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 }
 
 }  // namespace
+
+int cluster_gemm_capacity(int R) {
+  static std::mutex mu;
+  static int cached_dev = -1;
+  static int cap[MAX_CLUSTER_GROUPS + 1] = {};
+  int dev = 0;
+  if (R < 2 || R > MAX_CLUSTER_GROUPS || cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached_dev != dev) {
+    auto kern = iso_leaf_tree_gemm_kernel<EPI_CLUSTER, false, false, 4, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
+      return 0;
+    for (int r = 2; r <= MAX_CLUSTER_GROUPS; r *= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = static_cast<unsigned>(r);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(r * (sm_count() / r)));
+      cfg.blockDim = dim3(GEMM_THREADS);
+      cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      cap[r] = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
+    }
+    cached_dev = dev;
+  }
+  return cap[R];
+}
 
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                        cudaStream_t s, const CUtensorMap* tmA2) {
@@ -1092,6 +1229,9 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
     case EPI_LOGPROB:
       return pair ? launch_one<EPI_LOGPROB, true>(tmA, tmB, p, max_units, s, a2)
                   : launch_one<EPI_LOGPROB, false>(tmA, tmB, p, max_units, s, a2);
+    case EPI_CLUSTER:
+      if (pair || p.cluster < 2 || p.cluster > MAX_CLUSTER_GROUPS) return ISO_ERR_INVALID_ARG;
+      return launch_one<EPI_CLUSTER, false>(tmA, tmB, p, max_units, s, a2);
     default:
       return ISO_ERR_INVALID_ARG;
   }

@@ -80,8 +80,13 @@ constexpr int LP_CHUNK_TILES = 19;
 constexpr int ATT_CHUNK_KEYS = 80;
 constexpr float ATT_LAZY_LOG2 = 8.0f;
 
-enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2, EPI_SWIGLU = 3 };
-enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2, UNIT_LEAF_SPLIT = 3 };
+// EPI_CLUSTER: one row block, the L leaves split into R groups that run as one thread-block
+// cluster of R CTAs per 128-column tile; each CTA leaves its group's fp32 subtree root in its
+// shared memory and, after a cluster barrier, combines one R-th of the tile's columns over all R
+// groups (distributed shared memory) with the top log2 R levels of the tree, then rounds to bf16.
+enum EpiMode { EPI_BF16 = 0, EPI_F32 = 1, EPI_LOGPROB = 2, EPI_SWIGLU = 3, EPI_CLUSTER = 4 };
+enum UnitMode { UNIT_GEMM = 0, UNIT_LOGPROB = 1, UNIT_GROUPED = 2, UNIT_LEAF_SPLIT = 3, UNIT_CLUSTER = 4 };
+constexpr int MAX_CLUSTER_GROUPS = 8;  // portable cluster size
 
 struct GemmParams {
   int M, N, K;     // K = contraction length handled by this launch
@@ -91,6 +96,7 @@ struct GemmParams {
   int kb_per_leaf; // ceil(leaf_len / BK)
   int stages;      // pipeline stages (even, <= MAX_STAGES)
   int spill;       // 1 when L > TMEM_TREE_LEAVES: the root of leaves [0, L/2) is parked in shared memory
+  int cluster;     // EPI_CLUSTER: leaf groups per tile = CTAs per cluster (the group root uses the park region)
   int epi_staged;  // 1: bf16 roots go out through the shared-memory staging area
   int pair;        // 1: clusters of two CTAs, M = 256 MMAs; a unit covers 2 x 128 rows
   int a_rows;      // rows of the A box (16, 32, 64 or 128)
@@ -157,5 +163,8 @@ iso_status make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t rows
 // tmA2: the 32-column A boxes of whole-leaf stages (p.leaf_stage), else unused (may be null).
 iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                        cudaStream_t s, const CUtensorMap* tmA2 = nullptr);
+// Clusters of R CTAs of the EPI_CLUSTER GEMM that are resident at once on the current device
+// (0 when R is not 2, 4 or 8 or the query fails).
+int cluster_gemm_capacity(int R);
 
 }  // namespace iso

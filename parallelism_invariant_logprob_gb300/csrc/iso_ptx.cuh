@@ -99,7 +99,13 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t ran
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-// Every thread of both CTAs arrives and waits (release / acquire at cluster scope).
+// Two fp32 from a shared::cluster address (this CTA's or a peer's shared memory), 8-byte aligned.
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t cluster_addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(cluster_addr) : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster arrives and waits (release / acquire at cluster scope).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -297,3 +297,22 @@ def test_canary_guard_bands(c8, M, K):
 
 def test_device_status_clean(c8):
     assert B.last_device_status(c8) == B.ISO_OK
+
+
+@pytest.mark.parametrize("M,K,N,L", [(1, 4096, 4096, 8), (33, 1024, 392, 8), (128, 2048, 1024, 4), (64, 12288, 4096, 8),
+                                     (2, 512, 520, 2)])
+def test_cluster_leaf_groups_equal_single_pass(M, K, N, L):
+    """One row block with few column tiles runs its leaf groups as thread-block clusters (each
+    CTA one group, the top tree levels over distributed shared memory).  Its rows must equal the
+    same rows computed inside a 300-row product (single pass, one CTA per tile and all leaves),
+    and exact integers must equal the oracle."""
+    c = B.Contract(L)
+    A, Bm = inputs.gemm_inputs(300, K, N, seed=K + N + M)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    big = B.gemm(c, Ad, Bd)
+    for r0 in (0, 300 - M):
+        assert same_bits(B.gemm(c, Ad[r0:r0 + M].contiguous(), Bd), big[r0:r0 + M]), r0
+    Ai = inputs.small_int_bf16((M, K), -3, 3, seed=M + 7)
+    Bi = inputs.small_int_bf16((K, N), -3, 3, seed=N + 7)
+    assert np.array_equal(bits(B.gemm(c, Ai.to(DEV), Bi.to(DEV))), oracle.gemm(bits(Ai), bits(Bi), L))
+    assert B.last_device_status(c) == B.ISO_OK
