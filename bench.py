@@ -369,6 +369,68 @@ def logprob_summary(lp):
                 vocab_parallel_same_bits=all(v["same_bits_as_single_call"] for v in vp.values()))
 
 
+def run_tp(args, rank, world):
+    """Row-parallel TP step (--parallel tp): the same three M = 4096 projections with K split over
+    the N ranks (rank r owns the contiguous leaves of its K slice): each rank's leaf partial, an
+    all-gather of the fp32 subtree roots (transport only) and the tree combine on every rank.
+    Total work is fixed, so scaling is strong; value = the step's flops / the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import exchange, inputs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    c = B.Contract(LEAVES)
+    ops = exchange.LibraryOps(c, stream=torch.cuda.current_stream())
+    group = dist.group.WORLD if world > 1 else None
+    As, Bs = [], []
+    for i, (K, N) in enumerate(SHAPES):
+        X, W = inputs.gemm_inputs(M_TOKENS, K, N, seed=100 + i, device=dev)
+        Kl = K // world
+        As.append(X[:, rank * Kl:(rank + 1) * Kl].contiguous())
+        Bs.append(W[rank * Kl:(rank + 1) * Kl].contiguous())
+        del X, W
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for i in range(len(SHAPES)):
+            if world > 1:
+                exchange.row_parallel_gemm(As[i], Bs[i], ops, group)
+            else:
+                B.tree_combine(c, B.gemm_leaf_partial(c, 0, 1, As[i], Bs[i])[None])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    for _ in range(args.steps):
+        flush.zero_()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+    assert B.last_device_status(c) == B.ISO_OK
+    ms = max_over_ranks(statistics.mean(ts), world, dev)
+    if rank == 0:
+        config = bench_config(world)
+        config.update(parallelism=f"tp{world}", global_batch=M_TOKENS,
+                      exchange="all-gather of fp32 subtree roots (transport only), then the tree combine")
+        line = dict(metric=METRIC, value=step_flops() / (ms * 1e-3) / 1e12, unit="TFLOP/s", n_gpus=world,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="strong",
+                    vs_baseline=None, dtype="bf16", data="synthetic", config=config, clocks=clocks,
+                    gpu_launches=args.steps * len(SHAPES) * 2)
+        print(json.dumps(rnd(line)), flush=True)
+
+
 def time_call(fn, iters, warm, stream, flush=None):
     import torch
     for _ in range(warm):
@@ -674,6 +736,8 @@ def main():
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--details", default=None, help="write the full secondary measurements to this JSON file")
+    ap.add_argument("--parallel", default="dp", choices=["dp", "tp"],
+                    help="dp: data-parallel replicas (the default step); tp: row-parallel TP over K-leaves")
     ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small",
                                                      "diagnostics"],
                     help="run one workload --steps times without timing (for ncu) and exit")
@@ -691,7 +755,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     try:
-        run_ours(args, rank, world)
+        if args.parallel == "tp":
+            run_tp(args, rank, world)
+        else:
+            run_ours(args, rank, world)
     finally:
         if world > 1:
             import torch.distributed as dist
