@@ -55,7 +55,8 @@ typedef enum {
   ISO_ERR_CUDA = 8,              /* a CUDA runtime call failed */
   ISO_ERR_DEVICE_TIMEOUT = 9,    /* a device-side wait ran out of time */
   ISO_ERR_NOT_IMPLEMENTED = 10,
-  ISO_ERR_BAD_TOKEN_ID = 11      /* a token id outside [0, V) reached the device */
+  ISO_ERR_BAD_TOKEN_ID = 11,     /* a token id outside [0, V) reached the device */
+  ISO_ERR_DEVICE_CHECK = 12      /* debug build only: a device-side bounds check failed */
 } iso_status;
 
 typedef enum { ISO_TREE_BALANCED_BINARY = 0 } iso_tree_schedule;
@@ -98,8 +99,12 @@ int iso_contract_leaf_count(const iso_contract* c);
 iso_status iso_sha256(const void* data, size_t n, uint8_t digest[32]);
 const char* iso_status_string(iso_status s);
 /* Synchronizes `stream`, then reads and clears the current device's status
- * word: ISO_OK, ISO_ERR_DEVICE_TIMEOUT, ISO_ERR_BAD_TOKEN_ID or ISO_ERR_SHAPE
- * (a device-side shape check failed, e.g. iso_attention's sequence table). */
+ * word: ISO_OK, ISO_ERR_DEVICE_TIMEOUT, ISO_ERR_BAD_TOKEN_ID, ISO_ERR_SHAPE
+ * (a device-side shape check failed, e.g. iso_attention's sequence table) or,
+ * in the debug build (libiso_debug.so, compiled with -DISO_DEBUG: the same
+ * entry points with a bounds check before every data-dependent global store
+ * and gather, each of which records this status and skips the access instead
+ * of trapping), ISO_ERR_DEVICE_CHECK. */
 iso_status iso_last_device_status(iso_stream stream);
 
 /* ---------------------------------------------------------------- iso_gemm

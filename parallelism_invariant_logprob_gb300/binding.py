@@ -22,7 +22,7 @@ STATUS_NAMES = {
     0: "ISO_OK", 1: "ISO_ERR_INVALID_ARG", 2: "ISO_ERR_SHAPE", 3: "ISO_ERR_ALIGNMENT",
     4: "ISO_ERR_UNPROVEN_TOPOLOGY", 5: "ISO_ERR_UNSUPPORTED", 6: "ISO_ERR_CONTRACT_MISMATCH",
     7: "ISO_ERR_WORKSPACE", 8: "ISO_ERR_CUDA", 9: "ISO_ERR_DEVICE_TIMEOUT", 10: "ISO_ERR_NOT_IMPLEMENTED",
-    11: "ISO_ERR_BAD_TOKEN_ID",
+    11: "ISO_ERR_BAD_TOKEN_ID", 12: "ISO_ERR_DEVICE_CHECK",
 }
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
@@ -107,22 +107,22 @@ class Library:
             raise IsoError(status, what)
 
 
-_LIB = None
+_LIB = {}
 
 
-def load(build_if_missing: bool = True) -> Library:
-    """Load the CUDA library; builds it in-tree if absent.  Raises if neither works."""
-    global _LIB
-    if _LIB is not None:
-        return _LIB
-    path = library_path()
+def load(build_if_missing: bool = True, debug: bool = False) -> Library:
+    """Load the CUDA library (``debug``: the bounds-checked build ``libiso_debug.so``); builds it
+    in-tree if absent.  Raises if neither works."""
+    if debug in _LIB:
+        return _LIB[debug]
+    path = library_path(debug)
     if not os.path.exists(path):
         if not build_if_missing:
             raise FileNotFoundError(f"CUDA library not built: {path}")
         from .build_lib import build
-        build()
-    _LIB = Library(path)
-    return _LIB
+        build(debug=debug)
+    _LIB[debug] = Library(path)
+    return _LIB[debug]
 
 
 # ------------------------------------------------------------------ contract

@@ -81,6 +81,7 @@ struct AttnParams {
   const int32_t* k_start;  // [B+1]
   const int32_t* pos0;     // [B]
   int B, Hq, Hkv;
+  int Tq;   // query rows of the call (the debug build's store bound)
   int gp;   // query heads per tile (the G = Hq / Hkv heads of a KV group when G divides 128, else 1)
   int tpt;  // tokens per tile, 128 / gp: tile row r is token r / gp, head r % gp of the group
   float scale_log2e;  // scale * log2(e), rounded to fp32
@@ -477,8 +478,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tmem_ld_wait_only();
 #pragma unroll
       for (int q = 0; q < AT_D / 32; ++q) tmem_ld_tie(o + q * 32);
-      if (row_valid) {
-        const int64_t row = q0 + (tileA + t) * tpt + tok;
+      const int64_t row = q0 + (tileA + t) * tpt + tok;
+      if (row_valid && ISO_DCHECK(row >= 0 && row < p.Tq && head < p.Hq, p.status)) {
         __nv_bfloat16* dst = p.out + (row * p.Hq + head) * AT_D;
         const float inv_l = __frcp_rn(l);
 #pragma unroll
@@ -544,6 +545,7 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   p.k_start = k_start;
   p.pos0 = pos0;
   p.B = B;
+  p.Tq = Tq;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.gp = gp;

@@ -235,6 +235,7 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.b_tile_cols = BN;
   p.b_box2_off = 64;
   set_a_rows(p, 128);
+  p.out_rows = M;
   p.status = device_status_ptr();
   p.timeout_ns = wait_timeout_ns();
   return p;
@@ -354,6 +355,7 @@ iso_status iso_last_device_status(iso_stream stream) {
   const unsigned int zero = 0;
   if (cudaMemcpy(device_status_ptr(), &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ISO_ERR_CUDA;
   if (w & kDevTimeout) return ISO_ERR_DEVICE_TIMEOUT;
+  if (w & kDevCheck) return ISO_ERR_DEVICE_CHECK;
   if (w & kDevBadToken) return ISO_ERR_BAD_TOKEN_ID;
   if (w) return ISO_ERR_SHAPE;
   return ISO_OK;
@@ -795,6 +797,7 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   p.E = E;
   p.out = hb;
   p.ldo = F;
+  p.out_rows = P;
   if (kMoePairs) {
     p.pair = 1;
     set_a_rows(p, 128);
@@ -808,6 +811,7 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   q.E = E;
   q.out = y;
   q.ldo = H;
+  q.out_rows = P;
   q.row_scatter = perm;
   if (kMoePairs) {
     q.pair = 1;

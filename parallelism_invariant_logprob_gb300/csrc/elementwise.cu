@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
 __global__ void __launch_bounds__(MOE_PERM_THREADS)
     moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, const int32_t* __restrict__ hist,
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
-                       int32_t* __restrict__ perm) {
+                       int32_t* __restrict__ perm, unsigned int* status) {
   constexpr int NW = MOE_PERM_THREADS / 32;
   __shared__ int base[MOE_MAX_EXPERTS];
   __shared__ int wcnt[NW][MOE_MAX_EXPERTS];
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(MOE_PERM_THREADS)
     if (id >= 0) {
       int pos = base[id] + rank;
       for (int w = 0; w < warp; ++w) pos += wcnt[w][id];
-      perm[pos] = static_cast<int32_t>(p);
+      if (ISO_DCHECK(pos >= 0 && pos < P, status)) perm[pos] = static_cast<int32_t>(p);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -430,12 +430,14 @@ __global__ void __launch_bounds__(MOE_PERM_THREADS)
 // x_perm[i] = x[perm[i] / k]: one warp per row, 16-byte vectors, 8 loads per lane in flight
 // before their stores (one load at a time per lane left the copy latency-bound).
 __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm,
-                                  const int32_t* __restrict__ total, int k, int H, __nv_bfloat16* __restrict__ xp) {
+                                  const int32_t* __restrict__ total, int k, int H, __nv_bfloat16* __restrict__ xp,
+                                  int64_t P, unsigned int* status) {
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int n = *total;
   const int nvec = H / 8;
   for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < n; i += gridDim.x * warps) {
+    if (!ISO_DCHECK(i < P && perm[i] >= 0 && perm[i] < P, status)) continue;
     const int t = perm[i] / k;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(i) * H);
@@ -634,7 +636,7 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || C == 0) return e;
   moe_scatter_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, counts, offsets,
-                                                                                perm);
+                                                                                perm, device_status_ptr());
   return cudaGetLastError();
 }
 
@@ -642,7 +644,8 @@ cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int3
                               int H, uint16_t* xp, cudaStream_t s) {
   const int threads = 256;
   moe_gather_kernel<<<grid_for(max_rows * 32, threads, sm_count() * 16), threads, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), perm, total, k, H, reinterpret_cast<__nv_bfloat16*>(xp));
+      reinterpret_cast<const __nv_bfloat16*>(x), perm, total, k, H, reinterpret_cast<__nv_bfloat16*>(xp), max_rows,
+      device_status_ptr());
   return cudaGetLastError();
 }
 

@@ -861,10 +861,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             hw[q].z = pack_bf16x2(hv[4], hv[5]);
             hw[q].w = pack_bf16x2(hv[6], hv[7]);
           }
+          const bool h_ok = row_ok && ISO_DCHECK(row < p.out_rows, p.status);
           if (p.epi_staged) {
-            store_rows_staged<HC / 8>(wstage, lane, hw, row_ok ? row : -1, reinterpret_cast<__nv_bfloat16*>(p.out),
+            store_rows_staged<HC / 8>(wstage, lane, hw, h_ok ? row : -1, reinterpret_cast<__nv_bfloat16*>(p.out),
                                       p.ldo, n0 + h0, n0 + h0 + HC);
-          } else if (row_ok) {
+          } else if (h_ok) {
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
             for (int q = 0; q < HC / 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + h0 + q * 8) = hw[q];
@@ -893,7 +894,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             // box's rows) for the cluster combine after the main loop
             // as column pairs: pair q of row r is the 8-byte word (q a_rows + r), so one warp's
             // rows are consecutive words and a combine thread reads a pair in one load
-            if (row_in_tile < p.a_rows) {
+            if (row_in_tile < p.a_rows && ISO_DCHECK(c0 + RC <= BN, p.status)) {
 #pragma unroll
               for (int i = 0; i < RC; i += 2)
                 *reinterpret_cast<float2*>(&parked[2 * (((c0 + i) >> 1) * p.a_rows + row_in_tile)]) =
@@ -908,17 +909,19 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
               w[q].z = pack_bf16x2(u2f(v[q * 8 + 4]), u2f(v[q * 8 + 5]));
               w[q].w = pack_bf16x2(u2f(v[q * 8 + 6]), u2f(v[q * 8 + 7]));
             }
-            const int orow = row_ok ? ((p.row_scatter != nullptr) ? p.row_scatter[row] : row) : -1;
+            int orow = row_ok ? ((p.row_scatter != nullptr) ? p.row_scatter[row] : row) : -1;
+            if (orow >= 0 && !ISO_DCHECK(orow < p.out_rows, p.status)) orow = -1;
             store_rows_staged<RC / 8>(wstage, lane, w, orow, reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0 + c0,
                                       p.N);
           } else if (row_ok) {
             if (EPI == EPI_BF16) {
               const int orow = (p.row_scatter != nullptr) ? p.row_scatter[row] : row;
+              const bool o_ok = ISO_DCHECK(orow >= 0 && orow < p.out_rows, p.status);
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
 #pragma unroll
               for (int q = 0; q < RC / 8; ++q) {
                 const int col = n0 + c0 + q * 8;
-                if (col < p.N) {
+                if (o_ok && col < p.N) {
                   uint4 w;
                   w.x = pack_bf16x2(u2f(v[q * 8 + 0]), u2f(v[q * 8 + 1]));
                   w.y = pack_bf16x2(u2f(v[q * 8 + 2]), u2f(v[q * 8 + 3]));
@@ -930,10 +933,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             } else {
               float* dst = reinterpret_cast<float*>(p.out) + U.chunk * p.out_group_stride +
                            static_cast<int64_t>(row) * p.ldo;
+              const bool o_ok = ISO_DCHECK(row < p.out_rows, p.status);
 #pragma unroll
               for (int q = 0; q < RC / 4; ++q) {
                 const int col = n0 + c0 + q * 4;
-                if (col < p.N)
+                if (o_ok && col < p.N)
                   *reinterpret_cast<uint4*>(dst + col) = make_uint4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
               }
             }
@@ -996,7 +1000,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tb.push_free(root);
         }
       }
-      if (EPI == EPI_LOGPROB && ok && row_ok) {
+      if (EPI == EPI_LOGPROB && ok && row_ok && ISO_DCHECK(U.chunk < p.num_chunks && row < p.M, p.status)) {
         p.ws_stats[static_cast<int64_t>(U.chunk) * p.M + row] = make_float2(run_m, run_s);
         if (have_sel) p.ws_zsel[row] = zsel;
       }
@@ -1034,6 +1038,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           if (e < total) {
             const int row = e / npairs;
             const int pr = (c_base >> 1) + (e - row * npairs);  // column pair within the tile
+            if (!ISO_DCHECK(row < p.a_rows && pr < BN / 2, p.status)) continue;
 #pragma unroll
             for (int g = 0; g < MAX_CLUSTER_GROUPS; ++g)
               if (g < R)
@@ -1046,7 +1051,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           if (e >= total) continue;
           const int row = e / npairs;
           const int col = U.n_tile0 * BN + c_base + 2 * (e - row * npairs);
-          if (col >= p.N) continue;
+          if (col >= p.N || !ISO_DCHECK(row < p.out_rows && row < p.a_rows, p.status)) continue;
           // balanced tree over the groups, left operand = lower group (fp32 rn adds)
 #pragma unroll
           for (int w = 1; w < MAX_CLUSTER_GROUPS; w *= 2) {

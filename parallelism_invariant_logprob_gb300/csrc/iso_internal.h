@@ -14,7 +14,17 @@ enum : unsigned int {
   kDevTimeout = 1u << 0,   // an mbarrier wait ran out of time
   kDevBadToken = 1u << 1,  // a token id outside [0, V)
   kDevBadShape = 1u << 2,  // a device-side shape check failed
+  kDevCheck = 1u << 3,     // a debug-build bounds check failed (the access was skipped)
 };
+
+// Device-side bounds checks of the debug build (-DISO_DEBUG, libiso_debug.so): a failed check
+// records kDevCheck in the status word and the guarded access is skipped, instead of trapping
+// (a trap would take the context down).  In the normal build the condition is not evaluated.
+#ifdef ISO_DEBUG
+#define ISO_DCHECK(cond, status) ((cond) ? true : (atomicOr((status), ::iso::kDevCheck), false))
+#else
+#define ISO_DCHECK(cond, status) true
+#endif
 
 // Output tile of one CTA: 128 rows (TMEM lanes) x 128 columns; K staged in
 // blocks of 64 (one 128-byte swizzle row of bf16).
@@ -109,6 +119,7 @@ struct GemmParams {
   int group_m;     // GEMM raster: m-blocks per group
   void* out;
   int64_t ldo;
+  int64_t out_rows;  // rows of `out` (per leaf group) the epilogue may write: the debug build's store bound
   const int32_t* row_scatter;  // grouped down projection: destination row of each permuted row
   // logprob
   const int32_t* ids;
