@@ -770,7 +770,7 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   int32_t* hist = reinterpret_cast<int32_t*>(base + lay.hist);
   const int64_t P = static_cast<int64_t>(T) * k;
   // the down projection's leaves of 96 k (F = 768 with 8 leaves) run on whole-leaf stages
-  const bool leaf_stage = F / L == LS_LEAF && !kMoePairs;
+  const bool leaf_stage = F / L == LS_LEAF && L <= TMEM_TREE_LEAVES && !kMoePairs;
   CUtensorMap tX, tW1, tH, tH2, tW2;
   iso_status st = make_tmap_bf16(&tX, xp, P, H, H, BK, BM);
   if (st == ISO_OK) st = make_tmap_bf16(&tW1, W1, static_cast<uint64_t>(E) * H, 2 * F, 2 * F, 64, BK);

@@ -383,6 +383,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 "8 epilogue warps: single CTA, bf16/SwiGLU outputs");
   static_assert(GEMM_THREADS_FUSED == 384 && GEMM_THREADS_EPI8 == 384, "12-warp launches");
   static_assert(!LS || (EPI == EPI_BF16 && !PAIR && !FUSED && EPW == 8), "whole-leaf stages: the 8-warp bf16 path");
+  // The 16-leaf park exists only in the 4-epilogue-warp instances (the host never launches an
+  // 8-warp instance with p.spill), so the 8-warp epilogues carry none of its code.
+  const bool spill = (EPW == 4) && p.spill != 0;
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
@@ -651,9 +654,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 }
               }
             }
-            const int nm = tmem_merges_after_leaf(leaf, p.L, p.spill);
+            const int nm = tmem_merges_after_leaf(leaf, p.L, spill);
             for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
-            if (p.spill && leaf == p.L / 2 - 1) tb.push_free(tb.pop());  // parked in shared memory
+            if (spill && leaf == p.L / 2 - 1) tb.push_free(tb.pop());  // parked in shared memory
             if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
           }
         }
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           }
           fill_par ^= 1u << b;
           tc_fence_after();
-          const int nm = tmem_merges_after_leaf(l, p.L, p.spill);
+          const int nm = tmem_merges_after_leaf(l, p.L, spill);
           for (int m = 0; m < nm; ++m) {
             const int rb = tb.pop();
             const int lb = tb.top();
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             release_tmem_buf<PAIR>(buf_free, rb, lane);
             tb.push_free(rb);
           }
-          if (p.spill && l == p.L / 2 - 1) {
+          if (spill && l == p.L / 2 - 1) {
             // park the root of leaves [0, L/2): this warp's columns of its rows (the columns it
             // merges) into shared memory, then give the TMEM buffer back
             const int sb = tb.pop();
@@ -835,7 +838,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < 2 * HC / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
 #pragma unroll
             for (int i = 0; i < HC; ++i) {
               v[i] = f2u(__fadd_rn(parked[(h0 + i) * BM + row_in_tile], u2f(v[i])));
@@ -881,7 +884,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < RC / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
 #pragma unroll
             for (int i = 0; i < RC; ++i) v[i] = f2u(__fadd_rn(parked[(c0 + i) * BM + row_in_tile], u2f(v[i])));
           }
@@ -953,7 +956,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           tmem_ld_wait_only();
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (p.spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
+          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
 #pragma unroll
             for (int i = 0; i < BN; ++i) v[i] = f2u(__fadd_rn(parked[i * BM + row_in_tile], u2f(v[i])));
           }
@@ -1205,7 +1208,7 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
                        cudaStream_t s, const CUtensorMap* tmA2) {
   const CUtensorMap& a2 = tmA2 != nullptr ? *tmA2 : tmA;  // unused unless p.leaf_stage
   if (p.leaf_stage) {
-    if (epi != EPI_BF16 || p.pair || p.a_transform || tmA2 == nullptr || p.leaf_len != LS_LEAF)
+    if (epi != EPI_BF16 || p.pair || p.a_transform || tmA2 == nullptr || p.leaf_len != LS_LEAF || p.spill)
       return ISO_ERR_INVALID_ARG;
     return launch_one<EPI_BF16, false, false, 8, true>(tmA, tmB, p, max_units, s, a2);
   }
@@ -1219,7 +1222,7 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
   // short leaves: 8 epilogue warps (the expert layer's grouped GEMMs: 1.07 -> 0.94 ms per layer)
   switch (epi) {
     case EPI_BF16:
-      if (!pair && p.leaf_len <= EPI8_MAX_LEAF_BF16)
+      if (!pair && !p.spill && p.leaf_len <= EPI8_MAX_LEAF_BF16)
         return launch_one<EPI_BF16, false, false, 8>(tmA, tmB, p, max_units, s, a2);
       return pair ? launch_one<EPI_BF16, true>(tmA, tmB, p, max_units, s, a2)
                   : launch_one<EPI_BF16, false>(tmA, tmB, p, max_units, s, a2);
@@ -1227,7 +1230,7 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
       return pair ? launch_one<EPI_F32, true>(tmA, tmB, p, max_units, s, a2)
                   : launch_one<EPI_F32, false>(tmA, tmB, p, max_units, s, a2);
     case EPI_SWIGLU:
-      if (!pair && p.leaf_len <= EPI8_MAX_LEAF_SWIGLU)
+      if (!pair && !p.spill && p.leaf_len <= EPI8_MAX_LEAF_SWIGLU)
         return launch_one<EPI_SWIGLU, false, false, 8>(tmA, tmB, p, max_units, s, a2);
       return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s, a2)
                   : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s, a2);
