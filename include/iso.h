@@ -361,7 +361,14 @@ iso_status iso_mismatch_diagnostics(const iso_contract* c, const float* logp_tra
  * W, ids) bit for bit; ws: iso_rmsnorm_selected_logprob_workspace(c, T, V) bytes
  * (the per-row factors first, then the logprob workspace; with less room than
  * that but at least the factors plus iso_selected_logprob_min_workspace the
- * chunk-unit schedule runs, same bits).  Other errors as the unfused calls. */
+ * chunk-unit schedule runs, same bits).  Other errors as the unfused calls.
+ * Speed: the fused form never writes or re-reads the normalised activations,
+ * but it normalises each A tile again for every 128-column output tile, so
+ * its extra work grows with N / 128: it pays only for narrow outputs (a few
+ * column tiles).  For the wide shapes of an LM (measured on GB300: M = 4096,
+ * K = N = 4096: 0.975 ms fused against 0.325 ms for iso_rmsnorm + iso_gemm;
+ * the T = 4096, V = 151936 logprob: 10.5 ms against 3.06 ms) the separate
+ * stages are the fast path, with the same bits. */
 size_t iso_rmsnorm_gemm_workspace(const iso_contract* c, int M);
 iso_status iso_rmsnorm_gemm(const iso_contract* c, const iso_bf16* x, const iso_bf16* gamma, float eps,
                             const iso_bf16* B, int64_t ldb, iso_bf16* C, int64_t ldc, int M, int N, int K, void* ws,
