@@ -688,6 +688,10 @@ def profile_target(target: str, calls: int):
         X, W = inputs.gemm_inputs(M_TOKENS, 4096, 12288, seed=100, device=dev)
         C = torch.empty(M_TOKENS, 12288, dtype=torch.bfloat16, device=dev)
         fn = lambda: B.gemm(c, X, W, out=C)
+    elif target == "gemm_m1":  # a decode-size GEMM: one row, 4096 x 4096 (leaf groups on clusters)
+        X, W = inputs.gemm_inputs(1, 4096, 4096, seed=100, device=dev)
+        C = torch.empty(1, 4096, dtype=torch.bfloat16, device=dev)
+        fn = lambda: B.gemm(c, X, W, out=C)
     elif target == "logprob":
         h, W, ids = logprob_workload(c, dev)
         out = torch.empty(LP_T, dtype=torch.float32, device=dev)
@@ -738,8 +742,8 @@ def main():
     ap.add_argument("--details", default=None, help="write the full secondary measurements to this JSON file")
     ap.add_argument("--parallel", default="dp", choices=["dp", "tp"],
                     help="dp: data-parallel replicas (the default step); tp: row-parallel TP over K-leaves")
-    ap.add_argument("--profile-target", choices=["gemm", "logprob", "moe", "rmsnorm", "attention", "attention_small",
-                                                     "diagnostics"],
+    ap.add_argument("--profile-target", choices=["gemm", "gemm_m1", "logprob", "moe", "rmsnorm", "attention",
+                                                     "attention_small", "diagnostics"],
                     help="run one workload --steps times without timing (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_target:
