@@ -343,6 +343,9 @@ def run_ours(args, rank, world):
                 with open(args.details, "w") as f:
                     json.dump(extra, f, indent=1)
             line["secondary"] = secondary_summary(extra)
+            bw = dict(extra["bitwise"])
+            bw["e2e_host_results_vs_resident"] = 0  # asserted above: the host copies equal the resident results
+            line["bitwise"] = dict(mismatching_elements_total=sum(bw.values()), checks=len(bw), detail=bw)
             line["logprob"] = logprob_summary(extra["logprob"])  # last: the end of the line is what logs keep
         print(json.dumps(rnd(line)), flush=True)
 
@@ -357,7 +360,8 @@ def secondary_summary(x):
                 rmsnorm_hbm_frac=x["rmsnorm"]["roofline_frac"],
                 attention=dict(prefill_tc_frac=at["roofline_frac"], decode_hbm_frac=at["decode"]["roofline_frac"]),
                 moe=dict(ms=x["moe"]["ms"], tflops=x["moe"]["tflops"], tc_frac=x["moe"]["roofline_frac"]),
-                diagnostics_ms=x["diagnostics"]["ms"])
+                diagnostics_ms=x["diagnostics"]["ms"], config1_us=x["config1"]["us"],
+                rollout=dict(tokens_per_s=x["rollout"]["tokens_per_s"], tc_frac=x["rollout"]["roofline_frac"]))
 
 
 def logprob_summary(lp):
@@ -431,6 +435,78 @@ def run_tp(args, rank, world):
         print(json.dumps(rnd(line)), flush=True)
 
 
+def mismatches(a, b) -> int:
+    """Elements whose bits differ (bf16 / fp32 / int tensors of the same shape)."""
+    import torch
+    if a.dtype in (torch.bfloat16, torch.float16):
+        a, b = a.view(torch.int16), b.view(torch.int16)
+    elif a.dtype == torch.float32:
+        a, b = a.view(torch.int32), b.view(torch.int32)
+    return int((a != b).sum().item())
+
+
+def config1_and_rollout(c, dev, stream, peaks, flush):
+    """Config 1 (A [32 x 2048] x B [2048 x 512], 4 leaves): time per call and its bitwise checks
+    (rows alone and in sub-batches of 1 / 7 / 32, leaf partials + combine for R = 1, 2, 4).
+    Config 5 (the packed rollout batch, 64 sequences of ~U[1, 8192] tokens, 259,611 rows):
+    iso_rmsnorm + iso_selected_logprob over the packed prefill, and sampled tokens as one-token
+    decode calls, which must give the prefill's bits."""
+    import torch
+    from parallelism_invariant_logprob_gb300 import binding as B
+    from parallelism_invariant_logprob_gb300 import inputs
+    out, bits = {}, {}
+    c4 = B.Contract(4)
+    A, Bm = inputs.gemm_inputs(32, 2048, 512, seed=0, device=dev)
+    C = B.gemm(c4, A, Bm)
+    t = time_call(lambda: B.gemm(c4, A, Bm, out=C, stream=stream), 20, 3, stream)
+    rows = 0
+    for M in (1, 7, 32):
+        for r0 in range(0, 32 - M + 1, max(1, M)):
+            rows += mismatches(B.gemm(c4, A[r0:r0 + M].contiguous(), Bm), C[r0:r0 + M])
+    tp = 0
+    for R in (1, 2, 4):
+        Kl = 2048 // R
+        S = torch.stack([B.gemm_leaf_partial(c4, r, R, A[:, r * Kl:(r + 1) * Kl].contiguous(), Bm[r * Kl:(r + 1) * Kl])
+                         for r in range(R)])
+        tp += mismatches(B.tree_combine(c4, S), C)
+    out["config1"] = dict(workload="A [32 x 2048] x B [2048 x 512], 4 leaves", us=t * 1e3,
+                          tflops=2.0 * 32 * 2048 * 512 / (t * 1e-3) / 1e12)
+    bits["config1_rows_m1_m7_m32"] = rows
+    bits["config1_partial_combine_r1_r2_r4"] = tp
+    # config 5
+    H, V = 4096, 151936
+    lens = inputs.sequence_lengths(64, 8192, seed=4)
+    total = sum(lens)
+    states = inputs.normal_bf16((total, H), 1.0, seed=5, device=dev)
+    _, gamma = inputs.rmsnorm_inputs(1, H, seed=6)
+    gamma = gamma.to(dev)
+    W = inputs.normal_bf16((H, V), 0.02, seed=7, device=dev)
+    ids = inputs.uniform_ids(total, V, seed=8, device=dev)
+    h = torch.empty_like(states)
+    lp = torch.empty(total, dtype=torch.float32, device=dev)
+    ws = torch.empty(B.selected_logprob_workspace(c, total, V), dtype=torch.uint8, device=dev)
+
+    def prefill():
+        B.rmsnorm(c, states, gamma, 1e-6, out=h, stream=stream)
+        B.selected_logprob(c, h, W, ids, out=lp, ws=ws, stream=stream)
+    tp5 = time_call(prefill, 3, 1, stream)
+    g = torch.Generator().manual_seed(9)
+    sample = torch.randperm(total, generator=g)[:256].tolist()
+    ws1 = torch.empty(B.selected_logprob_workspace(c, 1, V), dtype=torch.uint8, device=dev)
+    h1 = torch.empty(1, H, dtype=torch.bfloat16, device=dev)
+    dec = torch.empty(len(sample), 4, dtype=torch.float32, device=dev)
+    for i, t_ in enumerate(sample):
+        B.rmsnorm(c, states[t_:t_ + 1], gamma, 1e-6, out=h1, stream=stream)
+        B.selected_logprob(c, h1, W, ids[t_:t_ + 1], out=dec[i, :1], ws=ws1, stream=stream)
+    bits["rollout_decode_vs_prefill_256_tokens"] = mismatches(dec[:, 0].contiguous(), lp[torch.tensor(sample, device=dev)])
+    fl = 2.0 * total * H * V
+    out["rollout"] = dict(workload=f"64 packed sequences, {total} tokens: iso_rmsnorm + iso_selected_logprob, H=4096, "
+                                   f"V=151936", ms=tp5, tokens_per_s=total / (tp5 * 1e-3),
+                          tflops=fl / (tp5 * 1e-3) / 1e12, roofline_frac=fl / (peaks["tc"] * 1e12) / (tp5 * 1e-3))
+    del states, h, W, ws
+    return out, bits
+
+
 def time_call(fn, iters, warm, stream, flush=None):
     import torch
     for _ in range(warm):
@@ -458,6 +534,7 @@ def secondary(c, dev, stream, peaks, rank):
     from parallelism_invariant_logprob_gb300 import binding as B
     from parallelism_invariant_logprob_gb300 import inputs
     out = {}
+    bits = {}
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     # selected-token logprob, T = 4096, H = 4096, V = 151936; the hidden states are RMS-normalised
@@ -515,9 +592,10 @@ def secondary(c, dev, stream, peaks, rank):
         st_all, z_all = torch.cat(stats, 0), torch.stack(zs)
         t_comb = time_call(lambda: B.selected_logprob_combine(c, v0s, st_all, z_all, ids, LP_V, out=lp_out, stream=stream),
                            5, 2, stream, flush)
+        vp_bad = mismatches(lp_out, B.selected_logprob(c, h, W, ids))
+        bits[f"vocab_parallel_R{R}"] = vp_bad
         vp[f"R{R}"] = dict(shard_v0=v0s, ms_partial_max=max(parts), ms_partial_min=min(parts), ms_combine=t_comb,
-                           ms_single_call_over_R=t / R,
-                           same_bits_as_single_call=bool(torch.equal(lp_out, B.selected_logprob(c, h, W, ids))))
+                           ms_single_call_over_R=t / R, same_bits_as_single_call=vp_bad == 0)
     out["logprob"]["vocab_parallel"] = vp
     del h, W, ids, ws, xr, hn, ws_f
 
@@ -554,6 +632,12 @@ def secondary(c, dev, stream, peaks, rank):
                 B.tree_combine(c, S, out=Cc, stream=stream)
             tt = time_call(tp, 3, 1, stream, flush)
             gm[f"TP{R}_M4096_K{K}_N{N}"] = dict(ms=tt, tflops=2.0 * M_TOKENS * K * N / (tt * 1e-3) / 1e12)
+            full = B.gemm(c, X, Wt)
+            bits[f"tp{R}_partials_vs_single_{K}x{N}"] = mismatches(Cc, full)
+            if R == 2:  # rows alone and in a 7-row batch against the same rows of the 4096-row product
+                bits[f"rows_m1_m7_vs_m4096_{K}x{N}"] = (
+                    sum(mismatches(B.gemm(c, X[r:r + 1].contiguous(), Wt), full[r:r + 1]) for r in (0, 2047, 4095)) +
+                    mismatches(B.gemm(c, X[100:107].contiguous(), Wt), full[100:107]))
         del X, Wt
     out["gemm_sweep"] = gm
 
@@ -582,6 +666,7 @@ def secondary(c, dev, stream, peaks, rank):
                               hbm_gbs=byt / (tt * 1e-3) / 1e9, bound="fp64")
 
     out["attention"] = attention_measure(c, dev, stream, peaks, flush)
+    bits["attention_decode_vs_prefill_64_rows"] = out["attention"]["decode_vs_prefill_mismatches"]
 
     # MoE expert layer: T=8192, H=2048, E=128, F=768, k=8
     T, H, E, F, k = 8192, 2048, 128, 768, 8
@@ -594,6 +679,11 @@ def secondary(c, dev, stream, peaks, rank):
     fl = 2.0 * T * k * (H * 2 * F + F * H)
     out["moe"] = dict(workload="T=8192, H=2048, E=128, F=768, k=8", ms=tt, tflops=fl / (tt * 1e-3) / 1e12,
                       roofline_frac=fl / (peaks["tc"] * 1e12) / (tt * 1e-3))
+    moe_base = om.clone()
+    bits["moe_partitions_p2_p8_random"] = sum(
+        mismatches(B.grouped_gemm_moe(c, xm, ids_m, w_m, W1, W2, expert_partition=part, ws=wsm, stream=stream), moe_base)
+        for part in ([e * 2 // E for e in range(E)], [e * 8 // E for e in range(E)],
+                     inputs.random_partition(E, 4, seed=7).tolist()))
     # expert parallelism: R ranks own contiguous expert sets; a rank's time is its partial (the slot
     # rows of its experts), the job's the slowest partial plus the combine after the exchange
     ep = {}
@@ -606,11 +696,16 @@ def secondary(c, dev, stream, peaks, rank):
             parts.append(time_call(lambda: B.moe_experts_partial(c, xm, ids_m, W1, W2, mask, y_slots=ys, ws=ws_p,
                                                                   stream=stream), 5, 2, stream, flush))
         t_comb = time_call(lambda: B.moe_combine(c, ys.view(T, k, H), w_m, out=om, stream=stream), 5, 2, stream, flush)
+        ep_bad = mismatches(om, B.grouped_gemm_moe(c, xm, ids_m, w_m, W1, W2, ws=wsm, stream=stream))
+        bits[f"expert_parallel_R{R}"] = ep_bad
         ep[f"R{R}"] = dict(ms_partial_max=max(parts), ms_partial_min=min(parts), ms_combine=t_comb,
-                           ms_layer_over_R=tt / R,
-                           same_bits_as_layer=bool(torch.equal(om.view(torch.int16), B.grouped_gemm_moe(
-                               c, xm, ids_m, w_m, W1, W2, ws=wsm, stream=stream).view(torch.int16))))
+                           ms_layer_over_R=tt / R, same_bits_as_layer=ep_bad == 0)
     out["moe"]["expert_parallel"] = ep
+    del xm, W1, W2, wsm, ys, ws_p
+    extra, bits5 = config1_and_rollout(c, dev, stream, peaks, flush)
+    out.update(extra)
+    bits.update(bits5)
+    out["bitwise"] = bits
     return out
 
 
@@ -671,6 +766,7 @@ def attention_measure(c, dev, stream, peaks, flush):
     td = time_call(lambda: B.attention(c, Qd, K, V, dq, ks, dpos, scale, max_q_rows=1, out=od, lse=ld, stream=stream),
                    5, 2, stream, flush)
     byt = 2.0 * 2 * ATT_HKV * ATT_D * sum(lens) + 2.0 * 2 * len(lens) * ATT_HQ * ATT_D
+    r["decode_vs_prefill_mismatches"] = mismatches(od, o[last]) + mismatches(ld, lse[last])
     r["decode"] = dict(workload=f"one row per sequence at its last position, {len(lens)} sequences", ms=td,
                        hbm_gbs=byt / (td * 1e-3) / 1e9, roofline_frac=byt / (peaks["hbm"] * 1e9) / (td * 1e-3),
                        bound="hbm")

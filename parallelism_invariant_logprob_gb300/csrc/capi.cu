@@ -525,6 +525,7 @@ static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, co
   p.chunk_tiles = tiles ? 1 : LP_CHUNK_TILES;                   // tiles per work unit
   p.num_chunks = tiles ? lp_num_tiles(Vl) : lp_num_chunks(Vl);  // statistics entries per row
   p.num_units = p.m_blocks * p.num_chunks;
+  p.group_m = raster_group(p, H);  // row blocks whose hidden states share L2 (all of them up to ~48 MB)
   p.ids = ids;
   p.ws_stats = tiles ? tile_stats : chunk_stats;
   p.ws_zsel = zsel;

@@ -107,10 +107,17 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U,
     U.rows_valid = min(BM, p.M);
     U.chunk = g;
   } else if (p.unit_mode == UNIT_LOGPROB) {
-    // chunk-major: the row blocks working on one vocab chunk run together and
-    // share its W columns in L2.
-    const int chunk = u / p.m_blocks;
-    const int rb = u - chunk * p.m_blocks;
+    // Row-block groups whose hidden states fit L2 (group_m row blocks; all of them when the batch
+    // is small), chunk-major inside a group: the row blocks working on one vocab chunk run
+    // together and share its W columns in L2, and a group's A rows stay in L2 while the whole
+    // vocabulary streams past once per group.
+    const int per_group = p.group_m * p.num_chunks;
+    const int grp = u / per_group;
+    const int r = u - grp * per_group;
+    const int gm0 = grp * p.group_m;
+    const int gsz = min(p.group_m, p.m_blocks - gm0);
+    const int chunk = r / gsz;
+    const int rb = gm0 + (r - chunk * gsz);
     U.a_row0 = (rb * cl + rank) * BM;
     U.a_col0 = 0;
     U.b_row0 = 0;

@@ -214,3 +214,22 @@ def test_vocab_parallel_rejects_unaligned_shards(c8):
     stats = torch.zeros(63, T, 2, device=DEV)
     with pytest.raises(B.IsoError):
         B.selected_logprob_combine(c8, [0, 2500], stats, torch.zeros(2, T, device=DEV), ids, V)
+
+
+def test_logprob_rows_span_several_l2_groups():
+    """T = 7000 rows of H = 4096: more row blocks than one L2 raster group holds (the units run
+    group by group, chunk-major inside a group), with a ragged last group.  Each row's logprob is
+    the same bits as in a call of that row alone, and within 1e-3 of the oracle."""
+    c = B.Contract(8)
+    T, H, V = 7000, 4096, 2432 * 2 + 256
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=71, device=DEV)
+    full = B.selected_logprob(c, h, W, ids)
+    ws_min = torch.empty(B.selected_logprob_min_workspace(c, T, V), dtype=torch.uint8, device=DEV)
+    assert torch.equal(B.selected_logprob(c, h, W, ids, ws=ws_min), full)
+    rows = [0, 255, 256, 6143, 6144, 6999]
+    for r in rows:
+        assert torch.equal(B.selected_logprob(c, h[r:r + 1].contiguous(), W, ids[r:r + 1].contiguous()), full[r:r + 1]), r
+    idx = torch.tensor(rows, device=DEV)
+    ref = oracle.selected_logprob(bits(h[idx]), bits(W), ids[idx].cpu().numpy(), 8)["out"]
+    assert np.max(np.abs(full[idx].cpu().double().numpy() - ref)) <= 1e-3
+    assert B.last_device_status(c) == B.ISO_OK
