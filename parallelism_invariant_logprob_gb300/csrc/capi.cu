@@ -154,8 +154,8 @@ namespace {
 // A box rows and the stage count that fits the shared-memory budget (even, for the two producers).
 void set_a_rows(GemmParams& p, int a_rows) {
   p.a_rows = a_rows;
-  p.a_bytes = a_rows * BK * 2;
-  const int b_bytes = p.pair ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
+  p.a_bytes = a_rows * p.stage_k * 2;
+  const int b_bytes = p.pair ? p.stage_k * 64 * 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
   // the parked subtree root (spill), or a leaf group's root in cluster mode (the A box's rows only)
   const int reserve = p.spill ? SPILL_BYTES : (p.cluster > 1 ? a_rows * BN * 4 : 0);
   const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - reserve;
@@ -204,10 +204,29 @@ int raster_group(const GemmParams& p, int K) {
 constexpr int kPairMinLeafLen = 512;
 bool use_pair(int rows, int K, int L) { return rows > BM && K / L >= kPairMinLeafLen; }
 
+// One leaf: one producer thread feeds the pair, and 128-k stages halve its TMA instructions per
+// byte (measured on GB300, same-box A/B, bits identical: 4096 x 4096 x 4096 with one leaf 1192 ->
+// 1449 TFLOP/s).  With two producers the 64-k stages stay: 128-k stages release their shared
+// memory in larger steps, leaving fewer bytes in flight (8 leaves: 1389 -> 1361 TFLOP/s, the
+// T = 32768 logprob 28.4 -> 29.6 ms; 16 leaves, 2 stages: 1304 -> 885).
 void set_pair(GemmParams& p, int rows) {
   p.pair = 1;
   p.m_blocks = div_up(rows, 2 * BM);
+  if (p.L == 1 && p.leaf_len % 64 == 0) {
+    p.stage_k = PAIR_BK;
+    p.kb_per_leaf = div_up(p.leaf_len, PAIR_BK);
+  }
   set_a_rows(p, 128);
+}
+
+// A tensor maps of CTA pairs.  With 128-k stages a 3-D view {64 k, rows, K / 64 k-chunks} of the
+// row-major [rows x K] matrix (strides ld * 2 and 128 bytes), box {64, 128, 2}: one TMA brings a
+// CTA's [128 x 128] A stage as two consecutive 128-byte-swizzled [128 x 64] tiles.
+iso_status make_tmap_a(CUtensorMap* map, const GemmParams& p, const void* A, int rows, int K, int64_t ld) {
+  if (p.stage_k == PAIR_BK)
+    return make_tmap_bf16_3d(map, A, 64, static_cast<uint64_t>(rows), static_cast<uint64_t>(K / 64),
+                             static_cast<uint64_t>(ld), 64, 64, 128, 2);
+  return make_tmap_bf16(map, A, rows, K, ld, BK, static_cast<uint32_t>(p.a_rows));
 }
 
 // Smallest A box that covers a single row block of `rows` rows.
@@ -228,6 +247,7 @@ GemmParams base_params(int M, int N, int K, int L) {
   p.spill = L > TMEM_TREE_LEAVES ? 1 : 0;
   p.leaf_len = K / L;
   p.num_kb = div_up(K, BK);
+  p.stage_k = BK;
   p.kb_per_leaf = div_up(K / L, BK);
   p.m_blocks = div_up(M, BM);
   p.n_blocks = div_up(N, BN);
@@ -301,9 +321,9 @@ iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t 
   else if (use_pair(M, K, L))
     set_pair(p, M);
   CUtensorMap tA, tB;
-  iso_status st = make_tmap_bf16(&tA, A, M, K, lda, BK, static_cast<uint32_t>(p.a_rows));
+  iso_status st = make_tmap_a(&tA, p, A, M, K, lda);
   if (st != ISO_OK) return st;
-  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, BK);
+  st = make_tmap_bf16(&tB, B, K, N, ldb, 64, static_cast<uint32_t>(p.stage_k));
   if (st != ISO_OK) return st;
   p.unit_mode = UNIT_GEMM;
   p.num_units = p.m_blocks * p.n_blocks;
@@ -516,9 +536,9 @@ static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, co
     set_pair(p, T);
   }
   CUtensorMap tA, tB;
-  iso_status st = make_tmap_bf16(&tA, h, T, H, H, BK, static_cast<uint32_t>(p.a_rows));
+  iso_status st = make_tmap_a(&tA, p, h, T, H, H);
   if (st != ISO_OK) return st;
-  st = make_tmap_bf16(&tB, W, H, Vl, ldw, 64, BK);
+  st = make_tmap_bf16(&tB, W, H, Vl, ldw, 64, static_cast<uint32_t>(p.stage_k));
   if (st != ISO_OK) return st;
   const bool tiles = tile_stats != nullptr;
   p.unit_mode = UNIT_LOGPROB;
@@ -714,7 +734,6 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
 // The expert layer's grouped GEMMs run on single CTAs (units of 128 rows of one expert): its
 // leaves (H / L, F / L) are short, where CTA pairs lose (1.12 -> 1.84 ms per layer measured
 // at T = 8192, H = 2048, F = 768, E = 128, k = 8).
-constexpr bool kMoePairs = false;
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
 //   y_slots [P x H] bf16 (the full layer only; iso_moe_experts_partial writes the caller's) |
@@ -771,7 +790,7 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   int32_t* hist = reinterpret_cast<int32_t*>(base + lay.hist);
   const int64_t P = static_cast<int64_t>(T) * k;
   // the down projection's leaves of 96 k (F = 768 with 8 leaves) run on whole-leaf stages
-  const bool leaf_stage = F / L == LS_LEAF && L <= TMEM_TREE_LEAVES && !kMoePairs;
+  const bool leaf_stage = F / L == LS_LEAF && L <= TMEM_TREE_LEAVES;
   CUtensorMap tX, tW1, tH, tH2, tW2;
   iso_status st = make_tmap_bf16(&tX, xp, P, H, H, BK, BM);
   if (st == ISO_OK) st = make_tmap_bf16(&tW1, W1, static_cast<uint64_t>(E) * H, 2 * F, 2 * F, 64, BK);
@@ -781,7 +800,7 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
     st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, leaf_stage ? LS_LEAF : BK);
   if (st != ISO_OK) return st;
   const int up_nb = F / 64, dn_nb = H / BN;
-  const int unit_rows = kMoePairs ? 2 * BM : BM;  // rows of an expert per grouped work unit
+  const int unit_rows = BM;  // rows of an expert per grouped work unit
   if (launch_moe_permute(topk_ids, P, E, part_map, partition, counts, hist, perm, offs, up, up_nb, dn, dn_nb,
                          unit_rows, s) != cudaSuccess)
     return ISO_ERR_CUDA;
@@ -799,10 +818,6 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   p.out = hb;
   p.ldo = F;
   p.out_rows = P;
-  if (kMoePairs) {
-    p.pair = 1;
-    set_a_rows(p, 128);
-  }
   st = launch_gemm(EPI_SWIGLU, tX, tW1, p, sm_count(), s);
   if (st != ISO_OK) return st;
   GemmParams q = base_params(0, H, F, L);
@@ -814,10 +829,6 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
   q.ldo = H;
   q.out_rows = P;
   q.row_scatter = perm;
-  if (kMoePairs) {
-    q.pair = 1;
-    set_a_rows(q, 128);
-  }
   if (leaf_stage) {
     set_leaf_stage(q);
     return launch_gemm(EPI_BF16, tH, tW2, q, sm_count(), s, &tH2);

@@ -382,8 +382,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                               const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // B bytes per stage in this CTA
-  constexpr int BSTAGE = LS ? LS_B_BYTES : (PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES);
+  // k per stage and B bytes per stage in this CTA (a CTA of a pair holds half the B tile)
+  const int SBK = PAIR ? p.stage_k : BK;
+  const int BSTAGE = LS ? LS_B_BYTES : (PAIR ? SBK * 64 * 2 : B_STAGE_BYTES);
   constexpr int CL = PAIR ? 2 : 1;
   static_assert(!FUSED || (!PAIR && (EPI == EPI_BF16 || EPI == EPI_LOGPROB)), "fused prologue: single CTA, bf16/logprob");
   static_assert(EPW == 4 || (EPW == 8 && !PAIR && !FUSED && (EPI == EPI_BF16 || EPI == EPI_SWIGLU)),
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           const int n0 = (U.n_tile0 + t) * p.b_tile_cols;
           for (int g = 0; g < p.L / per && ok; ++g) {
             for (int j = 0; j < p.kb_per_leaf; ++j) {
-              const int kx = (g * per + me) * p.leaf_len + j * BK;
+              const int kx = (g * per + me) * p.leaf_len + j * SBK;
               const bool freed =
                   PAIR ? mbar_wait_cluster(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status)
                        : mbar_wait(&empty_bar[stage], (round & 1) ^ 1, p.timeout_ns, abort_flag, p.status);
@@ -498,8 +499,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                   const uint32_t fb = cluster_addr(&full_bar[stage], 0);
                   if (rank == 0)
                     mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(2 * (p.a_bytes + BSTAGE)));
-                  tma_load_2d_pair(sA, &tmA, fb, U.a_col0 + kx, U.a_row0);
-                  tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);
+                  if (SBK == PAIR_BK)  // A: {64 k, 128 rows, 2 k-chunks} of the 3-D view, one box
+                    tma_load_3d_pair(sA, &tmA, fb, 0, U.a_row0, (U.a_col0 + kx) / 64);
+                  else
+                    tma_load_2d_pair(sA, &tmA, fb, U.a_col0 + kx, U.a_row0);
+                  tma_load_2d_pair(sB, &tmB, fb, n0 + rank * p.b_box2_off, U.b_row0 + kx);  // 64 columns
                 } else if (FUSED) {
                   // raw x on raw_bar (the transform warps normalise it in place, then add their
                   // four arrivals to full_bar); B on full_bar
@@ -613,17 +617,28 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 const uint32_t b_lo = (smem_base + b_region + stage * BSTAGE) >> 4;
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(a_lo);
                 const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_lo);
-                const int rem = p.leaf_len - j * BK;
+                const int rem = p.leaf_len - j * SBK;
                 if (leader) {
                   if (PAIR) {
-                    if (rem >= BK) {
+                    // K = 16 step i reads A chunk i / 4 (a 128-k stage holds two 64-k chunks, the
+                    // second a_rows x 128 bytes on: 1024 units for 128 rows), +32 bytes per step
+                    // inside it, and B +2 KB per step down its rows.
+                    const uint64_t a_chunk = static_cast<uint64_t>((p.a_rows * 128) >> 4);
+                    if (rem >= SBK) {
                       umma_bf16_pair(d, adesc, bdesc, kIdescPair, j != 0 ? 1u : 0u);
                       umma_bf16_pair(d, adesc + 2, bdesc + 128, kIdescPair, 1u);
                       umma_bf16_pair(d, adesc + 4, bdesc + 256, kIdescPair, 1u);
                       umma_bf16_pair(d, adesc + 6, bdesc + 384, kIdescPair, 1u);
+                      if (SBK == PAIR_BK) {
+                        umma_bf16_pair(d, adesc + a_chunk, bdesc + 512, kIdescPair, 1u);
+                        umma_bf16_pair(d, adesc + a_chunk + 2, bdesc + 640, kIdescPair, 1u);
+                        umma_bf16_pair(d, adesc + a_chunk + 4, bdesc + 768, kIdescPair, 1u);
+                        umma_bf16_pair(d, adesc + a_chunk + 6, bdesc + 896, kIdescPair, 1u);
+                      }
                     } else {
                       for (int i = 0; i < rem / UMMA_K; ++i)
-                        umma_bf16_pair(d, adesc + 2 * i, bdesc + 128 * i, kIdescPair, (j != 0 || i != 0) ? 1u : 0u);
+                        umma_bf16_pair(d, adesc + (i >> 2) * a_chunk + 2 * (i & 3), bdesc + 128 * i, kIdescPair,
+                                       (j != 0 || i != 0) ? 1u : 0u);
                     }
                     if (j == p.kb_per_leaf - 1) umma_commit_pair(&leaf_full[b], 3);
                     umma_commit_pair(&empty_bar[stage], 3);
@@ -1220,6 +1235,14 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
     return launch_one<EPI_BF16, false, false, 8, true>(tmA, tmB, p, max_units, s, a2);
   }
   const bool pair = p.pair != 0;
+  // CTA pairs serve row-block units; deep stages read A through the 3-D chunk view (one leaf
+  // starting at k = 0, a whole number of 64-k chunks)
+  if (p.stage_k != (pair ? p.stage_k : BK) || (p.stage_k != BK && p.stage_k != PAIR_BK) ||
+      p.kb_per_leaf != (p.leaf_len + p.stage_k - 1) / p.stage_k)
+    return ISO_ERR_INVALID_ARG;
+  if (pair && ((p.unit_mode != UNIT_GEMM && p.unit_mode != UNIT_LOGPROB) ||
+               (p.stage_k == PAIR_BK && (p.L != 1 || p.leaf_len % 64 != 0))))
+    return ISO_ERR_INVALID_ARG;
   if (p.a_transform) {
     if (pair) return ISO_ERR_INVALID_ARG;
     if (epi == EPI_BF16) return launch_one<EPI_BF16, false, true>(tmA, tmB, p, max_units, s, a2);
@@ -1239,8 +1262,8 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
     case EPI_SWIGLU:
       if (!pair && !p.spill && p.leaf_len <= EPI8_MAX_LEAF_SWIGLU)
         return launch_one<EPI_SWIGLU, false, false, 8>(tmA, tmB, p, max_units, s, a2);
-      return pair ? launch_one<EPI_SWIGLU, true>(tmA, tmB, p, max_units, s, a2)
-                  : launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s, a2);
+      if (pair) return ISO_ERR_INVALID_ARG;
+      return launch_one<EPI_SWIGLU, false>(tmA, tmB, p, max_units, s, a2);
     case EPI_LOGPROB:
       return pair ? launch_one<EPI_LOGPROB, true>(tmA, tmB, p, max_units, s, a2)
                   : launch_one<EPI_LOGPROB, false>(tmA, tmB, p, max_units, s, a2);

@@ -44,6 +44,12 @@ constexpr int UMMA_K = 16;
 constexpr int MAX_STAGES = 12;
 constexpr int A_TILE_BYTES_MAX = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BK * BN * 2;
+// Deep stages of a CTA pair with one producer (a one-leaf contract): 128 k per stage, the CTA's
+// A tile [128 x 128] one TMA box of a 3-D view ({64 k, rows, k / 64}) and its 64-column half of
+// B one {64 x 128} box, two TMA instructions per 48 KB.  A producer thread pays ~200 cycles per
+// TMA (measured on GB300): alone, with 24 KB stages it delivers ~60 bytes/cycle/SM of the 94 a
+// pair consumes at the tensor rate.  Two producers (two or more leaves) keep 64-k stages.
+constexpr int PAIR_BK = 128;
 constexpr int GEMM_BARRIER_BYTES = 512;
 constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
@@ -103,7 +109,8 @@ struct GemmParams {
   int L;           // leaves in this launch
   int leaf_len;    // K / L, a multiple of 16
   int num_kb;      // ceil(K / BK)
-  int kb_per_leaf; // ceil(leaf_len / BK)
+  int kb_per_leaf; // ceil(leaf_len / stage_k)
+  int stage_k;     // k per pipeline stage: BK, or PAIR_BK on a one-producer CTA pair
   int stages;      // pipeline stages (even, <= MAX_STAGES)
   int spill;       // 1 when L > TMEM_TREE_LEAVES: the root of leaves [0, L/2) is parked in shared memory
   int cluster;     // EPI_CLUSTER: leaf groups per tile = CTAs per cluster (the group root uses the park region)

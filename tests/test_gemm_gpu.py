@@ -209,6 +209,42 @@ def test_cta_pair_units_ragged_exact(c8, M, K):
         assert same_bits(B.gemm(c8, Ad[r:r + 1].contiguous(), Bd), C[r:r + 1]), r
 
 
+@pytest.mark.parametrize("M,K", [(129, 576), (300, 1024), (257, 2048), (200, 528), (520, 640)])
+def test_cta_pair_one_leaf_deep_stages_exact(M, K):
+    """A one-leaf contract on CTA pairs stages 128 k at a time (A through the 3-D chunk view):
+    K = 576 and 640 end on a half stage whose second chunk lies past K (zero-filled, unused);
+    K = 528 is not a whole number of 64-k chunks and keeps 64-k stages.  Exact integers: the bits
+    equal the oracle's one-leaf chain, and rows equal their single-row results."""
+    c1 = B.Contract(1)
+    N = 264
+    A = inputs.small_int_bf16((M, K), -3, 3, seed=M + K)
+    Bm = inputs.small_int_bf16((K, N), -3, 3, seed=N + K)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    C = B.gemm(c1, Ad, Bd)
+    ref = oracle.gemm(bits(A), bits(Bm), 1)
+    assert np.array_equal(bits(C), ref), first_diff(C, torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16))
+    for r in (0, 128, 255 if M > 255 else M - 1, M - 1):
+        assert same_bits(B.gemm(c1, Ad[r:r + 1].contiguous(), Bd), C[r:r + 1]), r
+
+
+def test_cta_pair_one_leaf_normal_inputs_partial_and_repeats():
+    """Normal inputs on the one-leaf deep-stage pairs: sampled rows within tolerance of the
+    oracle, repeated launches give the same bits, and the R = 1 leaf partial (fp32 root through
+    the same pairs) + combine reproduces the single pass."""
+    c1 = B.Contract(1)
+    M, K, N = 1024, 4096, 1024
+    A, Bm = inputs.gemm_inputs(M, K, N, seed=43)
+    Ad, Bd = A.to(DEV), Bm.to(DEV)
+    full = B.gemm(c1, Ad, Bd)
+    rows = torch.tensor([0, 255, 256, 700, 1023])
+    check_row_tolerance(full[rows.to(DEV)], oracle.gemm_root(bits(A[rows]), bits(Bm), 1))
+    for _ in range(2):
+        assert same_bits(B.gemm(c1, Ad, Bd), full)
+    S = B.gemm_leaf_partial(c1, 0, 1, Ad, Bd)
+    assert same_bits(B.tree_combine(c1, S[None]), full)
+    assert B.last_device_status(c1) == B.ISO_OK
+
+
 def test_cta_pair_repeatable_many_tiles(c8):
     """Many 256-row tiles per CTA pair (K = 4096, 512-k leaves): repeated launches give the
     same bits, and rows equal their one-CTA results (guards the pair's TMEM-buffer release

@@ -148,6 +148,22 @@ def test_logprob_cta_pairs_match_single_rows(c8, T):
     assert np.max(np.abs(full[rows].cpu().double().numpy() - ref["out"])) <= 1e-3
 
 
+def test_logprob_one_leaf_deep_stage_pairs():
+    """A one-leaf contract's logprob GEMM runs on CTA pairs with 128-k stages (H = 1088 ends on a
+    half stage): within 1e-3 of the oracle, and rows equal their single-row results bitwise."""
+    c1 = B.Contract(1)
+    T, H, V = 300, 1088, 2440 * 2
+    h, W, ids = inputs.logprob_inputs(T, H, V, seed=77)
+    hd, Wd, idd = h.to(DEV), W.to(DEV), ids.to(DEV)
+    out = B.selected_logprob(c1, hd, Wd, idd)
+    ref = oracle.selected_logprob(bits(h), bits(W), ids.numpy(), 1)
+    assert np.max(np.abs(out.cpu().double().numpy() - ref["out"])) <= 1e-3
+    for t in (0, 128, 256, 299):
+        one = B.selected_logprob(c1, hd[t:t + 1].contiguous(), Wd, idd[t:t + 1].contiguous())
+        assert f32_same(one, out[t:t + 1]), t
+    assert B.last_device_status(c1) == B.ISO_OK
+
+
 def test_logprob_tile_units_and_chunk_units_agree_bitwise(c8):
     """With the full workspace every 128-column tile is its own work unit and a fold kernel
     folds each chunk's tiles left to right; with the minimum workspace one CTA folds a whole
