@@ -38,6 +38,8 @@ __device__ __forceinline__ float tree_sum(float (&v)[NMAX], int n) {
 // C[i, j] = bf16_rn(tree_r S[r][i, j]); each thread owns 4 consecutive columns.
 __global__ void tree_combine_kernel(const float* __restrict__ S, int64_t lds, int64_t rank_stride, int R,
                                     __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N) {
+  grid_dependency_wait();  // launched as a dependent grid: the partials come from the grid before
+  grid_launch_dependents();
   const int64_t nvec_row = N / 4;
   const int64_t total = static_cast<int64_t>(M) * nvec_row;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -170,6 +172,8 @@ __device__ __forceinline__ void lse_merge_into(float& m1, float& s1, float m2, f
 // to right -- the fold the GEMM epilogue performs when one CTA owns a whole chunk.
 __global__ void lse_fold_tiles_kernel(const float2* __restrict__ tile_stats, float2* __restrict__ chunk_stats, int T,
                                       int C, int ntiles, int chunk_tiles) {
+  grid_dependency_wait();  // launched as a dependent grid: the tile statistics come from the GEMM
+  grid_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(C) * T) return;
   const int c = static_cast<int>(idx / T);
@@ -199,6 +203,8 @@ __global__ void __launch_bounds__(32 * kFinalizeWarps)
                         const int32_t* __restrict__ ids, float* __restrict__ out, int T, int C, int V,
                         ShardBounds shards, unsigned int* status) {
   __shared__ float2 node[kFinalizeWarps][kFinalizeMaxChunks];
+  grid_dependency_wait();  // launched as a dependent grid: the statistics come from the grid before
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const int t = blockIdx.x * kFinalizeWarps + w;
@@ -522,9 +528,9 @@ static int grid_for(int64_t work_items, int threads, int max_blocks) {
 cudaError_t launch_tree_combine(const float* S, int64_t lds, int64_t rank_stride, int R, uint16_t* C, int64_t ldc,
                                 int M, int N, cudaStream_t s) {
   const int64_t work = static_cast<int64_t>(M) * (N / 4);
-  tree_combine_kernel<<<grid_for(work, 256, sm_count() * 8), 256, 0, s>>>(
-      S, lds, rank_stride, R, reinterpret_cast<__nv_bfloat16*>(C), ldc, M, N);
-  return cudaGetLastError();
+  const cudaError_t e = launch_dependent(tree_combine_kernel, dim3(grid_for(work, 256, sm_count() * 8)), dim3(256), 0,
+                                         s, 1u, S, lds, rank_stride, R, reinterpret_cast<__nv_bfloat16*>(C), ldc, M, N);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* y, int T, int H,
@@ -595,18 +601,19 @@ cudaError_t launch_lse_finalize(const float2* tile_stats, float2* chunk_stats, c
 
 cudaError_t launch_lse_combine(const float2* chunk_stats, const float* zsel, const int32_t* ids, float* out, int T,
                                int C, int V, const ShardBounds& shards, cudaStream_t s) {
-  lse_finalize_kernel<<<(T + kFinalizeWarps - 1) / kFinalizeWarps, 32 * kFinalizeWarps, 0, s>>>(
-      chunk_stats, zsel, ids, out, T, C, V, shards, device_status_ptr());
-  return cudaGetLastError();
+  const cudaError_t e =
+      launch_dependent(lse_finalize_kernel, dim3((T + kFinalizeWarps - 1) / kFinalizeWarps), dim3(32 * kFinalizeWarps),
+                       0, s, 1u, chunk_stats, zsel, ids, out, T, C, V, shards, device_status_ptr());
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_lse_fold_tiles(const float2* tile_stats, float2* chunk_stats, int T, int C, int ntiles,
                                   int chunk_tiles, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(C) * T;
   if (n == 0) return cudaSuccess;
-  lse_fold_tiles_kernel<<<static_cast<unsigned int>((n + 255) / 256), 256, 0, s>>>(tile_stats, chunk_stats, T, C,
-                                                                                     ntiles, chunk_tiles);
-  return cudaGetLastError();
+  const cudaError_t e = launch_dependent(lse_fold_tiles_kernel, dim3(static_cast<unsigned int>((n + 255) / 256)),
+                                         dim3(256), 0, s, 1u, tile_stats, chunk_stats, T, C, ntiles, chunk_tiles);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {

@@ -455,6 +455,10 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
   if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above overlaps the previous grid of the stream (programmatic dependent launch);
+  // inputs, routing tables and outputs are touched only after it has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int nunits = unit_count(p);
 
   // Leaves are issued in pairs (2g, 2g+1) by two MMA threads (warps 1 and 2), one leaf each;
@@ -1156,40 +1160,16 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
   if constexpr (EPI == EPI_CLUSTER) {
     // one CTA per unit, in clusters of p.cluster (the host checked that they fit at once)
     if (max_units <= 0 || max_units % p.cluster != 0) return ISO_ERR_INVALID_ARG;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(max_units));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, p) != cudaSuccess) return ISO_ERR_CUDA;
+    if (launch_dependent(kern, dim3(static_cast<unsigned>(max_units)), dim3(kThreads), GEMM_SMEM_BYTES, s,
+                         static_cast<unsigned>(p.cluster), tmA, tmB, tmA2, p) != cudaSuccess)
+      return ISO_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
   }
   const int units = max_units < slots ? max_units : slots;
   if (units <= 0) return ISO_OK;
-  if (!PAIR) {
-    kern<<<units, kThreads, GEMM_SMEM_BYTES, s>>>(tmA, tmB, tmA2, p);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
-    cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, p) != cudaSuccess) return ISO_ERR_CUDA;
-  }
+  if (launch_dependent(kern, dim3(static_cast<unsigned>(PAIR ? 2 * units : units)), dim3(kThreads), GEMM_SMEM_BYTES,
+                       s, PAIR ? 2u : 1u, tmA, tmB, tmA2, p) != cudaSuccess)
+    return ISO_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
 

@@ -185,4 +185,33 @@ iso_status launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, 
 // (0 when R is not 2, 4 or 8 or the query fails).
 int cluster_gemm_capacity(int R);
 
+// Launch with programmatic stream serialization allowed (and clusters of cluster_x CTAs when
+// cluster_x > 1): the grid may be scheduled while the stream's previous grid finishes, so it
+// overlaps that grid's tail and its own launch.  Only for kernels that execute
+// grid_dependency_wait before their first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             unsigned int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[2];
+  unsigned int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace iso

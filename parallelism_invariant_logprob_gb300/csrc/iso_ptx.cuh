@@ -157,6 +157,13 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(x), "r"(y)
       : "memory");
 }
+// Programmatic dependent launch.  A grid launched with programmatic stream serialization may
+// be scheduled while the previous grid of its stream is still running: it must execute
+// grid_dependency_wait (which returns once the grids it depends on have completed and their
+// memory operations are visible) before its first global-memory access.  grid_launch_dependents
+// lets the next such grid of the stream be scheduled early; it never weakens that wait.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // 3-D tiled load into this CTA's shared memory, completion counted on a pair barrier (as above).
 __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* m, uint32_t cluster_bar, int x,
                                                  int y, int z) {
