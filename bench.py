@@ -94,9 +94,14 @@ def load_peaks():
     return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, src="fallback")
 
 
+# the sources whose change invalidates committed traffic figures: the GEMM engine and the host
+# code that picks its schedule (pairs, stage depth, raster groups)
+ENGINE_SOURCES = ("gemm_tcgen05.cu", "iso_ptx.cuh", "iso_internal.h", "capi.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm_tcgen05.cu", "iso_ptx.cuh", "iso_internal.h", "capi.cu"):
+    for f in ENGINE_SOURCES:
         h.update(open(os.path.join(ROOT, "parallelism_invariant_logprob_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

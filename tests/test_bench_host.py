@@ -19,7 +19,7 @@ def test_traffic_reported_only_for_the_captured_engine_source(tmp_path, monkeypa
     src.mkdir(parents=True)
     real = os.path.join(os.path.dirname(os.path.abspath(bench.__file__)), "parallelism_invariant_logprob_gb300",
                         "csrc")
-    for f in ("gemm_tcgen05.cu", "iso_ptx.cuh", "iso_internal.h"):
+    for f in bench.ENGINE_SOURCES:
         (src / f).write_bytes(open(os.path.join(real, f), "rb").read())
     assert bench.committed_traffic(key) == 123.0
     # a changed engine source: the old figure is not reported
