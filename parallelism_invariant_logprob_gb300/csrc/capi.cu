@@ -714,7 +714,7 @@ iso_status iso_moe_permute(const iso_contract* c, const int32_t* topk_ids, int T
   int32_t* dn = up + (E + 1);
   int32_t* hist = dn + (E + 1);
   return launch_moe_permute(topk_ids, static_cast<int64_t>(T) * k, E, expert_partition, partition, counts_ws, hist,
-                            perm, offsets, up, 1, dn, 1, BM, S(stream)) == cudaSuccess
+                            perm, offsets, up, 1, dn, 1, BM, BM, S(stream)) == cudaSuccess
              ? ISO_OK
              : ISO_ERR_CUDA;
 }
@@ -731,9 +731,11 @@ iso_status iso_moe_combine(const iso_contract* c, const iso_bf16* y_slots, const
   return launch_moe_combine(y_slots, topk_w, T, k, H, out, S(stream)) == cudaSuccess ? ISO_OK : ISO_ERR_CUDA;
 }
 
-// The expert layer's grouped GEMMs run on single CTAs (units of 128 rows of one expert): its
-// leaves (H / L, F / L) are short, where CTA pairs lose (1.12 -> 1.84 ms per layer measured
-// at T = 8192, H = 2048, F = 768, E = 128, k = 8).
+// The expert layer's grouped GEMMs run on single CTAs (units of 128 rows of one expert).  CTA
+// pairs (256-row units) measured slower on GB300 at T = 8192, H = 2048, F = 768, E = 128, k = 8,
+// bits identical: 0.861 ms per layer on single CTAs, 1.008 with pairs for gate/up, 0.997 for
+// down, 1.137 for both (an expert's ~512 rows leave a ragged 256-row unit more often than a
+// ragged 128-row one, and the short leaves gain little from the smaller per-SM operand stream).
 
 // Workspace layout of the expert layer (each region 256-byte aligned):
 //   y_slots [P x H] bf16 (the full layer only; iso_moe_experts_partial writes the caller's) |
@@ -800,9 +802,9 @@ iso_status moe_experts_pass(const iso_contract* c, const iso_bf16* x, const int3
     st = make_tmap_bf16(&tW2, W2, static_cast<uint64_t>(E) * F, H, H, 64, leaf_stage ? LS_LEAF : BK);
   if (st != ISO_OK) return st;
   const int up_nb = F / 64, dn_nb = H / BN;
-  const int unit_rows = BM;  // rows of an expert per grouped work unit
-  if (launch_moe_permute(topk_ids, P, E, part_map, partition, counts, hist, perm, offs, up, up_nb, dn, dn_nb,
-                         unit_rows, s) != cudaSuccess)
+  // rows of an expert per grouped work unit: one row block for both GEMMs
+  if (launch_moe_permute(topk_ids, P, E, part_map, partition, counts, hist, perm, offs, up, up_nb, dn, dn_nb, BM,
+                         BM, s) != cudaSuccess)
     return ISO_ERR_CUDA;
   if (launch_moe_gather(x, perm, offs + E, P, k, H, xp, s) != cudaSuccess) return ISO_ERR_CUDA;
   // gate/up with SwiGLU fused: tile j pairs gate columns [64j, 64j+64) with up columns

@@ -343,7 +343,8 @@ __global__ void moe_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int 
 __global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
     moe_scan_kernel(int32_t* __restrict__ hist, int C, int E, const int32_t* __restrict__ part_map, int part,
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ up_prefix,
-                    int up_nblocks, int32_t* __restrict__ down_prefix, int down_nblocks, int unit_rows) {
+                    int up_nblocks, int32_t* __restrict__ down_prefix, int down_nblocks, int up_unit_rows,
+                    int down_unit_rows) {
   __shared__ int part_sum[4][MOE_MAX_EXPERTS];
   __shared__ int scan[3][MOE_MAX_EXPERTS + 1];
   const int g = threadIdx.x / MOE_MAX_EXPERTS;
@@ -372,10 +373,9 @@ __global__ void __launch_bounds__(4 * MOE_MAX_EXPERTS)
       if (part_map != nullptr && part_map[e] != part) cnt = 0;
       counts[e] = cnt;
     }
-    const int mb = (cnt + unit_rows - 1) / unit_rows;
     scan[0][e] = cnt;
-    scan[1][e] = mb * up_nblocks;
-    scan[2][e] = mb * down_nblocks;
+    scan[1][e] = (cnt + up_unit_rows - 1) / up_unit_rows * up_nblocks;
+    scan[2][e] = (cnt + down_unit_rows - 1) / down_unit_rows * down_nblocks;
   }
   __syncthreads();
   // exclusive scans over the experts: thread (g < 3, e == 0) runs array g sequentially
@@ -630,8 +630,8 @@ int64_t moe_perm_chunks(int64_t P) { return (P + MOE_PERM_CHUNK - 1) / MOE_PERM_
 
 cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
                                int32_t* counts, int32_t* hist, int32_t* perm, int32_t* offsets, int32_t* up_prefix,
-                               int up_nblocks, int32_t* down_prefix, int down_nblocks, int unit_rows,
-                               cudaStream_t s) {
+                               int up_nblocks, int32_t* down_prefix, int down_nblocks, int up_unit_rows,
+                               int down_unit_rows, cudaStream_t s) {
   const int64_t C = moe_perm_chunks(P);
   if (C > 0) {
     moe_hist_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, device_status_ptr());
@@ -639,7 +639,8 @@ cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32
     if (e != cudaSuccess) return e;
   }
   moe_scan_kernel<<<1, 4 * MOE_MAX_EXPERTS, 0, s>>>(hist, static_cast<int>(C), E, part_map, part, counts, offsets,
-                                                    up_prefix, up_nblocks, down_prefix, down_nblocks, unit_rows);
+                                                    up_prefix, up_nblocks, down_prefix, down_nblocks, up_unit_rows,
+                                                    down_unit_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || C == 0) return e;
   moe_scatter_kernel<<<static_cast<unsigned int>(C), MOE_PERM_THREADS, 0, s>>>(ids, P, E, hist, counts, offsets,

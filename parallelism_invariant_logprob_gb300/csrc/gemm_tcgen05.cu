@@ -32,14 +32,14 @@
 //             warp 2 the odd leaves of every leaf pair (one thread cannot issue
 //             128x128x16 MMAs as fast as the tensor core retires them); warp 1
 //             also owns the TMEM allocation.
-//   warps 4-7 epilogue: one thread per accumulator row (TMEM lane); they run
-//             the tree in TMEM (tcgen05.ld / add / tcgen05.st) while the MMAs
-//             fill the next leaves, and write the output.  With short leaves
-//             (bf16 and SwiGLU outputs) warps 8-11 join them: each warp then
-//             takes one 64-column half of its lane quarter's rows.
-// The tree's working set lives in four 128-column TMEM buffers.  Buffer
-// assignment is a FIFO free list replayed identically by the MMA thread and
-// the epilogue, so both sides agree without exchanging buffer ids.
+//   warps 4-7 epilogue: one thread per accumulator row (TMEM lane); they read
+//             each finished leaf once (tcgen05.ld) and run the tree in registers
+//             while the MMAs fill the next leaves, and write the output.  With
+//             short leaves (bf16 and SwiGLU outputs) warps 8-11 join them: each
+//             warp then takes one 64-column half of its lane quarter's rows.
+// Leaves accumulate in four 128-column TMEM buffers, the CTA's s-th leaf in
+// buffer s % 4, so the MMA threads and the epilogue agree on buffers and
+// barrier phases without exchanging anything.
 #include <cuda_bf16.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -153,41 +153,6 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, Unit& U,
   }
 }
 
-// FIFO of free TMEM buffers plus the tree stack, replayed identically by the
-// MMA thread and every epilogue thread.  Both live in registers as packed
-// 2-bit buffer ids (no local-memory arrays on the MMA issue path).
-struct TreeBufs {
-  uint32_t fifo;   // free buffers, front in bits [0,2)
-  uint32_t nfree;
-  uint32_t stack;  // tree stack, bottom in bits [0,2)
-  uint32_t depth;
-  __device__ __forceinline__ void init() {
-    fifo = 0u | (1u << 2) | (2u << 4) | (3u << 6);
-    nfree = NUM_TMEM_BUFS;
-    stack = 0u;
-    depth = 0u;
-  }
-  __device__ __forceinline__ int pop_free() {
-    const int b = static_cast<int>(fifo & 3u);
-    fifo >>= 2;
-    --nfree;
-    return b;
-  }
-  __device__ __forceinline__ void push_free(int b) {
-    fifo |= static_cast<uint32_t>(b) << (2u * nfree);
-    ++nfree;
-  }
-  __device__ __forceinline__ void push(int b) {
-    stack = (stack & ~(3u << (2u * depth))) | (static_cast<uint32_t>(b) << (2u * depth));
-    ++depth;
-  }
-  __device__ __forceinline__ int pop() {
-    --depth;
-    return static_cast<int>((stack >> (2u * depth)) & 3u);
-  }
-  __device__ __forceinline__ int top() const { return static_cast<int>((stack >> (2u * (depth - 1u))) & 3u); }
-};
-
 // Bounded wait until the shared leaf ticket reaches `want`.
 __device__ __forceinline__ bool wait_ticket(volatile uint32_t* ticket, uint32_t want, uint64_t timeout_ns,
                                             volatile int* abort_flag, unsigned int* status) {
@@ -206,8 +171,6 @@ __device__ __forceinline__ bool wait_ticket(volatile uint32_t* ticket, uint32_t 
   }
 }
 
-// Per-buffer phase bits (one bit per TMEM buffer) kept in a register.
-__device__ __forceinline__ uint32_t bit_of(uint32_t bits, int b) { return (bits >> b) & 1u; }
 
 // Register reallocation between warpgroups (every warp of a warpgroup executes the same one).
 template <int R>
@@ -229,17 +192,107 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-__device__ __forceinline__ int merges_after_leaf(int l) { return __ffs(l + 1) - 1; }  // trailing zeros of l+1
-
-// Merges in TMEM after leaf l of an L-leaf tree.  With a parked subtree (L > TMEM_TREE_LEAVES)
-// the last leaf's merges stop one level short: the top merge, with the root of leaves [0, L/2)
-// kept in shared memory, is made by the epilogue as it reads the root.
-__device__ __forceinline__ int tmem_merges_after_leaf(int l, int L, int spill) {
-  return merges_after_leaf(l) - ((spill && l == L - 1) ? 1 : 0);
-}
-
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// ---- The leaf tree in the epilogue ("spine")
+// Leaf s of this CTA (counting every tile's leaves in order) accumulates in TMEM buffer s % 4
+// (the four 128-column buffers); its use index s / 4 gives the parity of the leaf_full phase
+// the epilogue waits for and of the buf_free phase the next use of the buffer waits for.  The
+// epilogue takes leaves in groups of up to 8 (leaf l is l % 8 of its group, G = min(L, 8)
+// leaves per group) and keeps the group's partial root S in registers:
+//   G = 1: S = leaf.
+//   leaf 1 of the group: S = l0 + l1;  leaf 3: S = S + (l2 + l3)      (their buffers freed)
+//   leaf 5: l4 + l5 into l5's buffer, l4's buffer freed
+//   leaf 7: S = S + ((l4 + l5) + (l6 + l7))                          (the last three freed)
+// which is the contract's balanced tree over the group (left operand = lower leaves, fp32 adds
+// rounded to nearest).  With 16 leaves the first group's root waits in shared memory and the
+// tile's root is parked + S.  One register partial per thread suffices, TMEM is written once
+// per group of 8, and the buffer that the next tile's first leaf takes (l4's) is free two
+// leaves before the tile ends; merging in TMEM wrote every merge back and freed that buffer
+// only after three read-add-write merges.  Pieces of 16 columns keep the temporaries small
+// next to the 128-register partial of a 4-warp epilogue.
+
+// Column j (0 <= j < NC) of the columns an epilogue thread owns in every tile: all 128 with 4
+// epilogue warps; with 8, a 64-column half (bf16) or 32 gate and the matching 32 up columns
+// (SwiGLU, gate in [0, 64), up in [64, 128)).
+template <int EPI, int EPW>
+__device__ __forceinline__ int spine_col(int chalf, int j) {
+  if constexpr (EPW == 4) return j;
+  if constexpr (EPI == EPI_SWIGLU) return j < 32 ? chalf * 32 + j : 64 + chalf * 32 + (j - 32);
+  return chalf * 64 + j;
+}
+
+// S = the leaf in buffer t (G = 1).
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_load(uint32_t (&S)[NC], uint32_t t, int chalf) {
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) tmem_ld32p(t + static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 32)), S + c * 32);
+  tmem_ld_wait_only();
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) tmem_ld_tie(S + c * 32);
+}
+
+// S = (first ? x + y : S + (x + y)) for the leaves in buffers t0 (left) and t1.
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_pair(uint32_t (&S)[NC], uint32_t t0, uint32_t t1, int chalf, bool first) {
+#pragma unroll
+  for (int c = 0; c < NC / 16; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
+    uint32_t x[16], y[16];
+    tmem_ld16p(t0 + col, x);
+    tmem_ld16p(t1 + col, y);
+    tmem_ld_wait_only();
+    tmem_ld_tie16(x);
+    tmem_ld_tie16(y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float v = __fadd_rn(u2f(x[i]), u2f(y[i]));
+      S[c * 16 + i] = f2u(first ? v : __fadd_rn(u2f(S[c * 16 + i]), v));
+    }
+  }
+}
+
+// t1 = t0 + t1 in TMEM (leaves 4 and 5 of a group: left = t0), over this thread's columns.
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_merge(uint32_t t0, uint32_t t1, int chalf) {
+#pragma unroll
+  for (int c = 0; c < NC / 16; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
+    uint32_t x[16], y[16];
+    tmem_ld16p(t0 + col, x);
+    tmem_ld16p(t1 + col, y);
+    tmem_ld_wait_only();
+    tmem_ld_tie16(x);
+    tmem_ld_tie16(y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
+    tmem_st16p(t1 + col, y);
+  }
+  tmem_st_wait();
+}
+
+// S = S + (m + (x + y)) with m = leaves 4 + 5 in buffer tm and leaves 6, 7 in tx, ty.
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_last(uint32_t (&S)[NC], uint32_t tm, uint32_t tx, uint32_t ty, int chalf) {
+#pragma unroll
+  for (int c = 0; c < NC / 16; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
+    uint32_t m[16], x[16], y[16];
+    tmem_ld16p(tm + col, m);
+    tmem_ld16p(tx + col, x);
+    tmem_ld16p(ty + col, y);
+    tmem_ld_wait_only();
+    tmem_ld_tie16(m);
+    tmem_ld_tie16(x);
+    tmem_ld_tie16(y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float r = __fadd_rn(u2f(m[i]), __fadd_rn(u2f(x[i]), u2f(y[i])));
+      S[c * 16 + i] = f2u(__fadd_rn(u2f(S[c * 16 + i]), r));
+    }
+  }
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat16 a = __float2bfloat16_rn(lo);
@@ -560,10 +613,6 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       // ----------------------------------------------------------------- MMA
       // The whole warp runs the loop (warp-uniform values); one elected lane issues.
       const bool leader = elect_one();
-      TreeBufs tb;
-      tb.init();
-      uint32_t used = 0u;      // bit b: buffer b has been used before (both issuers' leaves)
-      uint32_t free_par = 0u;  // bit b: parity of the next buf_free phase of buffer b
       int stage = me;          // this thread's blocks sit at global stage indices me, me+per, ...
       uint32_t round = 0;
       bool ok = true;
@@ -583,13 +632,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
         decode_unit(p, u, U, CL, rank);
         for (int t = 0; t < U.n_tiles && ok; ++t) {
           for (int leaf = 0; leaf < p.L && ok; ++leaf, ++seq) {
-            // replay of the tree bookkeeping (identical in both issuers and the epilogue)
-            const int b = tb.pop_free();
-            tb.push(b);
-            const bool reuse = bit_of(used, b) != 0u;
-            const uint32_t wpar = bit_of(free_par, b);
-            if (reuse) free_par ^= 1u << b;
-            used |= 1u << b;
+            // leaf seq accumulates in buffer seq % 4; from its second use on, wait until the
+            // epilogue has freed the previous use (buf_free phase seq / 4 - 1)
+            const int b = static_cast<int>(seq & 3u);
+            const bool reuse = seq >= static_cast<uint32_t>(NUM_TMEM_BUFS);
+            const uint32_t wpar = ((seq >> 2) + 1u) & 1u;
             if (per == 1 || (leaf & 1) == me) {
               if (per == 2 && !wait_ticket(next_leaf, seq, p.timeout_ns, abort_flag, p.status)) {
                 ok = false;
@@ -680,10 +727,6 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                 }
               }
             }
-            const int nm = tmem_merges_after_leaf(leaf, p.L, spill);
-            for (int m = 0; m < nm; ++m) tb.push_free(tb.pop());
-            if (spill && leaf == p.L / 2 - 1) tb.push_free(tb.pop());  // parked in shared memory
-            if (leaf == p.L - 1) tb.push_free(tb.pop());  // root, freed after output
           }
         }
       }
@@ -747,9 +790,10 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
     uint8_t* const wstage = epi_stage + (EPW == 8 ? (warp - 4) * (32 * 128) : quarter * (32 * 256));
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    TreeBufs tb;
-    tb.init();
-    uint32_t fill_par = 0u;  // bit b: parity of the next leaf_full phase of buffer b
+    constexpr int NC = BN / (EPW / 4);  // columns of every tile this thread holds (spine_col)
+    const int G = p.L < 8 ? p.L : 8;    // leaves per group of the spine
+    const uint32_t tbase = tmem_base + lane_off;
+    uint32_t seq = 0u;  // leaves of this CTA so far, all tiles: leaf seq is in TMEM buffer seq % 4
     bool ok = true;
     for (int u = unit0; u < nunits && ok; u += unit_step) {
       Unit U;
@@ -763,90 +807,64 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       bool have_sel = false;
       for (int t = 0; t < U.n_tiles && ok; ++t) {
         const int n0 = (U.n_tile0 + t) * p.b_tile_cols;  // first output column of this tile
-        for (int l = 0; l < p.L; ++l) {
-          const int b = tb.pop_free();
-          tb.push(b);
+        uint32_t S[NC];  // the spine: the current group's partial root, at the end the tile's root
+        for (int l = 0; l < p.L; ++l, ++seq) {
+          const int b = static_cast<int>(seq & 3u);
           // One thread polls the barrier; the other epilogue warps sleep in a hardware named
           // barrier so they take no issue slots from the TMA and MMA threads.
           if (threadIdx.x == 128) {
+            const uint32_t par = (seq >> 2) & 1u;
             if (PAIR)
-              (void)mbar_wait_cluster(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+              (void)mbar_wait_cluster(&leaf_full[b], par, p.timeout_ns, abort_flag, p.status);
             else
-              (void)mbar_wait(&leaf_full[b], bit_of(fill_par, b), p.timeout_ns, abort_flag, p.status);
+              (void)mbar_wait(&leaf_full[b], par, p.timeout_ns, abort_flag, p.status);
           }
           named_bar_sync(1, 32 * EPW);
           if (*abort_flag) {
             ok = false;
             break;
           }
-          fill_par ^= 1u << b;
           tc_fence_after();
-          const int nm = tmem_merges_after_leaf(l, p.L, spill);
-          for (int m = 0; m < nm; ++m) {
-            const int rb = tb.pop();
-            const int lb = tb.top();
-            // left (lower leaves) += right, in place in TMEM, 64 columns per step as two
-            // 32-column pieces at ca and cb.  With 8 epilogue warps each warp merges exactly the
-            // columns it reads at the root (bf16: its 64-column half; SwiGLU: its 32 gate
-            // columns and the matching 32 up columns), so no warp reads TMEM columns that the
-            // other warp of its lane quarter writes.
-#pragma unroll 1
-            for (int c = 0; c < (EPW == 8 ? 1 : BN / 64); ++c) {
-              const int ca = EPW == 8 ? (EPI == EPI_SWIGLU ? chalf * 32 : chalf * 64) : c * 64;
-              const int cb = (EPW == 8 && EPI == EPI_SWIGLU) ? 64 + chalf * 32 : ca + 32;
-              uint32_t x[64], y[64];
-              const uint32_t lo = tmem_base + lane_off + static_cast<uint32_t>(lb * BN);
-              const uint32_t ro = tmem_base + lane_off + static_cast<uint32_t>(rb * BN);
-              tmem_ld32p(lo + ca, x);
-              tmem_ld32p(lo + cb, x + 32);
-              tmem_ld32p(ro + ca, y);
-              tmem_ld32p(ro + cb, y + 32);
-              tmem_ld_wait_only();
-              tmem_ld_tie(x);
-              tmem_ld_tie(x + 32);
-              tmem_ld_tie(y);
-              tmem_ld_tie(y + 32);
-#pragma unroll
-              for (int i = 0; i < 64; ++i) x[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
-              tmem_st32p(lo + ca, x);
-              tmem_st32p(lo + cb, x + 32);
-            }
-            tmem_st_wait();
+          const int lg = l & 7;  // this leaf's place in its group
+          if (G == 1) {
+            spine_load<EPI, EPW>(S, tbase + static_cast<uint32_t>(b * BN), chalf);
             tc_fence_before();
-            release_tmem_buf<PAIR>(buf_free, rb, lane);
-            tb.push_free(rb);
+            release_tmem_buf<PAIR>(buf_free, b, lane);
+          } else if (lg == 1 || lg == 3) {
+            const int b0 = static_cast<int>((seq - 1u) & 3u);
+            spine_pair<EPI, EPW>(S, tbase + static_cast<uint32_t>(b0 * BN), tbase + static_cast<uint32_t>(b * BN),
+                                 chalf, lg == 1);
+            tc_fence_before();
+            release_tmem_buf<PAIR>(buf_free, b0, lane);
+            release_tmem_buf<PAIR>(buf_free, b, lane);
+          } else if (lg == 5) {
+            const int b4 = static_cast<int>((seq - 1u) & 3u);
+            spine_merge<EPI, EPW, NC>(tbase + static_cast<uint32_t>(b4 * BN), tbase + static_cast<uint32_t>(b * BN), chalf);
+            tc_fence_before();
+            release_tmem_buf<PAIR>(buf_free, b4, lane);
+          } else if (lg == 7) {
+            const int b5 = static_cast<int>((seq - 2u) & 3u), b6 = static_cast<int>((seq - 1u) & 3u);
+            spine_last<EPI, EPW>(S, tbase + static_cast<uint32_t>(b5 * BN), tbase + static_cast<uint32_t>(b6 * BN),
+                                 tbase + static_cast<uint32_t>(b * BN), chalf);
+            tc_fence_before();
+            release_tmem_buf<PAIR>(buf_free, b5, lane);
+            release_tmem_buf<PAIR>(buf_free, b6, lane);
+            release_tmem_buf<PAIR>(buf_free, b, lane);
           }
-          if (spill && l == p.L / 2 - 1) {
-            // park the root of leaves [0, L/2): this warp's columns of its rows (the columns it
-            // merges) into shared memory, then give the TMEM buffer back
-            const int sb = tb.pop();
-            const uint32_t so = tmem_base + lane_off + static_cast<uint32_t>(sb * BN);
-#pragma unroll 1
-            for (int c = 0; c < (EPW == 8 ? 1 : BN / 64); ++c) {
-              const int ca = EPW == 8 ? (EPI == EPI_SWIGLU ? chalf * 32 : chalf * 64) : c * 64;
-              const int cb = (EPW == 8 && EPI == EPI_SWIGLU) ? 64 + chalf * 32 : ca + 32;
-              uint32_t x[64];
-              tmem_ld32p(so + ca, x);
-              tmem_ld32p(so + cb, x + 32);
-              tmem_ld_wait_only();
-              tmem_ld_tie(x);
-              tmem_ld_tie(x + 32);
+          if (spill && l == 7) {
+            // 16 leaves: the root of leaves [0, 8) waits in shared memory ([column][row]) while
+            // the second group runs
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                parked[(ca + i) * BM + row_in_tile] = u2f(x[i]);
-                parked[(cb + i) * BM + row_in_tile] = u2f(x[32 + i]);
-              }
-            }
-            tc_fence_before();
-            release_tmem_buf<PAIR>(buf_free, sb, lane);
-            tb.push_free(sb);
+            for (int j = 0; j < NC; ++j) parked[spine_col<EPI, EPW>(chalf, j) * BM + row_in_tile] = u2f(S[j]);
           }
         }
         if (!ok) break;
-        // ---- the root of this tile
-        const int root = tb.pop();
-        bool released = false;
-        const uint32_t root_addr = tmem_base + lane_off + static_cast<uint32_t>(root * BN);
+        if (spill) {  // the tree's top add: leaves [0, 8) + leaves [8, 16)
+#pragma unroll
+          for (int j = 0; j < NC; ++j)
+            S[j] = f2u(__fadd_rn(parked[spine_col<EPI, EPW>(chalf, j) * BM + row_in_tile], u2f(S[j])));
+        }
+        // ---- the root of this tile, in S (its TMEM buffers are already free)
         if (EPI == EPI_SWIGLU) {
           // columns [0,64) hold gate, [64,128) up (the second B box came from the up half):
           // g, u = bf16_rn(root); h = bf16_rn(silu(g) * u) with silu(g) = g / (1 + e^-g) in fp32
@@ -854,27 +872,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           // of h; the same instructions for every row, tile and schedule).  This warp's h
           // columns: all 64, or with 8 epilogue warps 32 (gate [h0, h0+32), up [64+h0, ...)).
           constexpr int HC = 64 / (EPW / 4);
+          static_assert(2 * HC == NC, "S holds this thread's gate columns, then the matching up columns");
           const int h0 = EPW == 8 ? chalf * HC : 0;
-          uint32_t v[2 * HC];
-#pragma unroll
-          for (int c = 0; c < HC / 32; ++c) {
-            tmem_ld32p(root_addr + h0 + c * 32, v + c * 32);
-            tmem_ld32p(root_addr + 64 + h0 + c * 32, v + HC + c * 32);
-          }
-          tmem_ld_wait_only();
-#pragma unroll
-          for (int c = 0; c < 2 * HC / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
-#pragma unroll
-            for (int i = 0; i < HC; ++i) {
-              v[i] = f2u(__fadd_rn(parked[(h0 + i) * BM + row_in_tile], u2f(v[i])));
-              v[HC + i] = f2u(__fadd_rn(parked[(64 + h0 + i) * BM + row_in_tile], u2f(v[HC + i])));
-            }
-          }
-          tc_fence_before();
-          release_tmem_buf<PAIR>(buf_free, root, lane);
-          tb.push_free(root);
-          released = true;
+          const uint32_t* v = S;
           uint4 hw[HC / 8];
 #pragma unroll
           for (int q = 0; q < HC / 8; ++q) {
@@ -900,24 +900,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             for (int q = 0; q < HC / 8; ++q) *reinterpret_cast<uint4*>(dst + n0 + h0 + q * 8) = hw[q];
           }
         } else if (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_CLUSTER) {
-          // the root into registers, its TMEM buffer released, then convert and store; this
-          // warp's columns: all 128, or with 8 epilogue warps the 64 of its half
-          constexpr int RC = BN / (EPW / 4);
+          // convert and store this thread's columns of the root: all 128, or with 8 epilogue
+          // warps the 64 of its warp's half
+          constexpr int RC = NC;
           const int c0 = EPW == 8 ? chalf * RC : 0;
-          uint32_t v[RC];
-#pragma unroll
-          for (int c = 0; c < RC / 32; ++c) tmem_ld32p(root_addr + c0 + c * 32, v + c * 32);
-          tmem_ld_wait_only();
-#pragma unroll
-          for (int c = 0; c < RC / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
-#pragma unroll
-            for (int i = 0; i < RC; ++i) v[i] = f2u(__fadd_rn(parked[(c0 + i) * BM + row_in_tile], u2f(v[i])));
-          }
-          tc_fence_before();
-          release_tmem_buf<PAIR>(buf_free, root, lane);
-          tb.push_free(root);
-          released = true;
+          const uint32_t* v = S;
           if (EPI == EPI_CLUSTER) {
             // the group's subtree root stays in this CTA's shared memory ([column][row], the A
             // box's rows) for the cluster combine after the main loop
@@ -974,22 +961,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
         } else {
           // tile statistics: m = max over the tile's valid columns (order-free),
           // s = sum over ascending columns of expf(z - m); then the left fold.
-          // The whole root comes into registers first and its TMEM buffer is
-          // released before the arithmetic, so the MMAs of the next tile need not wait.
-          uint32_t v[BN];
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld32p(root_addr + c * 32, v + c * 32);
-          tmem_ld_wait_only();
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld_tie(v + c * 32);
-          if (spill) {  // the tree's top add: parked leaves [0, L/2) + leaves [L/2, L)
-#pragma unroll
-            for (int i = 0; i < BN; ++i) v[i] = f2u(__fadd_rn(parked[i * BM + row_in_tile], u2f(v[i])));
-          }
-          tc_fence_before();
-          release_tmem_buf<PAIR>(buf_free, root, lane);
-          tb.push_free(root);
-          released = true;
+          static_assert(EPI != EPI_LOGPROB || NC == BN, "the logprob epilogue holds whole rows of the tile");
+          const uint32_t* v = S;
           const int sel_off = sel - n0;
           float m = -INFINITY;
           float s = 0.f;
@@ -1022,11 +995,6 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           } else {
             lse_merge(run_m, run_s, m, s);
           }
-        }
-        if (!released) {
-          tc_fence_before();
-          release_tmem_buf<PAIR>(buf_free, root, lane);
-          tb.push_free(root);
         }
       }
       if (EPI == EPI_LOGPROB && ok && row_ok && ISO_DCHECK(U.chunk < p.num_chunks && row < p.M, p.status)) {

@@ -28,11 +28,12 @@ cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int32_t* 
 // Chunks of the permutation's counting sort for P pairs; hist holds chunks x E int32.
 int64_t moe_perm_chunks(int64_t P);
 // part_map (device, [E]) selects experts with part_map[e] == part; NULL = all.  The unit
-// prefixes count ceil(count / unit_rows) row blocks per expert times the n-blocks.
+// prefixes count ceil(count / unit rows) row blocks per expert times the n-blocks (unit rows:
+// 128 for single-CTA units, 256 for CTA pairs; each GEMM its own).
 cudaError_t launch_moe_permute(const int32_t* ids, int64_t P, int E, const int32_t* part_map, int part,
                                int32_t* counts, int32_t* hist, int32_t* perm, int32_t* offsets, int32_t* up_prefix,
-                               int up_nblocks, int32_t* down_prefix, int down_nblocks, int unit_rows,
-                               cudaStream_t s);
+                               int up_nblocks, int32_t* down_prefix, int down_nblocks, int up_unit_rows,
+                               int down_unit_rows, cudaStream_t s);
 cudaError_t launch_moe_gather(const uint16_t* x, const int32_t* perm, const int32_t* total, int64_t max_rows, int k,
                               int H, uint16_t* xp, cudaStream_t s);
 cudaError_t launch_moe_combine(const uint16_t* y, const float* w, int T, int k, int H, uint16_t* out,

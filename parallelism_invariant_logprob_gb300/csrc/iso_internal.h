@@ -73,11 +73,11 @@ constexpr int GEMM_REGS_EPILOGUE_EPI8 = 200;  // and of warps 4-11
 static_assert(128 * GEMM_REGS_CONTROL_EPI8 + 256 * GEMM_REGS_EPILOGUE_EPI8 <= 384 * 168,
               "register split within the launch's allocation");
 constexpr int GEMM_REGS_CONTROL_FUSED = 120;  // setmaxnreg of warps 0-3 and 8-11 (epilogue: 256)
-// The eager merge stack of a tree over 8 leaves (depth 3) plus the incoming leaf fills the 4
-// TMEM buffers.  16 leaves need one more: the root of leaves [0, 8) is parked in shared memory
-// (fp32, 64 KB, [column][row] so consecutive rows are consecutive words) once its merges are
-// done, its TMEM buffer goes back to the free list, and the epilogue adds it to the root of
-// leaves [8, 16) at the top of the tree -- the same fp32 add the tree makes there.
+// The epilogue keeps one partial root per thread in registers for a group of up to 8 leaves.
+// With 16 leaves the root of leaves [0, 8) is parked in shared memory (fp32, 64 KB,
+// [column][row] so consecutive rows are consecutive words) while the second group runs, and
+// the epilogue adds it to the root of leaves [8, 16) at the top of the tree -- the same fp32
+// add the tree makes there.
 constexpr int TMEM_TREE_LEAVES = 8;
 constexpr int MAX_LEAVES = 16;
 constexpr int SPILL_BYTES = BM * BN * 4;
