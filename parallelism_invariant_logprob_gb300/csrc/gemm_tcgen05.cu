@@ -210,8 +210,7 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 // tile's root is parked + S.  One register partial per thread suffices, TMEM is written once
 // per group of 8, and the buffer that the next tile's first leaf takes (l4's) is free two
 // leaves before the tile ends; merging in TMEM wrote every merge back and freed that buffer
-// only after three read-add-write merges.  Pieces of 16 columns keep the temporaries small
-// next to the 128-register partial of a 4-warp epilogue.
+// only after three read-add-write merges.
 
 // Column j (0 <= j < NC) of the columns an epilogue thread owns in every tile: all 128 with 4
 // epilogue warps; with 8, a 64-column half (bf16) or 32 gate and the matching 32 up columns
@@ -233,22 +232,48 @@ __device__ __forceinline__ void spine_load(uint32_t (&S)[NC], uint32_t t, int ch
   for (int c = 0; c < NC / 32; ++c) tmem_ld_tie(S + c * 32);
 }
 
+// TMEM columns per load round of the spine steps: each round issues its loads, waits once and
+// adds.  A round costs a TMEM load latency, so wider pieces are faster; the 64-column share of
+// an 8-warp epilogue takes 32-column pieces, the 128-register partial of a 4-warp epilogue
+// 16-column ones (wider would spill).
+template <int EPW>
+constexpr int spine_piece() {
+  return EPW == 8 ? 32 : 16;
+}
+
+// w TMEM columns starting at taddr into r[0..w).
+template <int W>
+__device__ __forceinline__ void tmem_ld_piece(uint32_t taddr, uint32_t* r) {
+  if constexpr (W == 32)
+    tmem_ld32p(taddr, r);
+  else
+    tmem_ld16p(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_tie_piece(uint32_t* r) {
+  if constexpr (W == 32)
+    tmem_ld_tie(r);
+  else
+    tmem_ld_tie16(r);
+}
+
 // S = (first ? x + y : S + (x + y)) for the leaves in buffers t0 (left) and t1.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_pair(uint32_t (&S)[NC], uint32_t t0, uint32_t t1, int chalf, bool first) {
+  constexpr int W = spine_piece<EPW>();
 #pragma unroll
-  for (int c = 0; c < NC / 16; ++c) {
-    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
-    uint32_t x[16], y[16];
-    tmem_ld16p(t0 + col, x);
-    tmem_ld16p(t1 + col, y);
+  for (int c = 0; c < NC / W; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
+    uint32_t x[W], y[W];
+    tmem_ld_piece<W>(t0 + col, x);
+    tmem_ld_piece<W>(t1 + col, y);
     tmem_ld_wait_only();
-    tmem_ld_tie16(x);
-    tmem_ld_tie16(y);
+    tmem_tie_piece<W>(x);
+    tmem_tie_piece<W>(y);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < W; ++i) {
       const float v = __fadd_rn(u2f(x[i]), u2f(y[i]));
-      S[c * 16 + i] = f2u(first ? v : __fadd_rn(u2f(S[c * 16 + i]), v));
+      S[c * W + i] = f2u(first ? v : __fadd_rn(u2f(S[c * W + i]), v));
     }
   }
 }
@@ -256,18 +281,22 @@ __device__ __forceinline__ void spine_pair(uint32_t (&S)[NC], uint32_t t0, uint3
 // t1 = t0 + t1 in TMEM (leaves 4 and 5 of a group: left = t0), over this thread's columns.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_merge(uint32_t t0, uint32_t t1, int chalf) {
+  constexpr int W = spine_piece<EPW>();
 #pragma unroll
-  for (int c = 0; c < NC / 16; ++c) {
-    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
-    uint32_t x[16], y[16];
-    tmem_ld16p(t0 + col, x);
-    tmem_ld16p(t1 + col, y);
+  for (int c = 0; c < NC / W; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
+    uint32_t x[W], y[W];
+    tmem_ld_piece<W>(t0 + col, x);
+    tmem_ld_piece<W>(t1 + col, y);
     tmem_ld_wait_only();
-    tmem_ld_tie16(x);
-    tmem_ld_tie16(y);
+    tmem_tie_piece<W>(x);
+    tmem_tie_piece<W>(y);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
-    tmem_st16p(t1 + col, y);
+    for (int i = 0; i < W; ++i) y[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
+    if constexpr (W == 32)
+      tmem_st32p(t1 + col, y);
+    else
+      tmem_st16p(t1 + col, y);
   }
   tmem_st_wait();
 }
@@ -275,21 +304,22 @@ __device__ __forceinline__ void spine_merge(uint32_t t0, uint32_t t1, int chalf)
 // S = S + (m + (x + y)) with m = leaves 4 + 5 in buffer tm and leaves 6, 7 in tx, ty.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_last(uint32_t (&S)[NC], uint32_t tm, uint32_t tx, uint32_t ty, int chalf) {
+  constexpr int W = spine_piece<EPW>();
 #pragma unroll
-  for (int c = 0; c < NC / 16; ++c) {
-    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * 16));
-    uint32_t m[16], x[16], y[16];
-    tmem_ld16p(tm + col, m);
-    tmem_ld16p(tx + col, x);
-    tmem_ld16p(ty + col, y);
+  for (int c = 0; c < NC / W; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
+    uint32_t m[W], x[W], y[W];
+    tmem_ld_piece<W>(tm + col, m);
+    tmem_ld_piece<W>(tx + col, x);
+    tmem_ld_piece<W>(ty + col, y);
     tmem_ld_wait_only();
-    tmem_ld_tie16(m);
-    tmem_ld_tie16(x);
-    tmem_ld_tie16(y);
+    tmem_tie_piece<W>(m);
+    tmem_tie_piece<W>(x);
+    tmem_tie_piece<W>(y);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < W; ++i) {
       const float r = __fadd_rn(u2f(m[i]), __fadd_rn(u2f(x[i]), u2f(y[i])));
-      S[c * 16 + i] = f2u(__fadd_rn(u2f(S[c * 16 + i]), r));
+      S[c * W + i] = f2u(__fadd_rn(u2f(S[c * W + i]), r));
     }
   }
 }
@@ -810,14 +840,21 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
         uint32_t S[NC];  // the spine: the current group's partial root, at the end the tile's root
         for (int l = 0; l < p.L; ++l, ++seq) {
           const int b = static_cast<int>(seq & 3u);
-          // One thread polls the barrier; the other epilogue warps sleep in a hardware named
-          // barrier so they take no issue slots from the TMA and MMA threads.
+          const int lg = l & 7;  // this leaf's place in its group
+          // The tree steps run at the odd leaves of a group (every leaf when G = 1); a step
+          // waits for its own leaf and, with G > 1, the one before (the two leaves run on
+          // different MMA threads and may complete in either order).  One thread polls the
+          // barriers; the other epilogue warps sleep in a hardware named barrier so they take
+          // no issue slots from the TMA and MMA threads.
+          if (G > 1 && (lg & 1) == 0) continue;
           if (threadIdx.x == 128) {
-            const uint32_t par = (seq >> 2) & 1u;
-            if (PAIR)
-              (void)mbar_wait_cluster(&leaf_full[b], par, p.timeout_ns, abort_flag, p.status);
-            else
-              (void)mbar_wait(&leaf_full[b], par, p.timeout_ns, abort_flag, p.status);
+            for (uint32_t w = (G > 1 ? seq - 1u : seq); w <= seq; ++w) {
+              const uint32_t par = (w >> 2) & 1u;
+              if (PAIR)
+                (void)mbar_wait_cluster(&leaf_full[w & 3u], par, p.timeout_ns, abort_flag, p.status);
+              else
+                (void)mbar_wait(&leaf_full[w & 3u], par, p.timeout_ns, abort_flag, p.status);
+            }
           }
           named_bar_sync(1, 32 * EPW);
           if (*abort_flag) {
@@ -825,7 +862,6 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const int lg = l & 7;  // this leaf's place in its group
           if (G == 1) {
             spine_load<EPI, EPW>(S, tbase + static_cast<uint32_t>(b * BN), chalf);
             tc_fence_before();
