@@ -833,6 +833,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       float run_m = -INFINITY, run_s = 0.f;  // logprob: running chunk statistics
       int sel = -1;
       if (EPI == EPI_LOGPROB && row_ok) sel = p.ids[row] - p.sel_base;  // this launch's column of the id
+      // destination row of the bf16 root (scattered rows: the expert layer's down projection);
+      // an 8-warp epilogue loads it here so that its latency hides behind the unit's leaves
+      // (a 4-warp one, short of registers, at the root)
+      int orow_u = row;
+      if (EPI == EPI_BF16 && EPW == 8 && row_ok && p.row_scatter != nullptr) orow_u = p.row_scatter[row];
       float zsel = 0.f;
       bool have_sel = false;
       for (int t = 0; t < U.n_tiles && ok; ++t) {
@@ -961,13 +966,13 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
               w[q].z = pack_bf16x2(u2f(v[q * 8 + 4]), u2f(v[q * 8 + 5]));
               w[q].w = pack_bf16x2(u2f(v[q * 8 + 6]), u2f(v[q * 8 + 7]));
             }
-            int orow = row_ok ? ((p.row_scatter != nullptr) ? p.row_scatter[row] : row) : -1;
+            int orow = row_ok ? ((EPW == 4 && p.row_scatter != nullptr) ? p.row_scatter[row] : orow_u) : -1;
             if (orow >= 0 && !ISO_DCHECK(orow < p.out_rows, p.status)) orow = -1;
             store_rows_staged<RC / 8>(wstage, lane, w, orow, reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0 + c0,
                                       p.N);
           } else if (row_ok) {
             if (EPI == EPI_BF16) {
-              const int orow = (p.row_scatter != nullptr) ? p.row_scatter[row] : row;
+              const int orow = (EPW == 4 && p.row_scatter != nullptr) ? p.row_scatter[row] : orow_u;
               const bool o_ok = ISO_DCHECK(orow >= 0 && orow < p.out_rows, p.status);
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(orow) * p.ldo;
 #pragma unroll
