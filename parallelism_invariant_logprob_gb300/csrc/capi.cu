@@ -404,8 +404,10 @@ iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, co
   iso_status st = check_gemm_args(A, lda, B, ldb, C, ldc, 8, M, N, K, L);
   if (st != ISO_OK || M == 0) return st;
   if (!ensure_device_state()) return ISO_ERR_CUDA;
-  // one row block whose leaf groups fit as clusters: iso_gemm's own one-launch schedule
-  if (cluster_groups(M, N, L) > 1) return run_gemm(EPI_BF16, A, lda, B, ldb, C, ldc, M, N, K, L, S(stream));
+  // With a workspace the groups run as plain CTAs and the combine as a second, dependent launch
+  // (its launch overlaps the GEMM's tail), which measured faster than iso_gemm's one-launch
+  // cluster schedule on GB300: M = 1, 4096 x 4096, R = 4: 19.1 -> 17.0 us after an L2 flush,
+  // 12.4 -> 11.5 us back to back; 12288 x 4096: 23.1 -> 21.2 us back to back.
   // Leaf groups: with one row block and fewer column tiles than SMs, R groups of L/R leaves run
   // as separate units (R = the largest power of two <= L with R x tiles <= SMs); each writes
   // its group's fp32 subtree root to ws and the tree combine applies the top log2 R levels --
