@@ -385,16 +385,17 @@ __device__ __forceinline__ int stage_slot(int c, int r) {
   return CH >= 8 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
 }
 
-// One epilogue warp writes the bf16 tile rows of its 32 TMEM lanes.  Lane r holds
-// row r as CH chunks of 8 bf16 (16 bytes) and its destination row `orow` (-1: row not
-// stored).  The rows go through the warp's staging area (32 rows x CH*16 bytes, chunk c of
-// row r at slot stage_slot(c, r)), then out whole rows at a time: each store instruction
-// covers 512/(CH*16) complete rows, so global writes are whole rows (whole 128-byte lines
-// for CH >= 8) instead of 32 scattered 16-byte pieces.  Columns at or past col_end are not
-// stored.
+// One epilogue warp writes its 32 TMEM lanes' pieces of the output rows.  Lane r holds
+// CH 16-byte chunks of row r (8 bf16 or 4 fp32 each) and its destination row `orow` (-1:
+// row not stored).  The rows go through the warp's staging area (32 rows x CH*16 bytes,
+// chunk c of row r at slot stage_slot(c, r)), then out whole rows at a time: each store
+// instruction covers 512/(CH*16) complete rows, so global writes are whole rows (whole
+// 128-byte lines for CH >= 8) instead of 32 scattered 16-byte pieces.  Row r's chunk c goes
+// to byte b0 + 16 c of the row (rows ld bytes apart in `out`); chunks at or past byte b_end
+// are not stored.
 template <int CH>
 __device__ __forceinline__ void store_rows_staged(uint8_t* wst, int lane, const uint4 (&w)[CH], int orow,
-                                                  __nv_bfloat16* out, int64_t ldo, int n0, int col_end) {
+                                                  uint8_t* out, int64_t ld, int64_t b0, int64_t b_end) {
   constexpr int ROW_BYTES = CH * 16;
   constexpr int ROWS_PER_STEP = 32 / CH;
 #pragma unroll
@@ -407,9 +408,8 @@ __device__ __forceinline__ void store_rows_staged(uint8_t* wst, int lane, const 
     const int r = t * ROWS_PER_STEP + lane / CH;
     const int dst_row = __shfl_sync(0xffffffffu, orow, r);
     const uint4 x = *reinterpret_cast<const uint4*>(wst + r * ROW_BYTES + (stage_slot<CH>(c, r) << 4));
-    const int col = n0 + c * 8;
-    if (dst_row >= 0 && col < col_end)
-      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(dst_row) * ldo + col) = x;
+    const int64_t b = b0 + 16 * c;
+    if (dst_row >= 0 && b < b_end) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(dst_row) * ld + b) = x;
   }
   __syncwarp();
 }
@@ -933,8 +933,8 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
           }
           const bool h_ok = row_ok && ISO_DCHECK(row < p.out_rows, p.status);
           if (p.epi_staged) {
-            store_rows_staged<HC / 8>(wstage, lane, hw, h_ok ? row : -1, reinterpret_cast<__nv_bfloat16*>(p.out),
-                                      p.ldo, n0 + h0, n0 + h0 + HC);
+            store_rows_staged<HC / 8>(wstage, lane, hw, h_ok ? row : -1, reinterpret_cast<uint8_t*>(p.out), p.ldo * 2,
+                                      2 * static_cast<int64_t>(n0 + h0), 2 * static_cast<int64_t>(n0 + h0 + HC));
           } else if (h_ok) {
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo;
 #pragma unroll
@@ -968,8 +968,25 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             }
             int orow = row_ok ? ((EPW == 4 && p.row_scatter != nullptr) ? p.row_scatter[row] : orow_u) : -1;
             if (orow >= 0 && !ISO_DCHECK(orow < p.out_rows, p.status)) orow = -1;
-            store_rows_staged<RC / 8>(wstage, lane, w, orow, reinterpret_cast<__nv_bfloat16*>(p.out), p.ldo, n0 + c0,
-                                      p.N);
+            store_rows_staged<RC / 8>(wstage, lane, w, orow, reinterpret_cast<uint8_t*>(p.out), p.ldo * 2,
+                                      2 * static_cast<int64_t>(n0 + c0), 2 * static_cast<int64_t>(p.N));
+          } else if (EPI == EPI_F32 && PAIR && p.epi_staged) {
+            // fp32 rows of 512 bytes go out in two staged halves of 64 columns (256-byte rows).
+            // CTA pairs only: they serve many row blocks, while single CTAs serve one-row-block
+            // leaf groups, where most staged rows would be empty (and the staging spilled
+            // registers of the single-CTA instance: iso_gemm_ws at M = 64 19.1 -> 21.1 us)
+            const int orow = (row_ok && ISO_DCHECK(row < p.out_rows, p.status)) ? row : -1;
+            uint8_t* out = reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.out) + U.chunk * p.out_group_stride);
+#pragma unroll
+            for (int hh = 0; hh < RC / 64; ++hh) {
+              uint4 w[16];
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                w[q] = make_uint4(v[hh * 64 + q * 4 + 0], v[hh * 64 + q * 4 + 1], v[hh * 64 + q * 4 + 2],
+                                  v[hh * 64 + q * 4 + 3]);
+              store_rows_staged<16>(wstage, lane, w, orow, out, p.ldo * 4, 4 * static_cast<int64_t>(n0 + c0 + hh * 64),
+                                    4 * static_cast<int64_t>(p.N));
+            }
           } else if (row_ok) {
             if (EPI == EPI_BF16) {
               const int orow = (EPW == 4 && p.row_scatter != nullptr) ? p.row_scatter[row] : orow_u;
