@@ -55,7 +55,7 @@ constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int GEMM_THREADS_FUSED = 384;      // + warps 8..11: the fused RMSNorm prologue
-// Short leaves: the tree merges and the root of a tile outlast its MMAs, so warps 8..11 join
+// Short leaves: the tree steps and the root of a tile outlast its MMAs, so warps 8..11 join
 // the epilogue (two warps per TMEM lane quarter, each with its own columns of the tile).
 // Measured on GB300: a gain for SwiGLU roots with leaves up to 256 k and bf16 roots up to
 // 128 k; with bf16 roots and 256-k leaves the MMAs already hide the epilogue and the extra
