@@ -151,8 +151,10 @@ iso_status make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, ui
 
 namespace {
 
-// A box rows and the stage count that fits the shared-memory budget (even, for the two producers).
-void set_a_rows(GemmParams& p, int a_rows) {
+// A box rows and the stage count that fits the shared-memory budget.  By default an even count
+// (the output staging area usually fits beside it); epilogues that store no rows (the logprob
+// statistics) take every stage that fits (the two leaf-parity streams split an odd count).
+void set_a_rows(GemmParams& p, int a_rows, bool row_output = true) {
   p.a_rows = a_rows;
   p.a_bytes = a_rows * p.stage_k * 2;
   const int b_bytes = p.pair ? p.stage_k * 64 * 2 : B_STAGE_BYTES;  // a CTA of a pair holds half the B tile
@@ -161,8 +163,8 @@ void set_a_rows(GemmParams& p, int a_rows) {
   const int room = GEMM_SMEM_BYTES - 1024 - GEMM_BARRIER_BYTES - reserve;
   int st = room / (p.a_bytes + b_bytes);
   if (st > MAX_STAGES) st = MAX_STAGES;
-  p.stages = st & ~1;
-  p.epi_staged = (room - p.stages * (p.a_bytes + b_bytes) >= EPI_STAGE_BYTES) ? 1 : 0;
+  p.stages = row_output ? (st & ~1) : st;
+  p.epi_staged = (row_output && room - p.stages * (p.a_bytes + b_bytes) >= EPI_STAGE_BYTES) ? 1 : 0;
 }
 
 // Whole-leaf stages (leaves of 96 k, bf16 roots on one CTA): a stage holds a leaf, A in a
@@ -209,14 +211,14 @@ bool use_pair(int rows, int K, int L) { return rows > BM && K / L >= kPairMinLea
 // 1449 TFLOP/s).  With two producers the 64-k stages stay: 128-k stages release their shared
 // memory in larger steps, leaving fewer bytes in flight (8 leaves: 1389 -> 1361 TFLOP/s, the
 // T = 32768 logprob 28.4 -> 29.6 ms; 16 leaves, 2 stages: 1304 -> 885).
-void set_pair(GemmParams& p, int rows) {
+void set_pair(GemmParams& p, int rows, bool row_output = true) {
   p.pair = 1;
   p.m_blocks = div_up(rows, 2 * BM);
   if (p.L == 1 && p.leaf_len % 64 == 0) {
     p.stage_k = PAIR_BK;
     p.kb_per_leaf = div_up(p.leaf_len, PAIR_BK);
   }
-  set_a_rows(p, 128);
+  set_a_rows(p, 128, row_output);
 }
 
 // A tensor maps of CTA pairs.  With 128-k stages a 3-D view {64 k, rows, K / 64 k-chunks} of the
@@ -533,9 +535,9 @@ static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, co
     p.a_rinv = rinv;
     p.a_gamma = gamma;
   } else if (p.m_blocks == 1) {
-    set_a_rows(p, a_rows_for(T));
+    set_a_rows(p, a_rows_for(T), false);  // the statistics epilogue stores no rows
   } else if (use_pair(T, H, L)) {
-    set_pair(p, T);
+    set_pair(p, T, false);
   }
   CUtensorMap tA, tB;
   iso_status st = make_tmap_a(&tA, p, h, T, H, H);

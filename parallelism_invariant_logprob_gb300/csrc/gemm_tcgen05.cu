@@ -549,6 +549,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
   // leaf (L = 1) issuer 0 does everything.  K-blocks are leaf-relative: leaf l's block j covers
   // k in [l*leaf_len + 64 j, min(+64, (l+1)*leaf_len)).
   const int per = (p.L >= 2) ? 2 : 1;
+  // Each leaf-parity stream (producer warp 0 / MMA warp 1: even leaves; warp 3 / warp 2: odd
+  // leaves) cycles through its own ring of stages: stream q holds ring_n(q) stages starting at
+  // ring_base(q), so an odd stage count splits (n + 1) / 2 + n / 2.
+  auto ring_n = [&](int q) { return per == 1 ? nstages : (q == 0 ? (nstages + 1) / 2 : nstages / 2); };
+  auto ring_base = [&](int q) { return q == 0 ? 0 : (nstages + 1) / 2; };
 
   if (warp < 4 || (FUSED && warp >= 8)) {
   if constexpr (FUSED) regs_dec<GEMM_REGS_CONTROL_FUSED>();
@@ -559,7 +564,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       // ------------------------------------------------------------ producer
       // The whole warp runs the loop (warp-uniform values); one elected lane issues.
       const bool leader = elect_one();
-      int stage = me;
+      const int rn = ring_n(me), rb = ring_base(me);
+      int slot = 0;
+      int stage = rb;
       uint32_t round = 0;
       uint32_t issued = 0;  // stages issued by this thread
       bool ok = true;
@@ -610,28 +617,28 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
               }
               __syncwarp();
               ++issued;
-              stage += per;
-              if (stage >= nstages) {
-                stage -= nstages;
+              if (++slot == rn) {
+                slot = 0;
                 ++round;
               }
+              stage = rb + slot;
             }
           }
         }
       }
       if (!ok && rank == 0) {
         // drain: wait (bounded) for every load this thread issued to land (rank 0's barriers
-        // also count the peer's loads of the stages it armed).  This thread's k-th
-        // stage index is me + per*k; stage s was last filled in the round of its latest use.
+        // also count the peer's loads of the stages it armed).  This thread's k-th stage is
+        // slot k % rn of its ring, filled in round k / rn.
         const uint32_t total = issued;
-        for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(nstages / per); ++back) {
-          const uint32_t gidx = static_cast<uint32_t>(me) + static_cast<uint32_t>(per) * (total - back);
+        for (uint32_t back = 1; back <= total && back <= static_cast<uint32_t>(rn); ++back) {
+          const uint32_t k = total - back;
+          const int st = rb + static_cast<int>(k % static_cast<uint32_t>(rn));
           // FUSED: the raw x loads land on raw_bar (full_bar may also wait for transform
           // arrivals that an abort cut short; its B bytes land in the same window)
-          const uint32_t a = smem_u32(FUSED ? &raw_bar[gidx % static_cast<uint32_t>(nstages)]
-                                            : &full_bar[gidx % static_cast<uint32_t>(nstages)]);
+          const uint32_t a = smem_u32(FUSED ? &raw_bar[st] : &full_bar[st]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, (gidx / static_cast<uint32_t>(nstages)) & 1u)) {
+          while (!mbar_try_wait(a, (k / static_cast<uint32_t>(rn)) & 1u)) {
             if (globaltimer_ns() - t0 > p.timeout_ns) break;
           }
         }
@@ -643,7 +650,9 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       // ----------------------------------------------------------------- MMA
       // The whole warp runs the loop (warp-uniform values); one elected lane issues.
       const bool leader = elect_one();
-      int stage = me;          // this thread's blocks sit at global stage indices me, me+per, ...
+      const int rn = ring_n(me), rb = ring_base(me);  // this thread's stages: its stream's ring
+      int slot = 0;
+      int stage = rb;
       uint32_t round = 0;
       bool ok = true;
       // Descriptor start addresses are the low 18 bits of the shared::cta address (14 bits of
@@ -750,11 +759,11 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                   }
                 }
                 __syncwarp();
-                stage += per;
-                if (stage >= nstages) {
-                  stage -= nstages;
+                if (++slot == rn) {
+                  slot = 0;
                   ++round;
                 }
+                stage = rb + slot;
               }
             }
           }
@@ -780,21 +789,22 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
     }
   } else if constexpr (FUSED) {
     // ---------------------------------------------------- fused prologue (warps 8-11)
-    // Walk the stages in the producers' global order (for each K-block, the leaf of each
-    // parity); for each: wait for its raw x, normalise rows [32 w, 32 w + 32) in place,
-    // publish with one arrival on the stage's full barrier.
+    // Walk the stages in the producers' order (for each K-block, the leaf of each parity, each
+    // in its stream's ring); for each: wait for its raw x, normalise rows [32 w, 32 w + 32) in
+    // place, publish with one arrival on the stage's full barrier.
     const int w = warp - 8;
-    uint32_t cidx = 0;  // global stage counter
+    uint32_t kcnt = 0;  // K-blocks of each stream so far: stream me's kcnt-th stage
     bool ok = true;
     for (int u = unit0; u < nunits && ok; u += unit_step) {
       Unit U;
       decode_unit(p, u, U, CL, rank);
       for (int t = 0; t < U.n_tiles && ok; ++t) {
         for (int g = 0; g < p.L / per && ok; ++g) {
-          for (int j = 0; j < p.kb_per_leaf && ok; ++j) {
-            for (int me = 0; me < per; ++me, ++cidx) {
-              const int stage = static_cast<int>(cidx % static_cast<uint32_t>(nstages));
-              const uint32_t round = cidx / static_cast<uint32_t>(nstages);
+          for (int j = 0; j < p.kb_per_leaf && ok; ++j, ++kcnt) {
+            for (int me = 0; me < per; ++me) {
+              const uint32_t rn = static_cast<uint32_t>(ring_n(me));
+              const int stage = ring_base(me) + static_cast<int>(kcnt % rn);
+              const uint32_t round = kcnt / rn;
               ok = __all_sync(0xffffffffu, mbar_wait(&raw_bar[stage], round & 1, p.timeout_ns, abort_flag, p.status));
               if (!ok) break;
               const int kx = (g * per + me) * p.leaf_len + j * BK;

@@ -111,7 +111,7 @@ struct GemmParams {
   int num_kb;      // ceil(K / BK)
   int kb_per_leaf; // ceil(leaf_len / stage_k)
   int stage_k;     // k per pipeline stage: BK, or PAIR_BK on a one-producer CTA pair
-  int stages;      // pipeline stages (even, <= MAX_STAGES)
+  int stages;      // pipeline stages (<= MAX_STAGES), split between the two leaf-parity streams
   int spill;       // 1 when L > TMEM_TREE_LEAVES: the root of leaves [0, L/2) is parked in shared memory
   int cluster;     // EPI_CLUSTER: leaf groups per tile = CTAs per cluster (the group root uses the park region)
   int epi_staged;  // 1: bf16 roots go out through the shared-memory staging area
