@@ -31,9 +31,9 @@
 //              (TMEM lane); each also rescales its O rows and writes the output
 //   warp 8     TMA producer: Q of both tiles once, then K and V chunks into a 4-stage ring
 //   warps 9-12 MMA issuers, one lane each: Q K^T of tile A, P V of tile A, Q K^T of tile B,
-//              P V of tile B.  One thread cannot issue tcgen05 MMAs as fast as the tensor core
-//              retires them (one per ~190 cycles at any N on this part), so every chain that
-//              can run on its own has its own thread.  Warp 9 owns TMEM; warps 13-15 idle.
+//              P V of tile B.  The four chains depend on each other only through the softmax,
+//              so each has its own thread: a tile's Q K^T for the next chunk goes out while
+//              the other tile's P V is still being issued.  Warp 9 owns TMEM; warps 13-15 idle.
 // TMEM (512 columns): per tile t at 256 t: S (80 fp32 columns), P (40 columns of bf16 pairs, its
 // own region) and O (128 columns at 256 t + 128).  P apart from S lets Q K^T of chunk c + 1 run
 // as soon as the softmax has read S of chunk c, overlapping the softmax and P V of chunk c.
