@@ -233,12 +233,12 @@ __device__ __forceinline__ void spine_load(uint32_t (&S)[NC], uint32_t t, int ch
 }
 
 // TMEM columns per load round of the spine steps: each round issues its loads, waits once and
-// adds.  A round costs a TMEM load latency, so wider pieces are faster; the 64-column share of
-// an 8-warp epilogue takes 32-column pieces, the 128-register partial of a 4-warp epilogue
-// 16-column ones (wider would spill).
+// adds.  A round costs a TMEM load latency, so wider pieces are faster: 32 columns, the widest
+// load that keeps the temporaries of the three-buffer step beside a 4-warp epilogue's
+// 128-register partial without spilling.
 template <int EPW>
 constexpr int spine_piece() {
-  return EPW == 8 ? 32 : 16;
+  return 32;
 }
 
 // w TMEM columns starting at taddr into r[0..w).
