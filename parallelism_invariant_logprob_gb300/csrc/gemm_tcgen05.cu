@@ -232,44 +232,25 @@ __device__ __forceinline__ void spine_load(uint32_t (&S)[NC], uint32_t t, int ch
   for (int c = 0; c < NC / 32; ++c) tmem_ld_tie(S + c * 32);
 }
 
-// TMEM columns per load round of the spine steps: each round issues its loads, waits once and
-// adds.  A round costs a TMEM load latency, so wider pieces are faster: 32 columns, the widest
-// load that keeps the temporaries of the three-buffer step beside a 4-warp epilogue's
-// 128-register partial without spilling.
-template <int EPW>
-constexpr int spine_piece() {
-  return 32;
-}
-
-// w TMEM columns starting at taddr into r[0..w).
-template <int W>
-__device__ __forceinline__ void tmem_ld_piece(uint32_t taddr, uint32_t* r) {
-  if constexpr (W == 32)
-    tmem_ld32p(taddr, r);
-  else
-    tmem_ld16p(taddr, r);
-}
-template <int W>
-__device__ __forceinline__ void tmem_tie_piece(uint32_t* r) {
-  if constexpr (W == 32)
-    tmem_ld_tie(r);
-  else
-    tmem_ld_tie16(r);
-}
+// The spine steps read TMEM in 32-column pieces: each piece is one load round (loads, one
+// wait, adds).  A round costs a TMEM load latency, so wide pieces are faster; 32 columns keep
+// the temporaries of the three-buffer step beside a 4-warp epilogue's 128-register partial
+// without spilling (16-column pieces were slower and spilled).
+constexpr int SPINE_PIECE = 32;
 
 // S = (first ? x + y : S + (x + y)) for the leaves in buffers t0 (left) and t1.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_pair(uint32_t (&S)[NC], uint32_t t0, uint32_t t1, int chalf, bool first) {
-  constexpr int W = spine_piece<EPW>();
+  constexpr int W = SPINE_PIECE;
 #pragma unroll
   for (int c = 0; c < NC / W; ++c) {
     const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
     uint32_t x[W], y[W];
-    tmem_ld_piece<W>(t0 + col, x);
-    tmem_ld_piece<W>(t1 + col, y);
+    tmem_ld32p(t0 + col, x);
+    tmem_ld32p(t1 + col, y);
     tmem_ld_wait_only();
-    tmem_tie_piece<W>(x);
-    tmem_tie_piece<W>(y);
+    tmem_ld_tie(x);
+    tmem_ld_tie(y);
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       const float v = __fadd_rn(u2f(x[i]), u2f(y[i]));
@@ -281,22 +262,19 @@ __device__ __forceinline__ void spine_pair(uint32_t (&S)[NC], uint32_t t0, uint3
 // t1 = t0 + t1 in TMEM (leaves 4 and 5 of a group: left = t0), over this thread's columns.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_merge(uint32_t t0, uint32_t t1, int chalf) {
-  constexpr int W = spine_piece<EPW>();
+  constexpr int W = SPINE_PIECE;
 #pragma unroll
   for (int c = 0; c < NC / W; ++c) {
     const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
     uint32_t x[W], y[W];
-    tmem_ld_piece<W>(t0 + col, x);
-    tmem_ld_piece<W>(t1 + col, y);
+    tmem_ld32p(t0 + col, x);
+    tmem_ld32p(t1 + col, y);
     tmem_ld_wait_only();
-    tmem_tie_piece<W>(x);
-    tmem_tie_piece<W>(y);
+    tmem_ld_tie(x);
+    tmem_ld_tie(y);
 #pragma unroll
     for (int i = 0; i < W; ++i) y[i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
-    if constexpr (W == 32)
-      tmem_st32p(t1 + col, y);
-    else
-      tmem_st16p(t1 + col, y);
+    tmem_st32p(t1 + col, y);
   }
   tmem_st_wait();
 }
@@ -304,18 +282,18 @@ __device__ __forceinline__ void spine_merge(uint32_t t0, uint32_t t1, int chalf)
 // S = S + (m + (x + y)) with m = leaves 4 + 5 in buffer tm and leaves 6, 7 in tx, ty.
 template <int EPI, int EPW, int NC>
 __device__ __forceinline__ void spine_last(uint32_t (&S)[NC], uint32_t tm, uint32_t tx, uint32_t ty, int chalf) {
-  constexpr int W = spine_piece<EPW>();
+  constexpr int W = SPINE_PIECE;
 #pragma unroll
   for (int c = 0; c < NC / W; ++c) {
     const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
     uint32_t m[W], x[W], y[W];
-    tmem_ld_piece<W>(tm + col, m);
-    tmem_ld_piece<W>(tx + col, x);
-    tmem_ld_piece<W>(ty + col, y);
+    tmem_ld32p(tm + col, m);
+    tmem_ld32p(tx + col, x);
+    tmem_ld32p(ty + col, y);
     tmem_ld_wait_only();
-    tmem_tie_piece<W>(m);
-    tmem_tie_piece<W>(x);
-    tmem_tie_piece<W>(y);
+    tmem_ld_tie(m);
+    tmem_ld_tie(x);
+    tmem_ld_tie(y);
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       const float r = __fadd_rn(u2f(m[i]), __fadd_rn(u2f(x[i]), u2f(y[i])));
