@@ -122,6 +122,29 @@ def test_rmsnorm_batch_invariance_bitwise(c8):
     assert torch.equal(B.rmsnorm(c8, xd[perm].contiguous(), gd, 1e-6).view(torch.int16), full[perm].view(torch.int16))
 
 
+@pytest.mark.parametrize("H", [1024, 2048, 4096])
+def test_rmsnorm_large_batch_bulk_staged(c8, H):
+    """Batches of >= 32768 rows run the bulk-staged kernel (rows copied into shared memory by
+    bulk copies): sampled rows within one bf16 ulp of the oracle, rows computed alone (the
+    register kernel) equal their rows of the batch bitwise, and so does a shuffled batch."""
+    T = 40000
+    x, gamma = inputs.rmsnorm_inputs(T, H, seed=H + 7)
+    xd, gd = x.to(DEV), gamma.to(DEV)
+    full = B.rmsnorm(c8, xd, gd, 1e-6)
+    rows = torch.tensor([0, 1, 7, 8, 1215, 1216, 20011, T - 2, T - 1])
+    sub = full[rows.to(DEV)]
+    ref, ye = oracle.rmsnorm(bits(x[rows]), bits(gamma), 1e-6, exact=True)
+    got = oracle.bf16_to_f64(bits(sub))
+    ulp = np.spacing(np.abs(oracle.bf16_to_f64(ref)).astype(np.float32)) * 65536
+    assert np.all(np.abs(got - ye) <= ulp * 1.01)
+    for t in rows.tolist():
+        assert torch.equal(B.rmsnorm(c8, xd[t:t + 1].contiguous(), gd, 1e-6).view(torch.int16),
+                           full[t:t + 1].view(torch.int16)), t
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(1)).to(DEV)
+    assert torch.equal(B.rmsnorm(c8, xd[perm].contiguous(), gd, 1e-6).view(torch.int16), full[perm].view(torch.int16))
+    assert B.last_device_status(c8) == B.ISO_OK
+
+
 def test_rmsnorm_constant_row(c8):
     H = 4096
     x = torch.full((2, H), 2.0, dtype=torch.bfloat16, device=DEV)
