@@ -204,6 +204,7 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 //   G = 1: S = leaf.
 //   leaf 1 of the group: S = l0 + l1;  leaf 3: S = S + (l2 + l3)      (their buffers freed)
 //   leaf 5: l4 + l5 into l5's buffer, l4's buffer freed
+//           (8 epilogue warps: Q = l4 + l5 in registers, both buffers freed)
 //   leaf 7: S = S + ((l4 + l5) + (l6 + l7))                          (the last three freed)
 // which is the contract's balanced tree over the group (left operand = lower leaves, fp32 adds
 // rounded to nearest).  With 16 leaves the first group's root waits in shared memory and the
@@ -297,6 +298,47 @@ __device__ __forceinline__ void spine_last(uint32_t (&S)[NC], uint32_t tm, uint3
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       const float r = __fadd_rn(u2f(m[i]), __fadd_rn(u2f(x[i]), u2f(y[i])));
+      S[c * W + i] = f2u(__fadd_rn(u2f(S[c * W + i]), r));
+    }
+  }
+}
+
+// 8 epilogue warps (64 columns per thread) keep leaves 4 + 5 in registers beside S instead of
+// writing them back to TMEM: Q = l4 + l5 at leaf 5 (both buffers freed at once), then
+// S = S + (Q + (l6 + l7)) at leaf 7 -- the same adds in the same order as the TMEM merge.  With
+// two 64-register partials live, these steps read 16-column pieces.
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_pair_regs(uint32_t (&Q)[NC], uint32_t t0, uint32_t t1, int chalf) {
+  constexpr int W = 16;
+#pragma unroll
+  for (int c = 0; c < NC / W; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
+    uint32_t x[W], y[W];
+    tmem_ld16p(t0 + col, x);
+    tmem_ld16p(t1 + col, y);
+    tmem_ld_wait_only();
+    tmem_ld_tie16(x);
+    tmem_ld_tie16(y);
+#pragma unroll
+    for (int i = 0; i < W; ++i) Q[c * W + i] = f2u(__fadd_rn(u2f(x[i]), u2f(y[i])));
+  }
+}
+template <int EPI, int EPW, int NC>
+__device__ __forceinline__ void spine_last_regs(uint32_t (&S)[NC], const uint32_t (&Q)[NC], uint32_t tx, uint32_t ty,
+                                                int chalf) {
+  constexpr int W = 16;
+#pragma unroll
+  for (int c = 0; c < NC / W; ++c) {
+    const uint32_t col = static_cast<uint32_t>(spine_col<EPI, EPW>(chalf, c * W));
+    uint32_t x[W], y[W];
+    tmem_ld16p(tx + col, x);
+    tmem_ld16p(ty + col, y);
+    tmem_ld_wait_only();
+    tmem_ld_tie16(x);
+    tmem_ld_tie16(y);
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const float r = __fadd_rn(u2f(Q[c * W + i]), __fadd_rn(u2f(x[i]), u2f(y[i])));
       S[c * W + i] = f2u(__fadd_rn(u2f(S[c * W + i]), r));
     }
   }
@@ -433,8 +475,8 @@ __device__ __forceinline__ void release_tmem_buf(uint64_t* buf_free, int b, int 
 // normalise the A stages in place; registers rebalanced by setmaxnreg (epilogue 256, the rest
 // 120: 128 x 256 + 256 x 120 = 63,488 <= the launch's 384 x 168).
 // EPW: epilogue warps, 4 or 8 (8: single CTA, EPI_BF16 / EPI_SWIGLU, 12 warps; warp 4 + 4h + q
-// holds lane quarter q, column half h; setmaxnreg gives the 8 epilogue warps 200 registers and
-// warps 0-3 104: 256 x 200 + 128 x 104 = 64,512 = the launch's 384 x 168).
+// holds lane quarter q, column half h; setmaxnreg gives the 8 epilogue warps 224 registers and
+// warps 0-3 56: 256 x 224 + 128 x 56 = 64,512 = the launch's 384 x 168).
 // LS: whole-leaf stages for leaves of 96 k (GemmParams::leaf_stage; single CTA, bf16 roots,
 // 8 epilogue warps): tmA2 maps the A operand with 32-column boxes and a 64-byte swizzle.
 template <int EPI, bool PAIR, bool FUSED, int EPW, bool LS>
@@ -831,6 +873,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       for (int t = 0; t < U.n_tiles && ok; ++t) {
         const int n0 = (U.n_tile0 + t) * p.b_tile_cols;  // first output column of this tile
         uint32_t S[NC];  // the spine: the current group's partial root, at the end the tile's root
+        uint32_t Q[EPW == 8 ? NC : 1];  // 8 warps: leaves 4 + 5 of the group (spine_pair_regs)
         for (int l = 0; l < p.L; ++l, ++seq) {
           const int b = static_cast<int>(seq & 3u);
           const int lg = l & 7;  // this leaf's place in its group
@@ -868,17 +911,34 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
             release_tmem_buf<PAIR>(buf_free, b, lane);
           } else if (lg == 5) {
             const int b4 = static_cast<int>((seq - 1u) & 3u);
-            spine_merge<EPI, EPW, NC>(tbase + static_cast<uint32_t>(b4 * BN), tbase + static_cast<uint32_t>(b * BN), chalf);
-            tc_fence_before();
-            release_tmem_buf<PAIR>(buf_free, b4, lane);
+            if constexpr (EPW == 8) {
+              spine_pair_regs<EPI, EPW, NC>(Q, tbase + static_cast<uint32_t>(b4 * BN), tbase + static_cast<uint32_t>(b * BN),
+                                            chalf);
+              tc_fence_before();
+              release_tmem_buf<PAIR>(buf_free, b4, lane);
+              release_tmem_buf<PAIR>(buf_free, b, lane);
+            } else {
+              spine_merge<EPI, EPW, NC>(tbase + static_cast<uint32_t>(b4 * BN), tbase + static_cast<uint32_t>(b * BN),
+                                        chalf);
+              tc_fence_before();
+              release_tmem_buf<PAIR>(buf_free, b4, lane);
+            }
           } else if (lg == 7) {
             const int b5 = static_cast<int>((seq - 2u) & 3u), b6 = static_cast<int>((seq - 1u) & 3u);
-            spine_last<EPI, EPW>(S, tbase + static_cast<uint32_t>(b5 * BN), tbase + static_cast<uint32_t>(b6 * BN),
-                                 tbase + static_cast<uint32_t>(b * BN), chalf);
-            tc_fence_before();
-            release_tmem_buf<PAIR>(buf_free, b5, lane);
-            release_tmem_buf<PAIR>(buf_free, b6, lane);
-            release_tmem_buf<PAIR>(buf_free, b, lane);
+            if constexpr (EPW == 8) {
+              spine_last_regs<EPI, EPW, NC>(S, Q, tbase + static_cast<uint32_t>(b6 * BN), tbase + static_cast<uint32_t>(b * BN),
+                                            chalf);
+              tc_fence_before();
+              release_tmem_buf<PAIR>(buf_free, b6, lane);
+              release_tmem_buf<PAIR>(buf_free, b, lane);
+            } else {
+              spine_last<EPI, EPW>(S, tbase + static_cast<uint32_t>(b5 * BN), tbase + static_cast<uint32_t>(b6 * BN),
+                                   tbase + static_cast<uint32_t>(b * BN), chalf);
+              tc_fence_before();
+              release_tmem_buf<PAIR>(buf_free, b5, lane);
+              release_tmem_buf<PAIR>(buf_free, b6, lane);
+              release_tmem_buf<PAIR>(buf_free, b, lane);
+            }
           }
           if (spill && l == 7) {
             // 16 leaves: the root of leaves [0, 8) waits in shared memory ([column][row]) while

@@ -68,8 +68,8 @@ constexpr int LS_LEAF = 96;
 constexpr int LS_A2_OFF = BM * 64 * 2;            // the 32-column A box, after the 64-column one
 constexpr int LS_A_BYTES = BM * LS_LEAF * 2;      // 24 KB
 constexpr int LS_B_BYTES = LS_LEAF * BN * 2;      // 24 KB
-constexpr int GEMM_REGS_CONTROL_EPI8 = 104;   // setmaxnreg of warps 0-3 with 8 epilogue warps
-constexpr int GEMM_REGS_EPILOGUE_EPI8 = 200;  // and of warps 4-11
+constexpr int GEMM_REGS_CONTROL_EPI8 = 56;    // setmaxnreg of warps 0-3 with 8 epilogue warps
+constexpr int GEMM_REGS_EPILOGUE_EPI8 = 224;  // and of warps 4-11
 static_assert(128 * GEMM_REGS_CONTROL_EPI8 + 256 * GEMM_REGS_EPILOGUE_EPI8 <= 384 * 168,
               "register split within the launch's allocation");
 constexpr int GEMM_REGS_CONTROL_FUSED = 120;  // setmaxnreg of warps 0-3 and 8-11 (epilogue: 256)
