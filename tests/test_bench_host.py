@@ -22,8 +22,12 @@ def test_traffic_reported_only_for_the_captured_engine_source(tmp_path, monkeypa
     for f in bench.ENGINE_SOURCES:
         (src / f).write_bytes(open(os.path.join(real, f), "rb").read())
     assert bench.committed_traffic(key) == 123.0
+    # a comment or blank-line edit keeps it
+    orig = open(os.path.join(real, "gemm_tcgen05.cu"), "rb").read()
+    (src / "gemm_tcgen05.cu").write_bytes(orig + b"\n// a note\n\n/* and another */\n")
+    assert bench.committed_traffic(key) == 123.0
     # a changed engine source: the old figure is not reported
-    (src / "gemm_tcgen05.cu").write_bytes(open(os.path.join(real, "gemm_tcgen05.cu"), "rb").read() + b"\n// x\n")
+    (src / "gemm_tcgen05.cu").write_bytes(orig + b"\nstatic int x;\n")
     assert bench.committed_traffic(key) is None
     assert bench.committed_traffic("no such kernel") is None
 
