@@ -304,6 +304,7 @@ iso_status run_gemm_cluster(const void* A, int64_t lda, const void* B, int64_t l
   if (st != ISO_OK) return st;
   p.unit_mode = UNIT_CLUSTER;
   p.num_units = p.n_blocks * R;
+  p.b_stream = 1;
   p.out = C;
   p.ldo = ldc;
   trace("gemm[cluster leaf groups]", M, N, K, R);
@@ -330,6 +331,7 @@ iso_status run_gemm(int epi, const void* A, int64_t lda, const void* B, int64_t 
   p.unit_mode = UNIT_GEMM;
   p.num_units = p.m_blocks * p.n_blocks;
   p.group_m = raster_group(p, K);
+  p.b_stream = p.m_blocks == 1 ? 1 : 0;
   p.out = C;
   p.ldo = ldc;
   trace(epi == EPI_BF16 ? "gemm" : "gemm_partial", M, N, K, L);
@@ -431,6 +433,7 @@ iso_status iso_gemm_ws(const iso_contract* c, const iso_bf16* A, int64_t lda, co
   float* S_all = static_cast<float*>(ws);
   p.unit_mode = UNIT_LEAF_SPLIT;
   p.num_units = R * p.n_blocks;
+  p.b_stream = 1;
   p.out = S_all;
   p.ldo = N;
   p.out_group_stride = static_cast<int64_t>(M) * N;
@@ -550,6 +553,7 @@ static iso_status run_logprob_stats(const iso_contract* c, const iso_bf16* h, co
   p.num_chunks = tiles ? lp_num_tiles(Vl) : lp_num_chunks(Vl);  // statistics entries per row
   p.num_units = p.m_blocks * p.num_chunks;
   p.group_m = raster_group(p, H);  // row blocks whose hidden states share L2 (all of them up to ~48 MB)
+  p.b_stream = p.m_blocks == 1 ? 1 : 0;
   p.ids = ids;
   p.ws_stats = tiles ? tile_stats : chunk_stats;
   p.ws_zsel = zsel;

@@ -585,6 +585,7 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
       // The whole warp runs the loop (warp-uniform values); one elected lane issues.
       const bool leader = elect_one();
       const int rn = ring_n(me), rb = ring_base(me);
+      const uint64_t b_policy = l2_policy_evict_first();  // used when p.b_stream
       int slot = 0;
       int stage = rb;
       uint32_t round = 0;
@@ -631,8 +632,14 @@ __global__ void __launch_bounds__((FUSED || EPW == 8) ? 384 : GEMM_THREADS, 1)
                   tma_load_2d(sA, &tmA, &full_bar[stage], U.a_col0 + kx, U.a_row0);
                   if (LS)  // the leaf's last 32 columns, 64-byte swizzle
                     tma_load_2d(sA + LS_A2_OFF, &tmA2, &full_bar[stage], U.a_col0 + kx + 64, U.a_row0);
-                  tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
-                  tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
+                  if (p.b_stream) {
+                    tma_load_2d_hint(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx, b_policy);
+                    tma_load_2d_hint(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx,
+                                     b_policy);
+                  } else {
+                    tma_load_2d(sB, &tmB, &full_bar[stage], n0, U.b_row0 + kx);
+                    tma_load_2d(sB + BSTAGE / 2, &tmB, &full_bar[stage], n0 + p.b_box2_off, U.b_row0 + kx);
+                  }
                 }
               }
               __syncwarp();

@@ -152,6 +152,11 @@ struct GemmParams {
   // leaf, A as a 64-column box (128-byte swizzle) and a 32-column box (64-byte swizzle, second
   // tensor map), B as two 64-column x 96-row boxes; kb_per_leaf = 1
   int leaf_stage;
+  // 1: this launch reads each B element once (one row block: decode-size GEMMs and logprobs),
+  // so B loads carry an evict-first L2 policy and leave L2 to what is read again.  Measured on
+  // GB300: back-to-back one-row GEMMs 1-4 % faster; with many row blocks, whose B tiles are
+  // shared by a raster group, the same policy cost 2-5 %, so they keep the default.
+  int b_stream;
   const void* a_src;      // x, bf16
   int64_t lda_src;
   const float* a_rinv;    // [M] per-row 1 / sqrt(mean x^2 + eps)

@@ -83,6 +83,23 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// An L2 policy for data this launch reads once (createpolicy, evict-first for the whole
+// access), and a 2-D tiled load that carries it.  A cache hint changes only which lines L2
+// gives up first, never a value read.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], "
+      "[%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+
 // ------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs on neighbouring SMs (ranks 0 and 1) can run one
 // tcgen05.mma with M = 256: rank 0 issues it, each CTA supplies its own 128 A rows
