@@ -873,6 +873,16 @@ def profile_target(target: str, calls: int):
         o = torch.empty_like(Q)
         lse = torch.empty(Q.shape[0], ATT_HQ, dtype=torch.float32, device=dev)
         fn = lambda: B.attention(c, Q, K, V, qs, ks, p0, 1.0 / math.sqrt(ATT_D), max_q_rows=max(lens), out=o, lse=lse)
+    elif target == "attention_decode":  # one row per sequence of the rollout batch at its last position
+        import math
+        lens, Q, K, V, qs, ks, p0 = attention_workload(dev)
+        Qd = Q[(qs[1:] - 1).long()].contiguous()
+        del Q  # the packed queries are not needed for the decode rows
+        dq = torch.arange(len(lens) + 1, dtype=torch.int32, device=dev)
+        dpos = torch.tensor([L - 1 for L in lens], dtype=torch.int32, device=dev)
+        od = torch.empty_like(Qd)
+        ld = torch.empty(len(lens), ATT_HQ, dtype=torch.float32, device=dev)
+        fn = lambda: B.attention(c, Qd, K, V, dq, ks, dpos, 1.0 / math.sqrt(ATT_D), max_q_rows=1, out=od, lse=ld)
     elif target == "diagnostics":
         gen = torch.Generator().manual_seed(4)
         lens = torch.randint(1, 8193, (64,), generator=gen)
@@ -906,7 +916,7 @@ def main():
     ap.add_argument("--parallel", default="dp", choices=["dp", "tp"],
                     help="dp: data-parallel replicas (the default step); tp: row-parallel TP over K-leaves")
     ap.add_argument("--profile-target", choices=["gemm", "gemm_m1", "logprob", "moe", "rmsnorm", "attention",
-                                                     "attention_small", "diagnostics"],
+                                                     "attention_small", "diagnostics", "attention_decode"],
                     help="run one workload --steps times without timing (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_target:
