@@ -16,21 +16,25 @@
 //               vocab tile, folded left to right over the tiles of a vocab
 //               chunk with the two-block LSE merge [RL-Kernel blog, §4
 //               "Causal Chain: How Block Merge Order Alters LSE"; §7 "LogP"],
-//               plus the logit of the selected token.
+//               plus the logit of the selected token, or
+//   EPI_CLUSTER one row block split into leaf groups over a thread-block
+//               cluster: each CTA's group root meets the others' in
+//               distributed shared memory for the tree's top levels.
 //
 // A row's bits depend only on that row, the B columns and the contract: the
 // MMA instruction shape, the per-leaf chain and the tree are the same for
 // every M, every tile position and every schedule; nothing is split along K
 // beyond the contract's leaves and nothing uses atomics.
 //
-// Structure (one CTA per SM, persistent over work units):
+// Structure (one CTA per SM, persistent over work units; with PAIR two CTAs on
+// neighbouring SMs run M = 256 MMAs over both, each holding 128 A rows and half of B):
 //   warps 0,3 TMA producers, one elected lane each (warp 0 the stages of the even
 //             leaves, warp 3 those of the odd leaves): A tile 128x64 (K-major)
 //             and B tile 64x128 (MN-major, two 64-column boxes), 128-byte
-//             swizzle, 6-stage ring.
+//             swizzle, as many stages as shared memory holds (up to 12).
 //   warps 1-2 MMA issuers, one elected lane each: warp 1 issues the even leaves and
-//             warp 2 the odd leaves of every leaf pair (one thread cannot issue
-//             128x128x16 MMAs as fast as the tensor core retires them); warp 1
+//             warp 2 the odd leaves of every leaf pair, so one leaf's waits
+//             overlap the other's MMAs (a single issuer measured slower); warp 1
 //             also owns the TMEM allocation.
 //   warps 4-7 epilogue: one thread per accumulator row (TMEM lane); they read
 //             each finished leaf once (tcgen05.ld) and run the tree in registers
