@@ -42,6 +42,8 @@
 #include <cuda_bf16.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "iso_internal.h"
 #include "iso_ptx.cuh"
 
@@ -538,14 +540,15 @@ extern "C" iso_status iso_attention(const iso_contract* c, const iso_bf16* Q, co
   p.lse = lse;
   p.status = device_status_ptr();
   p.timeout_ns = wait_timeout_ns();
-  static int attr_dev = -1;
+  // the shared-memory attribute, once per device (concurrent first calls set the same value)
+  static std::atomic<bool> attr_set[ISO_MAX_DEVICES] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
-  if (attr_dev != dev) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ISO_MAX_DEVICES) return ISO_ERR_CUDA;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(iso_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM) !=
         cudaSuccess)
       return ISO_ERR_CUDA;
-    attr_dev = dev;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const dim3 grid(Hq / gp, B, pairs);
   iso_attention_kernel<<<grid, AT_THREADS, AT_SMEM, static_cast<cudaStream_t>(stream)>>>(tQ, tK, tV, p);

@@ -4,6 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "iso_elementwise.h"
@@ -16,10 +17,12 @@ namespace iso {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = ISO_MAX_DEVICES;
+// Filled once per device under g_mu; read without the lock (acquire / release), so threads that
+// launch on different devices at once see either nothing or the complete entry.
 std::mutex g_mu;
-unsigned int* g_status_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices] = {};
+std::atomic<int> g_sm_count[kMaxDevices] = {};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -35,17 +38,17 @@ int current_device() {
 bool ensure_device_state() {
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return false;
-  if (g_status_ptr[d] && g_sm_count[d]) return true;
+  if (g_status_ptr[d].load(std::memory_order_acquire) && g_sm_count[d].load(std::memory_order_acquire)) return true;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[d]) {
+  if (!g_status_ptr[d].load(std::memory_order_relaxed)) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_iso_status_word) != cudaSuccess) return false;
-    g_status_ptr[d] = static_cast<unsigned int*>(p);
+    g_status_ptr[d].store(static_cast<unsigned int*>(p), std::memory_order_release);
   }
-  if (!g_sm_count[d]) {
+  if (!g_sm_count[d].load(std::memory_order_relaxed)) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return false;
-    g_sm_count[d] = n;
+    g_sm_count[d].store(n, std::memory_order_release);
   }
   return true;
 }
@@ -67,13 +70,13 @@ bool device_ready() { return ensure_device_state(); }
 unsigned int* device_status_ptr() {
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return nullptr;
-  return g_status_ptr[d];
+  return g_status_ptr[d].load(std::memory_order_acquire);
 }
 
 int sm_count() {
   const int d = current_device();
-  if (d < 0 || d >= kMaxDevices || !g_sm_count[d]) return 148;
-  return g_sm_count[d];
+  const int n = (d < 0 || d >= kMaxDevices) ? 0 : g_sm_count[d].load(std::memory_order_acquire);
+  return n ? n : 148;
 }
 
 uint64_t wait_timeout_ns() {

@@ -48,6 +48,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "iso_internal.h"
@@ -1209,12 +1210,14 @@ template <int EPI, bool PAIR, bool FUSED = false, int EPW = 4, bool LS = false>
 iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_units,
                       cudaStream_t s, const CUtensorMap& tmA2) {
   constexpr int kThreads = FUSED ? GEMM_THREADS_FUSED : (EPW == 8 ? GEMM_THREADS_EPI8 : GEMM_THREADS);
-  static int attr_dev = -1;  // device whose function attributes are set
-  static int slots = 0;      // CTAs (pairs: clusters) resident at once on that device
+  // Per device, once: the function attributes, and the CTAs (pairs: clusters) resident at once.
+  // 0 = not yet; threads that get there together repeat the same idempotent setup.
+  static std::atomic<int> slots_by_dev[ISO_MAX_DEVICES] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ISO_MAX_DEVICES) return ISO_ERR_CUDA;
   auto kern = iso_leaf_tree_gemm_kernel<EPI, PAIR, FUSED, EPW, LS>;
-  if (attr_dev != dev) {
+  int slots = slots_by_dev[dev].load(std::memory_order_acquire);
+  if (slots == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES) != cudaSuccess)
       return ISO_ERR_CUDA;
     slots = sm_count();
@@ -1236,7 +1239,7 @@ iso_status launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
       if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return ISO_ERR_CUDA;
       slots = clusters;
     }
-    attr_dev = dev;
+    slots_by_dev[dev].store(slots, std::memory_order_release);
     const char* tr = getenv("ISO_TRACE");
     if (tr && tr[0] == '1')
       fprintf(stderr, "[iso] gemm kernel epi=%d pair=%d epilogue warps=%d: %d %s resident\n", EPI, PAIR ? 1 : 0,

@@ -53,6 +53,8 @@ constexpr int PAIR_BK = 128;
 constexpr int GEMM_BARRIER_BYTES = 512;
 constexpr int NUM_TMEM_BUFS = 4;  // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int TMEM_COLS = 512;
+// Per-device host caches (status word, SM count, kernel attributes) hold this many devices.
+constexpr int ISO_MAX_DEVICES = 64;
 constexpr int GEMM_THREADS = 256;  // warps 0,3 TMA; warps 1-2 MMA (even/odd leaves); warps 4..7 epilogue
 constexpr int GEMM_THREADS_FUSED = 384;      // + warps 8..11: the fused RMSNorm prologue
 // Short leaves: the tree steps and the root of a tile outlast its MMAs, so warps 8..11 join
