@@ -29,9 +29,11 @@
  *   - Alignment: device pointers 16-byte aligned; leading dimensions of bf16
  *     matrices multiples of 8 elements, of fp32 matrices multiples of 4.
  *   - Per-device state (the status word's address, the SM count, the static
- *     scratch's address) is looked up on a device's first call and kept for
- *     the life of the process: the library must not be used across a
- *     cudaDeviceReset of a device it has already run on.
+ *     scratch's address, kernel attributes) is looked up on a device's first
+ *     call and kept for the life of the process: the library must not be used
+ *     across a cudaDeviceReset of a device it has already run on.  Device
+ *     ordinals 0-63 are served; host threads may call concurrently, on the
+ *     same or different devices.
  */
 #ifndef ISO_H_
 #define ISO_H_
